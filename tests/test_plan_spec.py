@@ -1,0 +1,98 @@
+"""Invariants of the written split-KV plan specification (oracle/plan_spec.py).
+
+The chunking constants are design choices with no counterpart on the pages;
+these tests pin the specification against the properties it promises.
+"""
+
+import math
+import random
+
+import pytest
+
+from oracle.plan_spec import plan_spec
+
+
+def _cases():
+    rnd = random.Random(11)
+    out = []
+    for _ in range(60):
+        B = rnd.randint(1, 40)
+        Hkv = rnd.choice([1, 2, 4, 8])
+        ps = rnd.choice([16, 32])
+        ql = [rnd.randint(1, 6) for _ in range(B)]
+        kv = [max(ql[b], rnd.randint(1, 20000)) for b in range(B)]
+        if rnd.random() < 0.3:
+            kv[0] = 131072
+        W = rnd.choice([-1, -1, 0, 5, 4095])
+        out.append((kv, ql, 8 * Hkv, Hkv, ps, W, rnd.choice([4, 152]), rnd.choice([1, 2, 4]),
+                    256, rnd.random() < 0.8))
+    return out
+
+
+@pytest.mark.parametrize("case", _cases())
+def test_plan_covers_every_visited_page_once(case):
+    kv, ql, Hq, Hkv, ps, W, sms, waves, mct, frozen = case
+    p = plan_spec(kv, ql, Hq, Hkv, 128, ps, W, sms, waves, mct, frozen)
+    B = len(kv)
+    covered = {}
+    for (b, hk, ci, lo, hi) in p["items"]:
+        assert lo < hi
+        covered.setdefault((b, hk), []).append((ci, lo, hi))
+    for b in range(B):
+        n, L = kv[b], ql[b]
+        first_key = max(0, n - L - W) if (W >= 0 and frozen) else 0
+        want = list(range(first_key // ps, math.ceil(n / ps)))
+        for hk in range(Hkv):
+            ch = sorted(covered[(b, hk)])
+            assert [c for c, _, _ in ch] == list(range(p["n_chunks"][b]))
+            pages = [pg for _, lo, hi in ch for pg in range(lo, hi)]
+            assert pages == want
+            assert all(hi - lo <= p["chunk_pages"] for _, lo, hi in ch)
+
+
+@pytest.mark.parametrize("case", _cases())
+def test_plan_chunk_is_minimal_under_the_target(case):
+    kv, ql, Hq, Hkv, ps, W, sms, waves, mct, frozen = case
+    p = plan_spec(kv, ql, Hq, Hkv, 128, ps, W, sms, waves, mct, frozen)
+    B, T = len(kv), waves * sms
+    npg = [hi - lo for lo, hi in zip(p["page_lo"], p["page_hi"])]
+    c = p["chunk_pages"]
+    if B * Hkv >= T:
+        assert c == max(npg) and all(x == 1 for x in p["n_chunks"])
+        return
+    items = Hkv * sum(math.ceil(x / c) for x in npg)
+    assert items == len(p["items"]) and items <= T
+    c_lo = min(math.ceil(mct / ps), max(npg))
+    assert c >= c_lo
+    if c > c_lo:
+        assert Hkv * sum(math.ceil(x / (c - 1)) for x in npg) > T
+
+
+@pytest.mark.parametrize("case", _cases()[:20])
+def test_plan_order_partials_and_workspace(case):
+    kv, ql, Hq, Hkv, ps, W, sms, waves, mct, frozen = case
+    p = plan_spec(kv, ql, Hq, Hkv, 128, ps, W, sms, waves, mct, frozen)
+    npg = [hi - lo for lo, hi in zip(p["page_lo"], p["page_hi"])]
+    seq = [it[0] for it in p["items"]]
+    firsts = list(dict.fromkeys(seq))
+    assert firsts == p["order"]
+    assert all(npg[a] >= npg[b] for a, b in zip(firsts, firsts[1:]))
+    rows = 0
+    for b in range(len(kv)):
+        if p["n_chunks"][b] > 1:
+            assert p["part_base"][b] == rows
+            rows += p["n_chunks"][b] * ql[b] * Hq
+        else:
+            assert p["part_base"][b] == -1
+    assert p["partial_rows"] == rows
+    if rows:
+        assert p["workspace_bytes"] == math.ceil(rows * 128 * 4 / 256) * 256 + rows * 4
+    else:
+        assert p["workspace_bytes"] == 0
+
+
+def test_plan_skewed_long_request_is_split():
+    kv = [131072] + [2048] * 15
+    p = plan_spec(kv, [1] * 16, 64, 8, 128, 32, -1, 152, 2, 256)
+    assert p["n_chunks"][0] > 1 and p["order"][0] == 0
+    assert len(p["items"]) <= 2 * 152
