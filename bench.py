@@ -1,0 +1,477 @@
+"""Benchmark: paged decode effective KV HBM GB/s (and % of peak), prefill TFLOP/s.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line.  The headline `value` is the effective KV bandwidth of
+paged_decode_run on the Llama-3-8B-shaped decode workload (B=64, Hq=32,
+Hkv=8, D=128, page_size=16, kv_len U[512, 8192], 40K-page shuffled pool):
+algorithmic K+V bytes of the visited tokens / device time per call, with the
+inputs resident in HBM (each call reads ~1.1 GB, far more than the 129 MB L2,
+so no flush is needed).  The other decode workloads and the ragged prefill are
+measured in the same run and reported as sub-objects.
+
+Under torchrun (N > 1) every rank decodes its own batch of the same shape
+(weak scaling, no collective on the data path); `value` sums the bytes of all
+ranks over the slowest rank's time.
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "llama3_8b"
+METRIC = "paged decode effective KV HBM GB/s"
+UNIT = "GB/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kv_bytes(inp):
+    """Algorithmic K+V bytes of one decode call: every visited key of every
+    request, once per KV head, K and V, bf16 (window-trimmed, not page-rounded)."""
+    seq = inp["seq_lens_kv"].cpu().tolist()
+    if inp["qo_indptr"] is not None:
+        ind = inp["qo_indptr"].cpu().tolist()
+        qls = [ind[i + 1] - ind[i] for i in range(len(seq))]
+    else:
+        qls = [inp["q_len"]] * len(seq)
+    W = inp["window_left"]
+    D = inp["q"].shape[2]
+    keys = 0
+    for n, L in zip(seq, qls):
+        first = max(0, n - L - W) if W >= 0 else 0
+        keys += n - first
+    return keys * inp["num_kv_heads"] * D * 2 * 2, keys
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline leg and the --impl reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_task(task):
+    """Run the fp64 oracle for one request in a worker process; return seconds."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import oracle
+    (q_bits, k_bits, v_bits, table, seq, L, Hkv, ps, causal, W, sinks) = task
+    t0 = time.perf_counter()
+    oracle.paged_decode_request(0, q_bits, k_bits, v_bits, table[None], seq, 0, L, Hkv, ps,
+                                causal=causal, window_left=W, sinks=sinks)
+    return time.perf_counter() - t0
+
+
+def oracle_sample_tasks(inp, n_requests):
+    """Per-request oracle inputs (only the pages each request uses) for a sample."""
+    import numpy as np
+    import torch
+    from paged_kv_attention_32_gb300 import workloads as wl
+    seq = inp["seq_lens_kv"].cpu().numpy()
+    bt = inp["block_tables"].cpu().numpy()
+    ps = inp["page_size"]
+    ind = (inp["qo_indptr"].cpu().numpy() if inp["qo_indptr"] is not None
+           else np.arange(len(seq) + 1) * inp["q_len"])
+    sinks = inp["sinks"].cpu().double().numpy() if inp["sinks"] is not None else None
+    tasks, nbytes = [], 0
+    D = inp["q"].shape[2]
+    for b in range(min(n_requests, len(seq))):
+        n, L = int(seq[b]), int(ind[b + 1] - ind[b])
+        npg = -(-n // ps)
+        ids = torch.as_tensor(bt[b, :npg].astype(np.int64), device=inp["k_pages"].device)
+        kb = wl.bf16_bits(inp["k_pages"].index_select(0, ids))
+        vb = wl.bf16_bits(inp["v_pages"].index_select(0, ids))
+        qb = wl.bf16_bits(inp["q"][int(ind[b]):int(ind[b + 1])])
+        W = inp["window_left"]
+        first = max(0, n - L - W) if W >= 0 else 0
+        nbytes += (n - first) * inp["num_kv_heads"] * D * 4
+        tasks.append((qb, kb, vb, np.arange(npg, dtype=np.int64), np.array([n]), L,
+                      inp["num_kv_heads"], ps, inp["causal"], W, sinks))
+    return tasks, nbytes
+
+
+def run_oracle_sample(tasks, cores):
+    """Oracle over the sample on `cores` spawned worker processes.  Returns the
+    makespan (max over workers of their summed compute seconds)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+    with ctx.Pool(cores) as pool:
+        secs = pool.map(_oracle_task, tasks, chunksize=1)
+    loads = [0.0] * cores
+    for s in sorted(secs, reverse=True):        # longest-first packing onto the cores
+        i = loads.index(min(loads))
+        loads[i] += s
+    return max(loads)
+
+
+def cpu_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+# GPU measurements
+# ---------------------------------------------------------------------------
+
+def make_plan(inp, **kw):
+    from paged_kv_attention_32_gb300 import api
+    args = dict(num_qo_heads=inp["q"].shape[1], num_kv_heads=inp["num_kv_heads"],
+                page_size=inp["page_size"], max_pages_per_seq=inp["block_tables"].shape[1],
+                num_pages=inp["k_pages"].shape[0], causal=inp["causal"],
+                window_left=inp["window_left"], return_lse=inp["return_lse"],
+                bmm2_scale=inp["bmm2_scale"])
+    if inp["qo_indptr"] is not None:
+        args["qo_indptr"] = inp["qo_indptr"].cpu()
+    else:
+        args["q_len"] = inp["q_len"]
+    args.update(kw)
+    return api.paged_decode_plan(inp["seq_lens_kv"].cpu(), **args)
+
+
+def decode_buffers(inp, plan):
+    import torch
+    q = inp["q"]
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=q.device)
+    return out, lse, ws
+
+
+def time_decode(inp, plan, steps, warmup, dist=None):
+    """Device time per paged_decode_run call (CUDA events on the launching stream)."""
+    import torch
+    from paged_kv_attention_32_gb300 import api
+    out, lse, ws = decode_buffers(inp, plan)
+    stream = torch.cuda.current_stream()
+    args = (plan, inp["q"], inp["k_pages"], inp["v_pages"], inp["block_tables"])
+    kw = dict(seq_lens_kv=inp["seq_lens_kv"], sinks=inp["sinks"], out=out, lse=lse, workspace=ws,
+              stream=stream)
+    for _ in range(warmup):
+        api.paged_decode_run(*args, **kw)
+    torch.cuda.synchronize()
+    plan.check()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        api.paged_decode_run(*args, **kw)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    plan.check()
+    return e0.elapsed_time(e1) / steps     # ms per call
+
+
+def time_decode_e2e(inp, plan_kw, steps, warmup):
+    """The user-facing call sequence with host buffers, wall clock per step:
+    pinned host q / block_tables / seq_lens -> device, host planning on the
+    lengths, paged_decode_run, device -> pinned host read of O (and LSE).
+    The KV pools are the cache: they stay resident on the device."""
+    import torch
+    from paged_kv_attention_32_gb300 import api
+    dev = inp["q"].device
+    h_q = inp["q"].cpu().pin_memory()
+    h_bt = inp["block_tables"].cpu().pin_memory()
+    h_seq = inp["seq_lens_kv"].cpu().pin_memory()
+    h_ind = inp["qo_indptr"].cpu().pin_memory() if inp["qo_indptr"] is not None else None
+    d_q = torch.empty_like(inp["q"])
+    d_bt = torch.empty_like(inp["block_tables"])
+    d_seq = torch.empty_like(inp["seq_lens_kv"])
+    h_out = torch.empty(inp["q"].shape, dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(inp["q"].shape[:2], dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    bytes_in = (h_q.numel() * 2 + h_bt.numel() * 4 + h_seq.numel() * 4)
+    bytes_out = h_out.numel() * 2 + (h_lse.numel() * 4 if inp["return_lse"] else 0)
+
+    def step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_seq.copy_(h_seq, non_blocking=True)
+        kw = dict(plan_kw)
+        if h_ind is not None:
+            kw["qo_indptr"] = h_ind
+        p = api.paged_decode_plan(h_seq, stream=stream, **kw)
+        r = api.paged_decode_run(p, d_q, inp["k_pages"], inp["v_pages"], d_bt,
+                                 seq_lens_kv=d_seq, sinks=inp["sinks"], stream=stream)
+        o = r[0] if isinstance(r, tuple) else r
+        h_out.copy_(o, non_blocking=True)
+        if inp["return_lse"]:
+            h_lse.copy_(r[1], non_blocking=True)
+        stream.synchronize()
+        return p
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    return (time.perf_counter() - t0) * 1e3 / steps, bytes_in, bytes_out
+
+
+def measure_workload(name, seed, steps, warmup, peak_gbs, dist=None):
+    """Inputs drawn on the GPU, plan, device timing; returns (result dict, inp, plan)."""
+    from paged_kv_attention_32_gb300 import workloads as wl
+    w = wl.DECODE_WORKLOADS[name]
+    inp = wl.make_decode_inputs(w, seed=seed, device="cuda")
+    plan = make_plan(inp)
+    ms = time_decode(inp, plan, steps, warmup, dist)
+    nbytes, keys = kv_bytes(inp)
+    info = plan.info
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res = {"workload": w.name, "ms_per_call": round(ms, 5), "kv_bytes": nbytes,
+           "kv_tokens": keys, "GB_per_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak_gbs, 4),
+           "kernel": ["cuda_core", "mma"][info["kernel"]], "ctas": info["num_items"],
+           "split_requests": info["num_split"], "launches_per_call": 1 + (info["num_split"] > 0)}
+    return res, inp, plan
+
+
+def measure_prefill(seed, steps, warmup, peak_tflops):
+    import torch
+    from paged_kv_attention_32_gb300 import api
+    from paged_kv_attention_32_gb300 import workloads as wl
+    w = wl.RAGGED_PREFILL
+    inp = wl.make_prefill_inputs(w, seed=seed, device="cuda")
+    lens = inp["lens"].tolist()
+    pairs = sum(n * (n + 1) // 2 for n in lens)
+    flops = 4 * 128 * pairs * w.num_qo_heads
+    try:
+        plan = api.batch_prefill_plan(inp["qo_indptr"].cpu(), inp["kv_indptr"].cpu(),
+                                      num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads)
+        out = torch.empty_like(inp["q"])
+        for _ in range(warmup):
+            api.batch_prefill_run(plan, inp["q"], inp["k"], inp["v"], out=out)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            api.batch_prefill_run(plan, inp["q"], inp["k"], inp["v"], out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        plan.check()
+        ms = e0.elapsed_time(e1) / steps
+    except Exception as exc:   # reported, not hidden: the line says why there is no number
+        return {"workload": w.name, "status": f"not measured: {exc}", "flops": flops}
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "ms_per_call": round(ms, 4), "flops": flops,
+            "TFLOP_per_s": round(tf, 1), "frac_of_measured_bf16": round(tf / peak_tflops, 4),
+            "tiles": plan.num_tiles}
+
+
+def cpu_baseline(inp, n_requests):
+    tasks, nbytes = oracle_sample_tasks(inp, n_requests)
+    cores = cpu_cores()
+    secs = run_oracle_sample(tasks, min(cores, len(tasks)))
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": min(cores, len(tasks)),
+            "kind": "oracle",
+            "sample": f"fp64 oracle on the first {len(tasks)} requests of the same batch "
+                      f"({nbytes / 1e6:.0f} MB of K+V), one spawned process per core, "
+                      f"{secs:.1f} s makespan"}
+
+
+def emit(line):
+    print(json.dumps(line), flush=True)
+
+
+def reference_arm(args, rank):
+    """--impl reference: the fp64 CPU oracle timed on the host cores."""
+    if rank != 0:
+        return
+    from paged_kv_attention_32_gb300 import workloads as wl
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = wl.make_decode_inputs(wl.DECODE_WORKLOADS[HEADLINE], seed=args.seed, device=dev)
+    tasks, nbytes = oracle_sample_tasks(inp, 8)
+    cores = min(cpu_cores(), len(tasks))
+    for _ in range(min(args.warmup, 1)):
+        run_oracle_sample(tasks[:cores], cores)
+    secs = [run_oracle_sample(tasks, cores) for _ in range(args.steps)]
+    total = sum(secs)
+    value = nbytes * args.steps / total / 1e9
+    cpu = {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"fp64 oracle, first {len(tasks)} requests of the "
+                     f"{wl.DECODE_WORKLOADS[HEADLINE].name} batch per step"}
+    emit({"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+          "ms_per_step": round(total * 1e3 / args.steps, 2), "higher_is_better": True,
+          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+          "config": {"workload": wl.DECODE_WORKLOADS[HEADLINE].name},
+          "cpu_baseline": cpu,
+          "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}})
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the CUDA path (no CPU fallback)")
+    torch.cuda.set_device(local)
+    peak_gbs, peak_tf, peak_kind = measured_peaks()
+
+    # ---- headline: Llama-3-8B-shaped decode ----
+    with ClockSampler(local) as clk:
+        head, inp, plan = measure_workload(HEADLINE, args.seed + rank, args.steps, args.warmup,
+                                           peak_gbs, dist)
+    clocks = clk.summary()
+    ms = head["ms_per_call"]
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    total_bytes = head["kv_bytes"] * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+    gbs_kernel = head["kv_bytes"] / (head["ms_per_call"] * 1e-3) / 1e9
+
+    line = None
+    if rank == 0:
+        from paged_kv_attention_32_gb300 import workloads as wl
+        w = wl.DECODE_WORKLOADS[HEADLINE]
+        plan_kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
+                       page_size=w.page_size, max_pages_per_seq=inp["block_tables"].shape[1],
+                       num_pages=inp["k_pages"].shape[0], return_lse=w.return_lse, q_len=1)
+        e2e_ms, bin_, bout = time_decode_e2e(inp, plan_kw, min(args.steps, 10),
+                                             max(3, min(args.warmup, 3)))
+        e2e_val = head["kv_bytes"] * world / (e2e_ms * 1e-3) / 1e9
+        cpu = cpu_baseline(inp, 16) if world == 1 else None
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                       "page_size": w.page_size, "kv_tokens": head["kv_tokens"],
+                       "kv_bytes_per_call": head["kv_bytes"],
+                       "l2": "inputs larger than L2 (each call reads >1 GB of K/V; no flush)",
+                       "parallelism": f"replicas x{world} (one batch per GPU)"},
+            "roofline": {"bound": "hbm", "kernel": f"decode_{head['kernel']}_kernel",
+                         "achieved": round(gbs_kernel, 1), "peak": peak_gbs, "unit": "GB/s",
+                         "frac": round(gbs_kernel / peak_gbs, 4), "peak_source": peak_kind,
+                         "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+                    "h2d_bytes_per_step": bin_, "d2h_bytes_per_step": bout,
+                    "note": "host planning + pinned H2D of q/tables/lengths + run + D2H of O; "
+                            "the KV cache stays resident"},
+            "gpu_launches": args.steps * head["launches_per_call"],
+            "clocks": clocks,
+        }
+    del inp, plan
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_extra:
+        extra = {}
+        for name in ("skewed", "spec"):
+            r, i2, p2 = measure_workload(name, args.seed, max(5, args.steps // 2),
+                                         max(3, args.warmup), peak_gbs)
+            extra[name] = r
+            del i2, p2
+            torch.cuda.empty_cache()
+        extra["prefill"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf)
+        line["decode_headline"] = head
+        line["other_workloads"] = extra
+    if rank == 0:
+        emit(line)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

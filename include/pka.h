@@ -1,0 +1,356 @@
+/*
+ * pka.h -- C ABI of the GB300 (sm_103a) paged-KV attention library.
+ *
+ * Operations (FlashInfer API documentation pages they follow):
+ *   paged_decode_plan / paged_decode_run
+ *       batched decode attention over a paged KV cache:
+ *       "flashinfer.attention.prims_ts.batch_decode_with_paged_kv_cache"
+ *       (plan-before-capture, fixed or packed query, mask_type, window_left,
+ *       bmm1_scale / bmm2_scale) and
+ *       "flashinfer.cudnn.cudnn_batch_decode_with_kv_cache"
+ *       (HND k_cache / v_cache, q_len_per_req causal rows, sinks, the base-2
+ *       LSE of the Note "LSE convention").
+ *   attn_merge_lse
+ *       merge of partial attention states by base-2 LSE (the "cascade-merge"
+ *       input named in the LSE convention of cudnn_batch_decode_with_kv_cache).
+ *   batch_prefill_plan / batch_prefill_run
+ *       packed ragged causal context attention:
+ *       "flashinfer.attention.prims_ts.batch_prefill".
+ *   paged_kv_gather
+ *       test hook: copies paged K or V rows to a dense buffer through the same
+ *       page addressing the decode kernels use.
+ *
+ * Conventions shared by every entry point
+ *   - Return value: PKA_OK (0) or a negative PKA_ERR_* code.  The message of
+ *     the last error on the calling thread is returned by pka_last_error().
+ *   - All arguments are checked on the host before anything is launched; an
+ *     invalid argument launches nothing.  No kernel traps or asserts.
+ *   - Device pointers are raw CUDA device addresses of the current device.
+ *     `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   - Element strides are in elements, not bytes.
+ *   - Only bf16 (PKA_DTYPE_BF16) q/K/V/out are supported; f16 returns
+ *     PKA_ERR_UNSUPPORTED.  head_dim must be 128.
+ *   - The caller owns every device buffer (q, pools, tables, lengths, out,
+ *     lse, workspace).  The library owns only the opaque plan objects.
+ *   - *_run entry points allocate nothing, never synchronise and never read
+ *     device memory on the host, so they may be captured in a CUDA graph.
+ *     Plans must be created before capture.
+ */
+#ifndef PKA_H
+#define PKA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define PKA_OK 0
+#define PKA_ERR_INVALID_ARG (-1)          /* a shape, length or pointer check failed   */
+#define PKA_ERR_UNSUPPORTED (-2)          /* valid on the pages, not built here        */
+#define PKA_ERR_WORKSPACE_TOO_SMALL (-3)  /* workspace_bytes below the plan's need     */
+#define PKA_ERR_CUDA (-4)                 /* a CUDA runtime/driver call failed         */
+#define PKA_ERR_DEVICE_BOUNDS (-5)        /* reserved: device-side bounds report       */
+#define PKA_ERR_DEVICE_TIMEOUT (-6)       /* a kernel gave up on a bounded wait        */
+
+/* ---- enums ------------------------------------------------------------- */
+#define PKA_DTYPE_BF16 0
+#define PKA_DTYPE_F16 1
+#define PKA_DTYPE_F32 2
+
+#define PKA_MASK_DENSE 0   /* mask_type 'dense': only padding is masked            */
+#define PKA_MASK_CAUSAL 1  /* mask_type 'causal': bottom-right aligned diagonal     */
+
+#define PKA_PLAN_HOST_ONLY 1  /* build the plan on the host only (no device copy);
+                                 such a plan can be inspected but not run        */
+
+#define PKA_KERNEL_CUDA_CORE 0  /* decode kernel on CUDA cores (FFMA2 + shuffles) */
+#define PKA_KERNEL_MMA 1        /* decode kernel on tensor cores (mma m16n8k16)   */
+
+/* Message of the last error raised on the calling thread ("" if none). */
+const char* pka_last_error(void);
+
+/* Library version string. */
+const char* pka_version(void);
+
+/* ======================================================================== */
+/* Paged decode                                                              */
+/* ======================================================================== */
+
+/*
+ * Problem description for a decode plan.
+ *
+ * batch_size         B, number of requests.
+ * num_qo_heads       Hq.  num_kv_heads Hkv.  Hq % Hkv == 0 is required
+ *                    (GQA/MQA: query head h reads KV head h / (Hq/Hkv);
+ *                    cudnn_batch_decode_with_kv_cache, Note).
+ * head_dim           D; must be 128.
+ * page_size          tokens per page: a multiple of 16 in [16, 256].
+ * max_pages_per_seq  C, the number of entries in each block_tables row.
+ * num_pages          pages in each of the K and V pools.
+ * dtype              PKA_DTYPE_BF16.
+ * q_len              fixed query rows per request, used when the plan gets no
+ *                    qo_indptr (batch_decode_with_paged_kv_cache, seq_len_q).
+ * max_q_len          packed mode: per-request capacity (0 = derive from
+ *                    qo_indptr); fixed mode: 0 or equal to q_len, anything
+ *                    else is PKA_ERR_INVALID_ARG (same page, max_seq_len_q).
+ * mask               PKA_MASK_DENSE or PKA_MASK_CAUSAL.  Causal row i of a
+ *                    request with L rows and n keys sees keys 0 .. n-L+i
+ *                    (cudnn_batch_decode_with_kv_cache, q_len_per_req).
+ * window_left        -1 disables; W >= 0 keeps the W keys before the row's
+ *                    diagonal position n-L+i plus that position
+ *                    (same page, window_left).  With mask DENSE the window is
+ *                    anchored at the same diagonal position.
+ * scale              softmax scale on q.k; NaN selects 1/sqrt(D)
+ *                    (bmm1_scale / scale).
+ * bmm2_scale         multiplies O (not the LSE).
+ * return_lse         nonzero: paged_decode_run writes the base-2 LSE.
+ * freeze_seq_lens    nonzero: the plan keeps the host lengths and run ignores
+ *                    its seq_lens_kv_dev argument.  Zero: run reads the live
+ *                    lengths from seq_lens_kv_dev; each must be >= its q_len
+ *                    and <= the length the plan saw (lengths above that are
+ *                    clamped to it), and the window start is then found at
+ *                    run time (batch_decode_with_paged_kv_cache, planner note:
+ *                    "bind a stable runtime seq_lens tensor or let the plan
+ *                    retain fixed sequence lengths").
+ * num_sms            SM count the planner balances for; 0 = the device's.
+ * split_waves        target CTAs = split_waves * num_sms; 0 = default (4).
+ * min_chunk_tokens   smallest split chunk in tokens; 0 = default (256).
+ * mma_min_rows       the tensor-core kernel is used when
+ *                    (Hq/Hkv) * max_q_len >= mma_min_rows; 0 = default (16).
+ * flags              PKA_PLAN_HOST_ONLY or 0.
+ */
+typedef struct pka_decode_desc {
+  int32_t batch_size;
+  int32_t num_qo_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t max_pages_per_seq;
+  int64_t num_pages;
+  int32_t dtype;
+  int32_t q_len;
+  int32_t max_q_len;
+  int32_t mask;
+  int32_t window_left;
+  float scale;
+  float bmm2_scale;
+  int32_t return_lse;
+  int32_t freeze_seq_lens;
+  int32_t num_sms;
+  int32_t split_waves;
+  int32_t min_chunk_tokens;
+  int32_t mma_min_rows;
+  int32_t flags;
+} pka_decode_desc;
+
+typedef struct pka_plan pka_plan; /* opaque decode plan */
+
+/* Summary of a decode plan. */
+typedef struct pka_plan_info {
+  int32_t num_items;        /* work items = CTAs of the decode kernel              */
+  int32_t chunk_pages;      /* split chunk length in pages                          */
+  int32_t num_split;        /* requests cut into more than one chunk                */
+  int32_t partial_rows;     /* fp32 partial rows in the workspace                   */
+  int64_t workspace_bytes;  /* bytes paged_decode_run needs in `workspace`          */
+  int32_t kernel;           /* PKA_KERNEL_CUDA_CORE or PKA_KERNEL_MMA               */
+  int32_t rows_per_cta;     /* query rows a CTA holds: (Hq/Hkv) * max_q_len         */
+  int32_t num_sms;          /* SM count the plan balanced for                       */
+  int32_t split_waves;
+  int32_t min_chunk_tokens;
+  int32_t total_q;          /* query rows in the batch                              */
+} pka_plan_info;
+
+/*
+ * Build a decode plan from host copies of the lengths.
+ *
+ * seq_lens_kv_host  [B] int32 host array, 1 <= kv_len <= C*page_size and
+ *                   kv_len >= the request's q_len (cudnn_batch_decode_with_kv_cache,
+ *                   q_len_per_req: "Every request needs kv_len >= q_len").
+ * qo_indptr_host    NULL (fixed q_len) or [B+1] int32 host array, cumulative
+ *                   query offsets starting at 0, every q_len >= 1 (packed mode,
+ *                   batch_decode_with_paged_kv_cache, qo_indptr).
+ * workspace_bytes_out  receives the workspace size paged_decode_run needs
+ *                   (0 when no request is split).
+ * stream            stream for the upload of the plan's device arrays.
+ *
+ * The plan (host arrays plus one device buffer for the work list) is owned
+ * by the library until paged_decode_plan_destroy.  Planning reads lengths on
+ * the host, so do it before graph capture.
+ */
+int paged_decode_plan(pka_plan** plan_out, const pka_decode_desc* desc,
+                      const int32_t* seq_lens_kv_host, const int32_t* qo_indptr_host,
+                      size_t* workspace_bytes_out, void* stream);
+
+/* Free a plan (NULL is ignored).  Must not be called while a run that uses
+ * the plan may still execute on the device. */
+void paged_decode_plan_destroy(pka_plan* plan);
+
+/* Fill `info` with the plan's summary. */
+int paged_decode_plan_info(const pka_plan* plan, pka_plan_info* info);
+
+/*
+ * Copy the plan's host arrays out (for bit-exact tests of the planner).
+ * items     [num_items * 5] int32: (request, kv_head, chunk, page_lo, page_hi)
+ *           in launch order; page_lo/page_hi index the request's table row.
+ * n_chunks, part_base, page_lo, page_hi  [B] int32 each (part_base -1 when
+ *           the request is not split).
+ * order     [B] int32: requests in launch order.
+ * Any output pointer may be NULL.
+ */
+int paged_decode_plan_export(const pka_plan* plan, int32_t* items, int32_t* n_chunks,
+                             int32_t* part_base, int32_t* page_lo, int32_t* page_hi,
+                             int32_t* order);
+
+/*
+ * Run the planned decode.
+ *
+ * q               bf16, rows [total_q] x heads [Hq] x D; element (t, h, d) at
+ *                 q + t*q_stride_tok + h*q_stride_head + d.  D innermost and
+ *                 dense; other strides free (cudnn_batch_decode_with_kv_cache,
+ *                 Note: "q may carry arbitrary batch/head strides").
+ *                 Strides must be multiples of 8 elements.
+ * k_pages, v_pages  HND pools: element (page, kv_head, slot, d) at
+ *                 base + page*kv_stride_page + kv_head*kv_stride_head + slot*D + d
+ *                 (k_cache / v_cache shapes (total_num_pages, num_heads_kv,
+ *                 page_size, head_dim)).  Strides multiples of 8 elements,
+ *                 bases 16-byte aligned.  A combined K/V tensor is passed as
+ *                 two base pointers with its strides.
+ * block_tables    int32 [B, C] device, row b at block_tables + b*bt_row_stride;
+ *                 token t of request b is in page block_tables[b, t/page_size],
+ *                 slot t % page_size (batch_decode_with_paged_kv_cache,
+ *                 block_tables).  Entries past a request's last page are not read.
+ * seq_lens_kv_dev int32 [B] device; read only when the plan is not frozen
+ *                 (may be NULL for a frozen plan).
+ * sinks           NULL or fp32 [Hq] device: per-head sink logits joining each
+ *                 row's softmax denominator with a zero value row
+ *                 (cudnn_batch_decode_with_kv_cache, sinks).
+ * out             bf16 [total_q, Hq, D] contiguous.
+ * lse             NULL or fp32 [total_q, Hq] contiguous: log2 of the sum over
+ *                 the row's valid keys of exp(scale * q.k) -- the sink is not
+ *                 included (Note "LSE convention").  Required when the plan
+ *                 has return_lse.
+ * workspace       device scratch of at least the plan's workspace_bytes
+ *                 (256-byte aligned); holds fp32 split-KV partials.
+ */
+int paged_decode_run(const pka_plan* plan, const void* q, int64_t q_stride_tok,
+                     int64_t q_stride_head, const void* k_pages, const void* v_pages,
+                     int64_t kv_stride_page, int64_t kv_stride_head,
+                     const int32_t* block_tables, int64_t bt_row_stride,
+                     const int32_t* seq_lens_kv_dev, const float* sinks, void* out, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Wait for `stream`, then read and clear the plan's device status word, which
+ * kernels set instead of trapping: returns PKA_OK, or PKA_ERR_DEVICE_TIMEOUT
+ * when some kernel of an earlier run gave up on a bounded (2 s) wait -- the
+ * outputs of that run are then not valid.  Synchronises; not for capture.
+ */
+int paged_decode_plan_check(const pka_plan* plan, void* stream);
+
+/* ======================================================================== */
+/* LSE merge                                                                 */
+/* ======================================================================== */
+
+/*
+ * Merge num_states partial attention results of the same rows.
+ *
+ * v_states   fp32 [num_states, num_rows, num_heads, head_dim] contiguous:
+ *            each state's normalised output over its own key subset.
+ * s_states   fp32 [num_states, num_rows, num_heads] contiguous: each state's
+ *            base-2 LSE (-inf for an empty subset).
+ * v_out      [num_rows, num_heads, head_dim] contiguous, out_dtype
+ *            PKA_DTYPE_BF16 or PKA_DTYPE_F32:
+ *            sum_i 2^(s_i - m) v_i / sum_i 2^(s_i - m), m = max_i s_i.
+ * s_out      NULL or fp32 [num_rows, num_heads]: m + log2 sum_i 2^(s_i - m).
+ * Rows whose states are all -inf get v = 0 and s = -inf.
+ * head_dim must be a multiple of 4 (<= 1024); num_states >= 1.
+ */
+int attn_merge_lse(const float* v_states, const float* s_states, int32_t num_states,
+                   int32_t num_rows, int32_t num_heads, int32_t head_dim, void* v_out,
+                   int32_t out_dtype, float* s_out, void* stream);
+
+/* ======================================================================== */
+/* Ragged causal prefill                                                     */
+/* ======================================================================== */
+
+/*
+ * batch_size, num_qo_heads, num_kv_heads, head_dim (128) as for decode.
+ * mask         PKA_MASK_CAUSAL (bottom-right aligned) or PKA_MASK_DENSE.
+ * window_left  must be -1 (the page's windowed GQA policy is not built).
+ * sm_scale     NaN selects 1/sqrt(D) (batch_prefill, sm_scale).
+ * output_scale multiplies O (batch_prefill, output_scale).
+ * return_lse   nonzero: batch_prefill_run writes the base-2 LSE.
+ * num_sms      0 = the device's.   flags  PKA_PLAN_HOST_ONLY or 0.
+ */
+typedef struct pka_prefill_desc {
+  int32_t batch_size;
+  int32_t num_qo_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t dtype;
+  int32_t mask;
+  int32_t window_left;
+  float sm_scale;
+  float output_scale;
+  int32_t return_lse;
+  int32_t num_sms;
+  int32_t flags;
+} pka_prefill_desc;
+
+typedef struct pka_prefill_plan pka_prefill_plan; /* opaque prefill plan */
+
+/*
+ * Build the tile schedule of a packed ragged prefill.
+ * qo_indptr_host, kv_indptr_host  [B+1] int32 host arrays, cumulative offsets
+ *           starting at 0 (batch_prefill, qo_indptr / kv_indptr).  For a
+ *           causal mask every request needs kv_len >= q_len.
+ * workspace_bytes_out  receives 0 (the prefill needs no workspace).
+ * num_tiles_out  NULL or receives the number of CTAs batch_prefill_run launches.
+ */
+int batch_prefill_plan(pka_prefill_plan** plan_out, const pka_prefill_desc* desc,
+                       const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
+                       size_t* workspace_bytes_out, int32_t* num_tiles_out, void* stream);
+
+void batch_prefill_plan_destroy(pka_prefill_plan* plan);
+
+/* As paged_decode_plan_check, for the prefill plan's device status word. */
+int batch_prefill_plan_check(const pka_prefill_plan* plan, void* stream);
+
+/*
+ * Run the planned prefill.
+ * q      bf16 packed [total_q, Hq, D]: (t, h, d) at q + t*q_stride_tok + h*q_stride_head + d.
+ * k, v   bf16 packed [total_kv, Hkv, D]: (t, h, d) at base + t*kv_stride_tok + h*kv_stride_head + d.
+ *        All strides multiples of 8 elements, bases 16-byte aligned.
+ * out    bf16 [total_q, Hq, D] contiguous.
+ * lse    NULL or fp32 [total_q, Hq] contiguous base-2 LSE (required with return_lse).
+ */
+int batch_prefill_run(const pka_prefill_plan* plan, const void* q, int64_t q_stride_tok,
+                      int64_t q_stride_head, const void* k, const void* v, int64_t kv_stride_tok,
+                      int64_t kv_stride_head, void* out, float* lse, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* ======================================================================== */
+/* Test hook                                                                 */
+/* ======================================================================== */
+
+/*
+ * Copy tokens [tok_begin, tok_end) of request `request`, KV head `kv_head`,
+ * from an HND pool (layout as for paged_decode_run) into `out`
+ * (bf16 [tok_end - tok_begin, head_dim] contiguous), through the same tensor
+ * map, page coordinates and shared-memory swizzle the decode kernels use.
+ * The caller guarantees that every table entry read is a valid page.
+ */
+int paged_kv_gather(const void* pages, int64_t num_pages, int64_t stride_page,
+                    int64_t stride_head, int32_t num_kv_heads, int32_t page_size,
+                    int32_t head_dim, const int32_t* block_tables, int64_t bt_row_stride,
+                    int32_t request, int32_t kv_head, int32_t tok_begin, int32_t tok_end,
+                    void* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKA_H */

@@ -1,0 +1,201 @@
+"""Python binding of the C ABI, same names as ``include/pka.h``.
+
+Argument marshalling only: tensors are turned into device pointers, strides
+and sizes, outputs are allocated with torch when the caller passes none, and
+every computation happens in ``libpka.so``.  There is no CPU path.
+"""
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib as L
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _host_i32(x):
+    """Contiguous host int32 array (kept alive by the caller) and its pointer."""
+    if x is None:
+        return None, None
+    t = torch.as_tensor(x).to(device="cpu", dtype=torch.int32).contiguous()
+    return t, ctypes.cast(t.data_ptr(), L._pi32)
+
+
+class DecodePlan:
+    """Owns a ``pka_plan*``; freed with ``paged_decode_plan_destroy``."""
+
+    def __init__(self, handle, desc, workspace_bytes):
+        self.handle = handle
+        self.desc = desc
+        self.workspace_bytes = workspace_bytes
+
+    @property
+    def info(self):
+        inf = L.PlanInfo()
+        L.check(L.lib().paged_decode_plan_info(self.handle, ctypes.byref(inf)), "plan_info")
+        return {f: getattr(inf, f) for f, _ in L.PlanInfo._fields_}
+
+    def export(self):
+        """Host arrays of the plan: items (n, 5), n_chunks, part_base, page_lo, page_hi, order."""
+        n = self.info["num_items"]
+        B = self.desc.batch_size
+        items = torch.zeros(max(n, 1) * 5, dtype=torch.int32)
+        arrs = [torch.zeros(B, dtype=torch.int32) for _ in range(5)]
+        ptrs = [ctypes.cast(a.data_ptr(), L._pi32) for a in [items] + arrs]
+        L.check(L.lib().paged_decode_plan_export(self.handle, *ptrs), "plan_export")
+        keys = ["n_chunks", "part_base", "page_lo", "page_hi", "order"]
+        out = {k: a.tolist() for k, a in zip(keys, arrs)}
+        out["items"] = [tuple(r) for r in items[: n * 5].view(n, 5).tolist()]
+        return out
+
+    def check(self, stream=None):
+        """Synchronise and read the device status word (raises on a kernel timeout)."""
+        L.check(L.lib().paged_decode_plan_check(self.handle, _stream(stream)), "plan_check")
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h:
+            L.lib().paged_decode_plan_destroy(h)
+
+
+def paged_decode_plan(seq_lens_kv, *, num_qo_heads, num_kv_heads, page_size, max_pages_per_seq,
+                      num_pages, qo_indptr=None, q_len=1, max_q_len=0, causal=False,
+                      window_left=-1, scale=None, bmm2_scale=1.0, return_lse=False,
+                      freeze_seq_lens=True, num_sms=0, split_waves=0, min_chunk_tokens=0,
+                      mma_min_rows=0, host_only=False, head_dim=128, stream=None):
+    """Plan a batched paged decode from host copies of the lengths (see pka.h)."""
+    seq_t, seq_p = _host_i32(seq_lens_kv)
+    ind_t, ind_p = _host_i32(qo_indptr)
+    d = L.DecodeDesc(
+        batch_size=seq_t.numel(), num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+        head_dim=head_dim, page_size=page_size, max_pages_per_seq=max_pages_per_seq,
+        num_pages=num_pages, dtype=L.PKA_DTYPE_BF16, q_len=q_len, max_q_len=max_q_len,
+        mask=L.PKA_MASK_CAUSAL if causal else L.PKA_MASK_DENSE, window_left=window_left,
+        scale=float("nan") if scale is None else scale, bmm2_scale=bmm2_scale,
+        return_lse=int(bool(return_lse)), freeze_seq_lens=int(bool(freeze_seq_lens)),
+        num_sms=num_sms, split_waves=split_waves, min_chunk_tokens=min_chunk_tokens,
+        mma_min_rows=mma_min_rows, flags=L.PKA_PLAN_HOST_ONLY if host_only else 0)
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    rc = L.lib().paged_decode_plan(ctypes.byref(h), ctypes.byref(d), seq_p, ind_p,
+                                   ctypes.byref(ws), _stream(stream) if not host_only else None)
+    L.check(rc, "paged_decode_plan")
+    return DecodePlan(h, d, ws.value)
+
+
+def paged_decode_run(plan, q, k_pages, v_pages, block_tables, seq_lens_kv=None, sinks=None,
+                     out=None, lse=None, workspace=None, stream=None):
+    """Run a planned decode; returns ``out`` (and ``lse`` when the plan returns it)."""
+    total_q, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if plan.desc.return_lse and lse is None:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None and plan.workspace_bytes > 0:
+        workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = L.lib().paged_decode_run(
+        plan.handle, _ptr(q), q.stride(0), q.stride(1), _ptr(k_pages), _ptr(v_pages),
+        k_pages.stride(0), k_pages.stride(1), _ptr(block_tables), block_tables.stride(0),
+        _ptr(seq_lens_kv), _ptr(sinks), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+        _stream(stream))
+    L.check(rc, "paged_decode_run")
+    return (out, lse) if plan.desc.return_lse else out
+
+
+def attn_merge_lse(v_states, s_states, out_dtype=torch.bfloat16, v_out=None, s_out=None,
+                   stream=None):
+    """Merge ``[N, S, H, D]`` fp32 states by their ``[N, S, H]`` base-2 LSEs."""
+    N, S, H, D = v_states.shape
+    if v_out is None:
+        v_out = torch.empty((S, H, D), dtype=out_dtype, device=v_states.device)
+    if s_out is None:
+        s_out = torch.empty((S, H), dtype=torch.float32, device=v_states.device)
+    code = L.PKA_DTYPE_BF16 if v_out.dtype == torch.bfloat16 else L.PKA_DTYPE_F32
+    rc = L.lib().attn_merge_lse(_ptr(v_states), _ptr(s_states), N, S, H, D, _ptr(v_out), code,
+                                _ptr(s_out), _stream(stream))
+    L.check(rc, "attn_merge_lse")
+    return v_out, s_out
+
+
+class PrefillPlan:
+    """Owns a ``pka_prefill_plan*``."""
+
+    def __init__(self, handle, desc, num_tiles):
+        self.handle = handle
+        self.desc = desc
+        self.num_tiles = num_tiles
+
+    def check(self, stream=None):
+        L.check(L.lib().batch_prefill_plan_check(self.handle, _stream(stream)), "prefill_check")
+
+    def __del__(self):
+        h, self.handle = getattr(self, "handle", None), None
+        if h:
+            L.lib().batch_prefill_plan_destroy(h)
+
+
+def batch_prefill_plan(qo_indptr, kv_indptr, *, num_qo_heads, num_kv_heads, causal=True,
+                       sm_scale=None, output_scale=1.0, return_lse=False, head_dim=128,
+                       window_left=-1, host_only=False, stream=None):
+    """Plan a packed ragged prefill from host copies of the indptr arrays."""
+    qo_t, qo_p = _host_i32(qo_indptr)
+    kv_t, kv_p = _host_i32(kv_indptr)
+    d = L.PrefillDesc(
+        batch_size=qo_t.numel() - 1, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+        head_dim=head_dim, dtype=L.PKA_DTYPE_BF16,
+        mask=L.PKA_MASK_CAUSAL if causal else L.PKA_MASK_DENSE, window_left=window_left,
+        sm_scale=float("nan") if sm_scale is None else sm_scale, output_scale=output_scale,
+        return_lse=int(bool(return_lse)), num_sms=0,
+        flags=L.PKA_PLAN_HOST_ONLY if host_only else 0)
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    nt = ctypes.c_int32()
+    rc = L.lib().batch_prefill_plan(ctypes.byref(h), ctypes.byref(d), qo_p, kv_p,
+                                    ctypes.byref(ws), ctypes.byref(nt),
+                                    _stream(stream) if not host_only else None)
+    L.check(rc, "batch_prefill_plan")
+    return PrefillPlan(h, d, nt.value)
+
+
+def batch_prefill_run(plan, q, k, v, out=None, lse=None, stream=None):
+    """Run a planned prefill; returns ``out`` (and ``lse`` when the plan returns it)."""
+    total_q, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if plan.desc.return_lse and lse is None:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    rc = L.lib().batch_prefill_run(plan.handle, _ptr(q), q.stride(0), q.stride(1), _ptr(k),
+                                   _ptr(v), k.stride(0), k.stride(1), _ptr(out), _ptr(lse),
+                                   None, 0, _stream(stream))
+    L.check(rc, "batch_prefill_run")
+    return (out, lse) if plan.desc.return_lse else out
+
+
+def paged_kv_gather(pages, block_tables, request, kv_head, tok_begin, tok_end, out=None,
+                    stream=None):
+    """Dense copy of paged rows ``[tok_begin, tok_end)`` through the decode addressing."""
+    P, Hkv, ps, D = pages.shape
+    if out is None:
+        out = torch.empty((tok_end - tok_begin, D), dtype=pages.dtype, device=pages.device)
+    rc = L.lib().paged_kv_gather(_ptr(pages), P, pages.stride(0), pages.stride(1), Hkv, ps, D,
+                                 _ptr(block_tables), block_tables.stride(0), request, kv_head,
+                                 tok_begin, tok_end, _ptr(out), _stream(stream))
+    L.check(rc, "paged_kv_gather")
+    return out
+
+
+def default_scale(head_dim=128):
+    return 1.0 / math.sqrt(head_dim)

@@ -1,0 +1,29 @@
+// Kernel launchers (defined in the .cu files, called by the C-ABI layer).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "plan.h"
+
+namespace pka {
+
+// Decode kernel (CUDA-core or mma variant, as the plan chose) followed, when
+// the plan split any request, by the partial-merge kernel.
+int launch_decode(const pka_plan& plan, const DecodeArgs& args, const CUtensorMap& kmap,
+                  const CUtensorMap& vmap, cudaStream_t stream);
+
+// Standalone merge of [N, S, H, D] fp32 states by their base-2 LSEs.
+int launch_merge_states(const float* v_states, const float* s_states, int32_t n, int32_t s,
+                        int32_t h, int32_t d, void* v_out, int32_t out_dtype, float* s_out,
+                        cudaStream_t stream);
+
+// Test hook: paged rows -> dense rows through the decode kernels' addressing.
+int launch_paged_gather(const CUtensorMap& map, const int32_t* block_tables,
+                        int64_t bt_row_stride, int32_t page_size, int32_t request,
+                        int32_t kv_head, int32_t tok_begin, int32_t tok_end, void* out,
+                        cudaStream_t stream);
+
+}  // namespace pka

@@ -1,0 +1,70 @@
+// Ragged causal prefill: plan object, tile schedule and kernel launcher.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pka.h"
+
+namespace pka {
+
+// One CTA of the prefill kernel: a 128-row query tile of one request for a
+// pair of query heads that share a KV head (or one head when the group is odd).
+struct PrefillTile {
+  int32_t request;
+  int32_t head;     // first query head of the tile
+  int32_t q_tile;   // 128-row tile index inside the request
+  int32_t n_kv;     // KV tiles (128 keys) the tile visits
+};
+
+struct PrefillArgs {
+  const void* q;
+  int64_t q_stride_tok;
+  int64_t q_stride_head;
+  void* out;
+  float* lse;
+  const PrefillTile* tiles;
+  const int32_t* qo_indptr;
+  const int32_t* kv_indptr;
+  int32_t* status;
+  int32_t num_tiles;
+  int32_t num_qo_heads;
+  int32_t num_kv_heads;
+  int32_t group;
+  int32_t causal;
+  int32_t heads_per_cta;
+  float scale_log2;
+  float output_scale;
+};
+
+}  // namespace pka
+
+struct pka_prefill_plan {
+  pka_prefill_desc desc;
+  int32_t B = 0, Hq = 0, Hkv = 0, G = 0, D = 0;
+  int32_t total_q = 0, total_kv = 0, heads_per_cta = 1;
+  float scale = 0.f;
+  std::vector<int32_t> qo, kv;
+  std::vector<pka::PrefillTile> tiles;
+  void* dev_buf = nullptr;
+  const pka::PrefillTile* d_tiles = nullptr;
+  const int32_t* d_qo = nullptr;
+  const int32_t* d_kv = nullptr;
+  int32_t* d_status = nullptr;
+  int device = -1;
+};
+
+namespace pka {
+
+// Builds the host tile schedule (heaviest tiles first).
+int build_prefill_plan(pka_prefill_plan& plan, const pka_prefill_desc& desc, const int32_t* qo,
+                       const int32_t* kv);
+
+// Launches the prefill kernel over the plan's tiles.
+int launch_prefill(const pka_prefill_plan& plan, const PrefillArgs& args, const CUtensorMap& qmap,
+                   const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream);
+
+}  // namespace pka

@@ -1,0 +1,76 @@
+// Host tile schedule of the ragged causal prefill (batch_prefill with packed
+// qo_indptr / kv_indptr).  One tile = 128 query rows of one request for the
+// query heads one CTA serves; tiles are ordered heaviest first (most KV tiles
+// to visit), so that the hardware block scheduler hands the long causal rows
+// out before the short ones (longest-processing-time order).
+#include <algorithm>
+#include <cmath>
+
+#include "host_common.h"
+#include "prefill.h"
+
+namespace pka {
+
+namespace {
+constexpr int kTileQ = 128;
+constexpr int kTileK = 128;
+}  // namespace
+
+int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const int32_t* qo,
+                       const int32_t* kv) {
+  pka_prefill_desc d = d_in;
+  PKA_CHECK_ARG(qo != nullptr && kv != nullptr, "qo_indptr_host and kv_indptr_host are required");
+  PKA_CHECK_ARG(d.batch_size >= 1, "batch_size must be >= 1");
+  PKA_CHECK_ARG(d.num_qo_heads >= 1 && d.num_kv_heads >= 1, "head counts must be >= 1");
+  PKA_CHECK_ARG(d.num_qo_heads % d.num_kv_heads == 0,
+                "num_qo_heads (%d) must be a multiple of num_kv_heads (%d)", d.num_qo_heads,
+                d.num_kv_heads);
+  if (d.dtype != PKA_DTYPE_BF16)
+    return fail(PKA_ERR_UNSUPPORTED, "only bf16 q/K/V are supported (dtype %d)", d.dtype);
+  if (d.head_dim != 128)
+    return fail(PKA_ERR_UNSUPPORTED, "prefill head_dim must be 128 (got %d; 256 not built)",
+                d.head_dim);
+  PKA_CHECK_ARG(d.mask == PKA_MASK_DENSE || d.mask == PKA_MASK_CAUSAL, "unknown mask %d", d.mask);
+  if (d.window_left != -1)
+    return fail(PKA_ERR_UNSUPPORTED, "prefill window_left must be -1");
+  if (std::isnan(d.sm_scale)) d.sm_scale = 1.0f / std::sqrt((float)d.head_dim);
+  PKA_CHECK_ARG(std::isfinite(d.sm_scale) && std::isfinite(d.output_scale),
+                "sm_scale and output_scale must be finite");
+  PKA_CHECK_ARG(qo[0] == 0 && kv[0] == 0, "indptr arrays must start at 0");
+  const int32_t B = d.batch_size;
+  p.desc = d;
+  p.B = B;
+  p.Hq = d.num_qo_heads;
+  p.Hkv = d.num_kv_heads;
+  p.G = p.Hq / p.Hkv;
+  p.D = d.head_dim;
+  p.scale = d.sm_scale;
+  p.heads_per_cta = (p.G % 2 == 0) ? 2 : 1;
+  p.qo.assign(qo, qo + B + 1);
+  p.kv.assign(kv, kv + B + 1);
+  p.tiles.clear();
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t lq = (int64_t)qo[b + 1] - qo[b], lk = (int64_t)kv[b + 1] - kv[b];
+    PKA_CHECK_ARG(lq >= 0 && lk >= 0, "indptr arrays must be non-decreasing (request %d)", b);
+    if (d.mask == PKA_MASK_CAUSAL)
+      PKA_CHECK_ARG(lk >= lq, "request %d: causal prefill needs kv_len >= q_len", b);
+    PKA_CHECK_ARG(lq == 0 || lk > 0, "request %d has queries but no keys", b);
+    const int64_t n_qt = ceil_div(lq, kTileQ);
+    for (int64_t m = 0; m < n_qt; ++m) {
+      // keys seen by the tile's last row: bottom-right causal diagonal
+      const int64_t last_row = std::min<int64_t>(lq, (m + 1) * kTileQ) - 1;
+      const int64_t hi = d.mask == PKA_MASK_CAUSAL ? lk - lq + last_row + 1 : lk;
+      const int32_t n_kv = (int32_t)ceil_div(hi, kTileK);
+      for (int32_t h = 0; h < p.Hq; h += p.heads_per_cta)
+        p.tiles.push_back(PrefillTile{b, h, (int32_t)m, n_kv});
+    }
+  }
+  std::stable_sort(p.tiles.begin(), p.tiles.end(),
+                   [](const PrefillTile& a, const PrefillTile& b) { return a.n_kv > b.n_kv; });
+  p.total_q = qo[B];
+  p.total_kv = kv[B];
+  PKA_CHECK_ARG(p.tiles.size() < (size_t)INT32_MAX, "too many prefill tiles");
+  return PKA_OK;
+}
+
+}  // namespace pka

@@ -1,0 +1,69 @@
+#include "tmap.h"
+
+#include <mutex>
+
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "host_common.h"
+
+namespace pka {
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                  cudaEnableDefault, &q);
+  if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+}  // namespace
+
+int encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box) {
+  std::call_once(g_encode_once, load_encode);
+  if (g_encode == nullptr) {
+    if (g_encode_err != cudaSuccess) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled lookup");
+    return fail(PKA_ERR_CUDA, "cuTensorMapEncodeTiled not found in the driver");
+  }
+  PKA_CHECK_ARG(((uintptr_t)base & 15) == 0, "tensor base %p is not 16-byte aligned", base);
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bdim[5], estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) {
+    PKA_CHECK_ARG(strides[i] % 16 == 0, "tensor stride %llu bytes is not a multiple of 16",
+                  (unsigned long long)strides[i]);
+    gstride[i] = strides[i];
+  }
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                        const_cast<void*>(base), gdim, gstride, bdim, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKA_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PKA_OK;
+}
+
+int encode_kv_pool_map(CUtensorMap* map, const void* pool, int64_t num_pages, int32_t num_heads,
+                       int32_t page_size, int32_t head_dim, int64_t stride_page,
+                       int64_t stride_head) {
+  PKA_CHECK_ARG(stride_head > 0 && stride_page > 0, "K/V strides must be positive");
+  const uint64_t dims[4] = {(uint64_t)head_dim, (uint64_t)page_size, (uint64_t)num_heads,
+                            (uint64_t)num_pages};
+  const uint64_t strides[3] = {(uint64_t)head_dim * 2, (uint64_t)stride_head * 2,
+                               (uint64_t)stride_page * 2};
+  // box: 16 token slots x 64 columns of one (page, head) block; a page of
+  // page_size slots is read as page_size / 16 such units, two boxes per unit.
+  const uint32_t box[4] = {64, 16, 1, 1};
+  return encode_bf16_map(map, pool, 4, dims, strides, box);
+}
+
+}  // namespace pka

@@ -1,0 +1,106 @@
+"""The C-ABI library loads, exports every function include/pka.h declares, and
+rejects invalid arguments on the host (no GPU needed for any of this)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_attention_32_gb300 import _lib as L
+from paged_kv_attention_32_gb300 import api
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "pka.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M))
+                  - {"if", "defined"})
+
+
+def test_header_declares_the_binding_symbols():
+    assert set(_declared()) == set(L.EXPORTED)
+
+
+@pytest.mark.parametrize("name", _declared())
+def test_library_exports_symbol(name):
+    lib = ctypes.CDLL(L.LIB_PATH)
+    assert hasattr(lib, name)
+
+
+def test_version_string():
+    assert b"sm_103a" in L.lib().pka_version()
+
+
+def _plan(**kw):
+    args = dict(num_qo_heads=8, num_kv_heads=2, page_size=16, max_pages_per_seq=20,
+                num_pages=100, num_sms=8, host_only=True)
+    args.update(kw)
+    seq = args.pop("seq", [100, 50])
+    return api.paged_decode_plan(seq, **args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_qo_heads=6, num_kv_heads=4), L.PKA_ERR_INVALID_ARG),      # Hq % Hkv
+    (dict(head_dim=64), L.PKA_ERR_UNSUPPORTED),                         # D != 128
+    (dict(page_size=8), L.PKA_ERR_UNSUPPORTED),
+    (dict(seq=[100, 0]), L.PKA_ERR_INVALID_ARG),                        # kv_len 0
+    (dict(seq=[3, 50], q_len=4), L.PKA_ERR_INVALID_ARG),                # kv_len < q_len
+    (dict(seq=[400, 50]), L.PKA_ERR_INVALID_ARG),                       # > C * page_size
+    (dict(q_len=2, max_q_len=3), L.PKA_ERR_INVALID_ARG),                # fixed: max != q_len
+    (dict(qo_indptr=[0, 2, 5], max_q_len=2), L.PKA_ERR_INVALID_ARG),    # above capacity
+    (dict(qo_indptr=[0, 2, 5], q_len=3, max_q_len=4), L.PKA_ERR_INVALID_ARG),  # alias clash
+    (dict(qo_indptr=[1, 2, 5]), L.PKA_ERR_INVALID_ARG),
+    (dict(qo_indptr=[0, 2, 2]), L.PKA_ERR_INVALID_ARG),                 # empty packed request
+    (dict(window_left=-2), L.PKA_ERR_INVALID_ARG),
+    (dict(num_qo_heads=64, num_kv_heads=1, q_len=2), L.PKA_ERR_UNSUPPORTED),  # 128 rows
+])
+def test_plan_rejects(kw, code):
+    with pytest.raises(L.PkaError) as ei:
+        _plan(**kw)
+    assert ei.value.code == code
+
+
+def test_plan_accepts_packed_and_reports_total_rows():
+    p = _plan(qo_indptr=[0, 2, 5], causal=True)
+    assert p.info["total_q"] == 5
+
+
+def test_run_rejects_host_only_plan_and_null_pointers():
+    p = _plan()
+    rc = L.lib().paged_decode_run(p.handle, None, 0, 0, None, None, 0, 0, None, 0, None, None,
+                                  None, None, None, 0, None)
+    assert rc == L.PKA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=256), L.PKA_ERR_UNSUPPORTED),
+    (dict(window_left=5), L.PKA_ERR_UNSUPPORTED),
+    (dict(num_qo_heads=6, num_kv_heads=4), L.PKA_ERR_INVALID_ARG),
+])
+def test_prefill_plan_rejects(kw, code):
+    args = dict(num_qo_heads=8, num_kv_heads=2, host_only=True)
+    args.update(kw)
+    with pytest.raises(L.PkaError) as ei:
+        api.batch_prefill_plan([0, 10, 30], [0, 10, 30], **args)
+    assert ei.value.code == code
+
+
+def test_prefill_plan_rejects_causal_kv_shorter_than_q():
+    with pytest.raises(L.PkaError):
+        api.batch_prefill_plan([0, 10], [0, 5], num_qo_heads=2, num_kv_heads=1, host_only=True)
+
+
+def test_prefill_tiles_heaviest_first():
+    p = api.batch_prefill_plan([0, 300, 310], [0, 300, 310], num_qo_heads=4, num_kv_heads=1,
+                               host_only=True)
+    # 3 q-tiles for request 0 + 1 for request 1, two head pairs each
+    assert p.num_tiles == (3 + 1) * 2
+
+
+def test_merge_rejects_bad_head_dim():
+    rc = L.lib().attn_merge_lse(None, None, 1, 1, 1, 6, None, 0, None, None)
+    assert rc == L.PKA_ERR_INVALID_ARG

@@ -1,0 +1,161 @@
+"""Paged decode on the GPU against the fp64 oracle (element by element)."""
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_attention_32_gb300 import api
+from paged_kv_attention_32_gb300 import workloads as wl
+
+from helpers import assert_close, oracle_decode, row_mask, run_decode
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+# Oracle-sized copies of the four decode workloads: same structure (GQA group,
+# page size, q_len mix, causal/window/sinks), fewer and shorter requests, still
+# spanning many 16-token units and a ragged last page.
+SMALL = {
+    "tiny": wl.TINY_DECODE,
+    "llama3_8b": wl.shrink(wl.LLAMA3_8B_DECODE, batch=6, kv_len_range=(512, 2100),
+                           pool_pages=1000, table_width=160, return_lse=True),
+    "skewed": wl.shrink(wl.SKEWED_DECODE, batch=5, fixed_first_kv_len=12000,
+                        kv_len_range=(1024, 4096), table_width=400),
+    "spec": wl.shrink(wl.SPEC_DECODE, batch=6, kv_len_range=(2048, 6000), table_width=400),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("seed", [0, 1])
+def test_decode_matches_oracle(name, seed):
+    inp = wl.make_decode_inputs(SMALL[name], seed=seed, device=DEV)
+    out, lse, plan = run_decode(inp)
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "skewed"])
+def test_decode_split_kv_path(name):
+    """Few SMs in the plan force a split of the long requests: partials + merge kernel."""
+    inp = wl.make_decode_inputs(SMALL[name], seed=3, device=DEV)
+    out, lse, plan = run_decode(inp, num_sms=32, split_waves=2, min_chunk_tokens=128)
+    assert plan.info["num_split"] > 0
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b", "skewed"])
+def test_decode_tensor_core_kernel_on_narrow_groups(name):
+    """The mma kernel also runs 4- and 8-row groups (rows padded to 16)."""
+    inp = wl.make_decode_inputs(SMALL[name], seed=4, device=DEV)
+    out, lse, plan = run_decode(inp, mma_min_rows=1)
+    assert plan.info["kernel"] == 1
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("G,L,causal,W,sinks", [
+    (4, 2, True, -1, False),     # 8 rows, CUDA-core kernel, causal multi-token
+    (2, 3, False, 40, True),     # dense mask with a window, sinks
+    (1, 1, False, 0, True),      # window 0: only the diagonal key
+    (8, 8, True, 100, True),     # 64 rows, four m16 tiles
+    (4, 3, True, 17, False),     # 12 rows: mma kernel
+])
+def test_decode_masks_and_groups(G, L, causal, W, sinks):
+    w = wl.DecodeWorkload(name="masks", batch=5, num_qo_heads=2 * G, num_kv_heads=2,
+                          head_dim=128, page_size=16, kv_len_range=(L, 700), q_len_range=(L, L),
+                          causal=causal, window_left=W, sinks=sinks)
+    inp = wl.make_decode_inputs(w, seed=5, device=DEV)
+    out, lse, plan = run_decode(inp)
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+def test_decode_page_size_64_and_bmm2_scale():
+    w = wl.DecodeWorkload(name="ps64", batch=4, num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                          page_size=64, kv_len_range=(1, 900), bmm2_scale=0.5)
+    inp = wl.make_decode_inputs(w, seed=6, device=DEV)
+    out, lse, _ = run_decode(inp)
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+def test_decode_live_lengths_unfrozen_plan():
+    """A plan that does not freeze the lengths reads them at run time (<= planned)."""
+    w = wl.shrink(wl.SPEC_DECODE, batch=4, kv_len_range=(300, 1500), table_width=120,
+                  window_left=200)
+    inp = wl.make_decode_inputs(w, seed=7, device=DEV)
+    plan_lens = inp["seq_lens_kv"].clone()
+    live = plan_lens - torch.tensor([0, 5, 17, 100], dtype=torch.int32, device=DEV)
+    from helpers import decode_plan_for
+    plan = decode_plan_for(inp, freeze_seq_lens=False, num_sms=8, split_waves=2)
+    inp2 = dict(inp, seq_lens_kv=live)
+    out, lse = api.paged_decode_run(plan, inp["q"], inp["k_pages"], inp["v_pages"],
+                                    inp["block_tables"], seq_lens_kv=live, sinks=inp["sinks"])
+    torch.cuda.synchronize()
+    plan.check()
+    ref_o, ref_l = oracle_decode(inp2)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+def test_decode_strided_query_and_combined_kv():
+    """q as a slice of a wider buffer; K and V interleaved in one pool tensor."""
+    w = wl.shrink(wl.TINY_DECODE, batch=3)
+    inp = wl.make_decode_inputs(w, seed=8, device=DEV)
+    q = inp["q"]
+    wide = torch.zeros((q.shape[0], q.shape[1] * 3, 128), dtype=q.dtype, device=DEV)
+    wide[:, 8:16] = q
+    qs = wide[:, 8:16]
+    P, H, ps, D = inp["k_pages"].shape
+    comb = torch.stack([inp["k_pages"], inp["v_pages"]], dim=1).contiguous()   # [P, 2, H, ps, D]
+    kview, vview = comb[:, 0], comb[:, 1]
+    from helpers import decode_plan_for
+    plan = decode_plan_for(inp)
+    out, lse = api.paged_decode_run(plan, qs, kview, vview, inp["block_tables"])
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+def test_decode_graph_capture_replays_eagerly_equal():
+    inp = wl.make_decode_inputs(SMALL["skewed"], seed=9, device=DEV)
+    from helpers import decode_plan_for
+    plan = decode_plan_for(inp, num_sms=32, split_waves=2)
+    out = torch.empty_like(inp["q"])
+    lse = torch.empty(inp["q"].shape[:2], dtype=torch.float32, device=DEV)
+    ws = torch.empty(max(plan.workspace_bytes, 1), dtype=torch.uint8, device=DEV)
+    args = (plan, inp["q"], inp["k_pages"], inp["v_pages"], inp["block_tables"])
+    api.paged_decode_run(*args, out=out, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    eager = out.clone(), lse.clone()
+    out.zero_()
+    lse.zero_()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            api.paged_decode_run(*args, out=out, lse=lse, workspace=ws, stream=s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager[0]) and torch.equal(lse, eager[1])
+
+
+# --------------------------------------------------------------------------
+# Full-size workloads, in the launch configuration bench.py times: sampled
+# requests (longest, shortest, a middle one) against the oracle.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["llama3_8b", "skewed", "spec"])
+def test_decode_full_size_sampled(name):
+    w = wl.DECODE_WORKLOADS[name]
+    inp = wl.make_decode_inputs(w, seed=0, device=DEV)
+    out, lse, plan = run_decode(inp, return_lse=True)
+    seq = inp["seq_lens_kv"].cpu().numpy()
+    order = np.argsort(-seq, kind="stable")
+    reqs = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2])})
+    ref_o, ref_l = oracle_decode(inp, requests=reqs)
+    rows = row_mask(inp, reqs)
+    assert_close(out, lse, ref_o, ref_l, rows=rows)
+    assert torch.isfinite(out.float()).all()

@@ -1,0 +1,52 @@
+"""Standalone LSE merge against the oracle's merge, and the paged gather hook
+bit for bit against a CPU gather."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_32_gb300 import api
+from paged_kv_attention_32_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("N,S,H,D", [(1, 3, 2, 128), (5, 17, 8, 128), (3, 4, 3, 64), (7, 2, 1, 256)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_merge_matches_oracle(N, S, H, D, out_dtype):
+    g = torch.Generator().manual_seed(N * 100 + D)
+    v = torch.randn((N, S, H, D), generator=g)
+    s = torch.randn((N, S, H), generator=g) * 6
+    s[:, 0, 0] = -float("inf")            # an all-empty row
+    if N > 1:
+        s[0, -1, -1] = -float("inf")      # one empty state
+    vo, so = api.attn_merge_lse(v.cuda(), s.cuda(), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    ref_v, ref_s = oracle.merge_states(v.double().numpy(), s.double().numpy())
+    got = vo.float().cpu().numpy()
+    tol = 2e-2 if out_dtype == torch.bfloat16 else 1e-5
+    assert np.all(np.abs(got - ref_v) <= tol + tol * np.abs(ref_v))
+    gs = so.cpu().numpy()
+    fin = np.isfinite(ref_s)
+    assert np.array_equal(np.isfinite(gs), fin)
+    assert np.all(np.abs(gs[fin] - ref_s[fin]) <= 1e-3)
+    assert np.all(got[0, 0] == 0)
+
+
+@pytest.mark.parametrize("ps", [16, 32, 64])
+def test_gather_is_bit_exact(ps):
+    w = wl.DecodeWorkload(name="g", batch=3, num_qo_heads=4, num_kv_heads=2, head_dim=128,
+                          page_size=ps, kv_len_range=(1, 500))
+    inp = wl.make_decode_inputs(w, seed=ps, device="cuda")
+    kp = inp["k_pages"]
+    bt = inp["block_tables"].cpu().numpy()
+    bits = wl.bf16_bits(kp)
+    for b, n in enumerate(inp["seq_lens_kv"].cpu().tolist()):
+        for hk in range(2):
+            for lo, hi in [(0, n), (n // 3, n), (min(5, n), min(21, n))]:
+                got = api.paged_kv_gather(kp, inp["block_tables"], b, hk, lo, hi)
+                torch.cuda.synchronize()
+                t = np.arange(lo, hi)
+                want = bits[bt[b, t // ps], hk, t % ps, :]
+                assert np.array_equal(wl.bf16_bits(got), want)

@@ -1,0 +1,77 @@
+"""The C++ planner against the written plan specification, bit for bit (CPU only).
+
+Plans are built with PKA_PLAN_HOST_ONLY, so no GPU is needed.
+"""
+
+import random
+
+import pytest
+
+from oracle.plan_spec import plan_spec
+from paged_kv_attention_32_gb300 import api
+
+
+def _cases():
+    rnd = random.Random(23)
+    cases = []
+    for _ in range(40):
+        B = rnd.randint(1, 48)
+        Hkv = rnd.choice([1, 2, 4, 8])
+        G = rnd.choice([1, 2, 4, 8])
+        ps = rnd.choice([16, 32, 64])
+        packed = rnd.random() < 0.5
+        ql = [rnd.randint(1, 6) if packed else 1 for _ in range(B)]
+        kv = [max(ql[b], rnd.randint(1, 30000)) for b in range(B)]
+        if rnd.random() < 0.3:
+            kv[rnd.randrange(B)] = 131072
+        W = rnd.choice([-1, -1, 0, 7, 4095])
+        cases.append(dict(kv=kv, ql=ql, packed=packed, Hq=G * Hkv, Hkv=Hkv, ps=ps, W=W,
+                          sms=rnd.choice([8, 132, 152]), waves=rnd.choice([1, 2, 4]),
+                          mct=rnd.choice([128, 256, 512]), frozen=rnd.random() < 0.8,
+                          causal=rnd.random() < 0.5))
+    return cases
+
+
+@pytest.mark.parametrize("c", _cases())
+def test_native_plan_matches_spec(c):
+    ps = c["ps"]
+    C = max(-(-n // ps) for n in c["kv"])
+    indptr = None
+    if c["packed"]:
+        indptr = [0]
+        for q in c["ql"]:
+            indptr.append(indptr[-1] + q)
+    G = c["Hq"] // c["Hkv"]
+    if G * max(c["ql"]) > 64:
+        pytest.skip("rows per KV head above the supported 64")
+    plan = api.paged_decode_plan(
+        c["kv"], num_qo_heads=c["Hq"], num_kv_heads=c["Hkv"], page_size=ps,
+        max_pages_per_seq=C, num_pages=10 ** 6, qo_indptr=indptr, q_len=1,
+        causal=c["causal"], window_left=c["W"], freeze_seq_lens=c["frozen"], num_sms=c["sms"],
+        split_waves=c["waves"], min_chunk_tokens=c["mct"], host_only=True)
+    got = plan.export()
+    info = plan.info
+    want = plan_spec(c["kv"], c["ql"], c["Hq"], c["Hkv"], 128, ps, c["W"], c["sms"], c["waves"],
+                     c["mct"], c["frozen"])
+    assert got["items"] == [tuple(x) for x in want["items"]]
+    assert got["n_chunks"] == want["n_chunks"]
+    assert got["part_base"] == want["part_base"]
+    assert got["page_lo"] == want["page_lo"]
+    assert got["page_hi"] == want["page_hi"]
+    assert got["order"] == want["order"]
+    assert info["chunk_pages"] == want["chunk_pages"]
+    assert info["partial_rows"] == want["partial_rows"]
+    assert info["workspace_bytes"] == want["workspace_bytes"]
+
+
+def test_kernel_choice_follows_rows_per_kv_head():
+    def kernel(G, L, mma_min_rows=0):
+        p = api.paged_decode_plan([100] * 2, num_qo_heads=G, num_kv_heads=1, page_size=16,
+                                  max_pages_per_seq=8, num_pages=100, q_len=L, num_sms=8,
+                                  mma_min_rows=mma_min_rows, host_only=True)
+        return p.info["kernel"], p.info["rows_per_cta"]
+    assert kernel(4, 1) == (0, 4)
+    assert kernel(8, 1) == (0, 8)
+    assert kernel(8, 2) == (1, 16)
+    assert kernel(4, 3) == (1, 12)      # 9..15 rows exceed one CUDA-core warp
+    assert kernel(4, 1, mma_min_rows=4) == (1, 4)
