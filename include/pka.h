@@ -250,6 +250,38 @@ int paged_decode_run(const pka_plan* plan, const void* q, int64_t q_stride_tok,
  */
 int paged_decode_plan_check(const pka_plan* plan, void* stream);
 
+/*
+ * paged_decode_run without any device allocation.  The pages have no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc themselves -- code inside an allocator hook, or a serving
+ * process whose device memory is a fixed pool it does not control.  Together
+ * with a plan built with PKA_PLAN_HOST_ONLY the whole decode allocates
+ * nothing on the device.
+ *
+ * Arguments are those of paged_decode_run without the workspace.  The plan's
+ * work list and the split-KV fp32 partials go to one fixed 16 MiB device
+ * array inside the library (held on every GPU that loads the library until
+ * the process exits); a plan that needs more returns
+ * PKA_ERR_WORKSPACE_TOO_SMALL -- use paged_decode_run for it.
+ *
+ * - The first call on a device looks up that array's device address
+ *   (cudaGetSymbolAddress) with the device current; make that first call
+ *   before any stream capture.
+ * - Every call on a device shares the one array and overwrites what the
+ *   previous call left there; calls whose executions overlap on the GPU (on
+ *   different streams, or from different threads) race and give wrong
+ *   results.  Serialise them.
+ * - The call copies the plan's host arrays into the array with
+ *   cudaMemcpyAsync and clears its status word with cudaMemsetAsync; it
+ *   calls no allocating routine.
+ */
+int paged_decode_run_noalloc(const pka_plan* plan, const void* q, int64_t q_stride_tok,
+                             int64_t q_stride_head, const void* k_pages, const void* v_pages,
+                             int64_t kv_stride_page, int64_t kv_stride_head,
+                             const int32_t* block_tables, int64_t bt_row_stride,
+                             const int32_t* seq_lens_kv_dev, const float* sinks, void* out,
+                             float* lse, void* stream);
+
 /* ======================================================================== */
 /* LSE merge                                                                 */
 /* ======================================================================== */

@@ -28,6 +28,7 @@ EXPORTED = (
     "pka_last_error", "pka_version",
     "paged_decode_plan", "paged_decode_plan_destroy", "paged_decode_plan_info",
     "paged_decode_plan_export", "paged_decode_run", "paged_decode_plan_check",
+    "paged_decode_run_noalloc",
     "attn_merge_lse",
     "batch_prefill_plan", "batch_prefill_plan_destroy", "batch_prefill_plan_check",
     "batch_prefill_run",
@@ -85,6 +86,8 @@ _SIGS = {
     "paged_decode_run": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _i64,
                                         _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "paged_decode_plan_check": (ctypes.c_int, [_vp, _vp]),
+    "paged_decode_run_noalloc": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _vp,
+                                                _i64, _vp, _vp, _vp, _vp, _vp]),
     "attn_merge_lse": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]),
     "batch_prefill_plan": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.POINTER(PrefillDesc),
                                           _pi32, _pi32, ctypes.POINTER(_sz), _pi32, _vp]),

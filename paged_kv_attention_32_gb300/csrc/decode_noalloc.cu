@@ -1,0 +1,144 @@
+// paged_decode_run_noalloc: the planned decode for callers that cannot
+// allocate device memory -- code running where cudaMalloc is not allowed
+// (inside an allocator hook, or a serving process whose device memory is a
+// fixed pool owned by someone else).  Everything the run needs beyond the
+// caller's inputs and outputs -- the plan's work list and the split-KV fp32
+// partials -- lives in one file-scope device array of fixed size.
+#include <cstring>
+#include <mutex>
+
+#include "host_common.h"
+#include "kernels.h"
+#include "plan.h"
+#include "tmap.h"
+
+namespace pka {
+namespace {
+
+// Fixed scratch: 16 MiB on every GPU that loads the library, held until the
+// process exits.  Layout per call: status word | work items | request info |
+// merge rows | partial outputs | partial LSEs, each 256-byte aligned.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 256;
+std::mutex g_setup_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Device address of the scratch array on `dev` (the current device), looked
+// up once per device.  In host code the symbol is only a stand-in: kernels
+// get this address, never the symbol itself.
+int scratch_address(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKA_ERR_INVALID_ARG, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_scratch_addr[dev] = p;
+  }
+  *out = static_cast<unsigned char*>(g_scratch_addr[dev]);
+  return PKA_OK;
+}
+
+}  // namespace
+}  // namespace pka
+
+using namespace pka;
+
+extern "C" int paged_decode_run_noalloc(const pka_plan* p, const void* q, int64_t q_stride_tok,
+                                        int64_t q_stride_head, const void* k_pages,
+                                        const void* v_pages, int64_t kv_stride_page,
+                                        int64_t kv_stride_head, const int32_t* block_tables,
+                                        int64_t bt_row_stride, const int32_t* seq_lens_kv_dev,
+                                        const float* sinks, void* out, float* lse, void* stream) {
+  clear_error();
+  PKA_CHECK_ARG(p != nullptr, "plan must not be NULL");
+  PKA_CHECK_ARG(q && k_pages && v_pages && block_tables && out,
+                "q, k_pages, v_pages, block_tables and out must not be NULL");
+  PKA_CHECK_ARG(p->desc.freeze_seq_lens || seq_lens_kv_dev != nullptr,
+                "seq_lens_kv_dev is required when the plan does not freeze the lengths");
+  PKA_CHECK_ARG(!p->desc.return_lse || lse != nullptr, "the plan returns the LSE: lse is NULL");
+  PKA_CHECK_ARG(reinterpret_cast<uintptr_t>(q) % 16 == 0 && q_stride_tok % 8 == 0 &&
+                    q_stride_head % 8 == 0 && q_stride_tok >= 0 && q_stride_head >= 0,
+                "q must be 16-byte aligned with non-negative strides that are multiples of 8");
+  PKA_CHECK_ARG(reinterpret_cast<uintptr_t>(out) % 16 == 0, "out must be 16-byte aligned");
+  PKA_CHECK_ARG(kv_stride_page % 8 == 0 && kv_stride_head % 8 == 0,
+                "K/V strides must be multiples of 8 elements");
+  PKA_CHECK_ARG(bt_row_stride >= p->C, "bt_row_stride is smaller than the table width");
+
+  // scratch layout for this plan
+  const size_t n_items = p->items.size() * sizeof(WorkItem);
+  const size_t n_reqs = p->reqs.size() * sizeof(ReqInfo);
+  const size_t n_merge = p->merge_rows.size() * sizeof(MergeRow);
+  const size_t off_items = 256;
+  const size_t off_reqs = off_items + up256(n_items);
+  const size_t off_merge = off_reqs + up256(n_reqs);
+  const size_t off_ws = off_merge + up256(n_merge);
+  const size_t off_lse = off_ws + (size_t)p->ws_lse_offset;
+  const size_t total = off_ws + (size_t)p->workspace_bytes;
+  if (total > kNoAllocScratchBytes)
+    return fail(PKA_ERR_WORKSPACE_TOO_SMALL,
+                "the plan needs %zu bytes of scratch; paged_decode_run_noalloc holds at most %zu "
+                "(use paged_decode_run with a caller workspace)",
+                total, kNoAllocScratchBytes);
+
+  int dev = -1;
+  PKA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+  unsigned char* base = nullptr;
+  int rc = scratch_address(dev, &base);
+  if (rc != PKA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Only the status word must start at zero: every partial row is written by
+  // its chunk before the merge kernel reads it.
+  PKA_CUDA_TRY(cudaMemsetAsync(base, 0, 256, s), "cudaMemsetAsync(no-alloc status)");
+  if (n_items)
+    PKA_CUDA_TRY(cudaMemcpyAsync(base + off_items, p->items.data(), n_items,
+                                 cudaMemcpyHostToDevice, s),
+                 "cudaMemcpyAsync(no-alloc items)");
+  PKA_CUDA_TRY(cudaMemcpyAsync(base + off_reqs, p->reqs.data(), n_reqs, cudaMemcpyHostToDevice, s),
+               "cudaMemcpyAsync(no-alloc requests)");
+  if (n_merge)
+    PKA_CUDA_TRY(cudaMemcpyAsync(base + off_merge, p->merge_rows.data(), n_merge,
+                                 cudaMemcpyHostToDevice, s),
+                 "cudaMemcpyAsync(no-alloc merge rows)");
+
+  CUtensorMap kmap, vmap;
+  rc = encode_kv_pool_map(&kmap, k_pages, p->desc.num_pages, p->Hkv, p->ps, p->D, kv_stride_page,
+                          kv_stride_head);
+  if (rc != PKA_OK) return rc;
+  rc = encode_kv_pool_map(&vmap, v_pages, p->desc.num_pages, p->Hkv, p->ps, p->D, kv_stride_page,
+                          kv_stride_head);
+  if (rc != PKA_OK) return rc;
+
+  DecodeArgs a{};
+  a.q = q;
+  a.q_stride_tok = q_stride_tok;
+  a.q_stride_head = q_stride_head;
+  a.block_tables = block_tables;
+  a.bt_row_stride = bt_row_stride;
+  a.seq_lens_live = p->desc.freeze_seq_lens ? nullptr : seq_lens_kv_dev;
+  a.sinks = sinks;
+  a.out = out;
+  a.lse = p->desc.return_lse ? lse : nullptr;
+  a.ws_o = reinterpret_cast<float*>(base + off_ws);
+  a.ws_lse = reinterpret_cast<float*>(base + off_lse);
+  a.items = reinterpret_cast<const WorkItem*>(base + off_items);
+  a.reqs = reinterpret_cast<const ReqInfo*>(base + off_reqs);
+  a.merge_rows = reinterpret_cast<const MergeRow*>(base + off_merge);
+  a.status = reinterpret_cast<int32_t*>(base);
+  a.num_items = (int32_t)p->items.size();
+  a.num_merge_rows = (int32_t)p->merge_rows.size();
+  a.num_qo_heads = p->Hq;
+  a.num_kv_heads = p->Hkv;
+  a.group = p->G;
+  a.page_size = p->ps;
+  a.causal = p->desc.mask == PKA_MASK_CAUSAL;
+  a.window_left = p->desc.window_left;
+  a.rows_per_cta = p->rows_per_cta;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.bmm2_scale = p->desc.bmm2_scale;
+  return launch_decode(*p, a, kmap, vmap, s);
+}

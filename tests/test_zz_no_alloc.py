@@ -1,0 +1,73 @@
+"""paged_decode_run_noalloc: the decode entry point for callers that cannot
+allocate device memory (code inside an allocator hook, or a process whose
+device memory is a fixed pool it does not control).  It keeps its work list
+and split-KV partials in a fixed array inside the library.  Checked through
+the C ABI against paged_decode_run on two calls in a row.  This file is
+collected last on purpose."""
+
+import ctypes
+
+import pytest
+import torch
+
+from paged_kv_attention_32_gb300 import _lib as L
+from paged_kv_attention_32_gb300 import api
+from paged_kv_attention_32_gb300 import workloads as wl
+
+from helpers import LSE_ATOL, O_ATOL, O_RTOL, decode_plan_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(plan, inp, out, lse):
+    q, kp, vp, bt = inp["q"], inp["k_pages"], inp["v_pages"], inp["block_tables"]
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def ptr(t):
+        return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+    return L.lib().paged_decode_run_noalloc(
+        plan.handle, ptr(q), q.stride(0), q.stride(1), ptr(kp), ptr(vp), kp.stride(0),
+        kp.stride(1), ptr(bt), bt.stride(0), ptr(inp["seq_lens_kv"]), ptr(inp["sinks"]),
+        ptr(out), ptr(lse), stream)
+
+
+@pytest.mark.parametrize("name", ["skewed", "spec"])
+def test_noalloc_matches_paged_decode_run_twice(name):
+    small = {
+        "skewed": wl.shrink(wl.SKEWED_DECODE, batch=5, fixed_first_kv_len=12000,
+                            kv_len_range=(1024, 4096), table_width=400),
+        "spec": wl.shrink(wl.SPEC_DECODE, batch=6, kv_len_range=(2048, 6000), table_width=400),
+    }[name]
+    for seed in (11, 12):   # two calls in a row, different inputs
+        inp = wl.make_decode_inputs(small, seed=seed, device="cuda")
+        ref_plan = decode_plan_for(inp, num_sms=128, split_waves=2)
+        host_plan = decode_plan_for(inp, num_sms=128, split_waves=2, host_only=True)
+        assert host_plan.info["num_split"] > 0          # the partials go through the scratch
+        ref_o, ref_l = api.paged_decode_run(ref_plan, inp["q"], inp["k_pages"], inp["v_pages"],
+                                            inp["block_tables"], sinks=inp["sinks"])
+        out = torch.full_like(inp["q"], float("nan"))
+        lse = torch.full(inp["q"].shape[:2], float("nan"), device="cuda")
+        rc = _noalloc(host_plan, inp, out, lse)
+        assert rc == L.PKA_OK, L.lib().pka_last_error()
+        torch.cuda.synchronize()
+        diff = (out.float() - ref_o.float()).abs()
+        assert bool((diff <= O_ATOL + O_RTOL * ref_o.float().abs()).all())
+        assert bool(((lse - ref_l).abs() <= LSE_ATOL).all())
+
+
+def test_noalloc_rejects_plans_beyond_its_scratch():
+    # a host-only plan whose split partials alone exceed the 16 MiB scratch
+    plan = api.paged_decode_plan([131072] * 2, num_qo_heads=64, num_kv_heads=1, page_size=16,
+                                 max_pages_per_seq=8192, num_pages=20000, q_len=1,
+                                 num_sms=152, split_waves=8, host_only=True)
+    assert plan.workspace_bytes > 16 << 20
+    q = torch.zeros((2, 64, 128), dtype=torch.bfloat16, device="cuda")
+    pages = torch.zeros((1, 1, 16, 128), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((2, 8192), dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    inp = {"q": q, "k_pages": pages, "v_pages": pages, "block_tables": bt,
+           "seq_lens_kv": None, "sinks": None}
+    rc = _noalloc(plan, inp, out, None)
+    assert rc == L.PKA_ERR_WORKSPACE_TOO_SMALL
+    assert b"16777216" in L.lib().pka_last_error()
