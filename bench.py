@@ -35,12 +35,48 @@ UNIT = "GB/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--workload", default=None,
+                    help="profiling: time only this decode workload (llama3_8b, skewed, spec) "
+                         "or 'prefill'")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="profiling: override the workload's batch size (smaller capture)")
+    ap.add_argument("--mma-min-rows", type=int, default=0,
+                    help="decode plan: rows per KV head from which the mma kernel is used")
+    ap.add_argument("--split-waves", type=int, default=0,
+                    help="decode plan: target CTAs = split_waves x SMs (0 = library default)")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
+
+
+PLAN_OVERRIDES = {}
+
+
+def profile_case(args):
+    """One workload only (for ncu captures and sweeps); prints a short JSON line."""
+    import torch
+    from paged_kv_attention_32_gb300 import workloads as wl
+    peak_gbs, peak_tf, _ = measured_peaks()
+    if args.workload == "prefill":
+        w = wl.RAGGED_PREFILL
+        if args.batch:
+            wl.RAGGED_PREFILL = wl.shrink(w, batch=args.batch)
+        r = measure_prefill(args.seed, args.steps, args.warmup, peak_tf)
+        wl.RAGGED_PREFILL = w
+    else:
+        w = wl.DECODE_WORKLOADS[args.workload]
+        if args.batch:
+            pool = None if w.pool_pages is None else max(1000, w.pool_pages * args.batch // w.batch)
+            wl.DECODE_WORKLOADS[args.workload] = wl.shrink(w, batch=args.batch, pool_pages=pool)
+        r, _, _ = measure_workload(args.workload, args.seed, args.steps, args.warmup, peak_gbs)
+        wl.DECODE_WORKLOADS[args.workload] = w
+    torch.cuda.synchronize()
+    emit({"profile_case": args.workload, "batch": args.batch, "plan": PLAN_OVERRIDES,
+          "result": r})
 
 
 def measured_peaks():
@@ -85,11 +121,11 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.2)
         return self
 
     def __exit__(self, *exc):
@@ -129,18 +165,26 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def _oracle_task(task):
-    """Run the fp64 oracle for one request in a worker process; return seconds."""
+    """Run the fp64 oracle for one request in a worker process, repeating it
+    until `min_seconds` have passed; return (seconds, repetitions)."""
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     import oracle
-    (q_bits, k_bits, v_bits, table, seq, L, Hkv, ps, causal, W, sinks) = task
+    (q_bits, k_bits, v_bits, table, seq, L, Hkv, ps, causal, W, sinks, min_seconds) = task
     t0 = time.perf_counter()
-    oracle.paged_decode_request(0, q_bits, k_bits, v_bits, table[None], seq, 0, L, Hkv, ps,
-                                causal=causal, window_left=W, sinks=sinks)
-    return time.perf_counter() - t0
+    reps = 0
+    while True:
+        oracle.paged_decode_request(0, q_bits, k_bits, v_bits, table[None], seq, 0, L, Hkv, ps,
+                                    causal=causal, window_left=W, sinks=sinks)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            return el, reps
 
 
-def oracle_sample_tasks(inp, n_requests):
-    """Per-request oracle inputs (only the pages each request uses) for a sample."""
+def oracle_sample_tasks(inp, n_requests, min_seconds=0.0):
+    """Per-request oracle inputs (only the pages each request uses) for a sample;
+    each task repeats its request for at least `min_seconds`.  Returns the tasks
+    and the K+V bytes of one pass over each task's request."""
     import numpy as np
     import torch
     from paged_kv_attention_32_gb300 import workloads as wl
@@ -150,7 +194,7 @@ def oracle_sample_tasks(inp, n_requests):
     ind = (inp["qo_indptr"].cpu().numpy() if inp["qo_indptr"] is not None
            else np.arange(len(seq) + 1) * inp["q_len"])
     sinks = inp["sinks"].cpu().double().numpy() if inp["sinks"] is not None else None
-    tasks, nbytes = [], 0
+    tasks, nbytes = [], []
     D = inp["q"].shape[2]
     for b in range(min(n_requests, len(seq))):
         n, L = int(seq[b]), int(ind[b + 1] - ind[b])
@@ -161,26 +205,28 @@ def oracle_sample_tasks(inp, n_requests):
         qb = wl.bf16_bits(inp["q"][int(ind[b]):int(ind[b + 1])])
         W = inp["window_left"]
         first = max(0, n - L - W) if W >= 0 else 0
-        nbytes += (n - first) * inp["num_kv_heads"] * D * 4
+        nbytes.append((n - first) * inp["num_kv_heads"] * D * 4)
         tasks.append((qb, kb, vb, np.arange(npg, dtype=np.int64), np.array([n]), L,
-                      inp["num_kv_heads"], ps, inp["causal"], W, sinks))
+                      inp["num_kv_heads"], ps, inp["causal"], W, sinks, min_seconds))
     return tasks, nbytes
 
 
-def run_oracle_sample(tasks, cores):
-    """Oracle over the sample on `cores` spawned worker processes.  Returns the
-    makespan (max over workers of their summed compute seconds)."""
+def run_oracle_sample(tasks, nbytes, cores):
+    """Oracle over the sample on `cores` spawned worker processes (one task per
+    worker).  Returns (bytes processed, makespan seconds)."""
     import multiprocessing as mp
     ctx = mp.get_context("spawn")
     os.environ["OPENBLAS_NUM_THREADS"] = "1"
     os.environ["OMP_NUM_THREADS"] = "1"
     with ctx.Pool(cores) as pool:
-        secs = pool.map(_oracle_task, tasks, chunksize=1)
+        res = pool.map(_oracle_task, tasks, chunksize=1)
     loads = [0.0] * cores
-    for s in sorted(secs, reverse=True):        # longest-first packing onto the cores
-        i = loads.index(min(loads))
-        loads[i] += s
-    return max(loads)
+    done = 0
+    for (sec, reps), nb in sorted(zip(res, nbytes), key=lambda x: -x[0][0]):
+        i = loads.index(min(loads))                # longest-first packing onto the cores
+        loads[i] += sec
+        done += reps * nb
+    return done, max(loads)
 
 
 def cpu_cores():
@@ -202,6 +248,7 @@ def make_plan(inp, **kw):
         args["qo_indptr"] = inp["qo_indptr"].cpu()
     else:
         args["q_len"] = inp["q_len"]
+    args.update(PLAN_OVERRIDES)
     args.update(kw)
     return api.paged_decode_plan(inp["seq_lens_kv"].cpu(), **args)
 
@@ -340,15 +387,61 @@ def measure_prefill(seed, steps, warmup, peak_tflops):
             "tiles": plan.num_tiles}
 
 
-def cpu_baseline(inp, n_requests):
-    tasks, nbytes = oracle_sample_tasks(inp, n_requests)
-    cores = cpu_cores()
-    secs = run_oracle_sample(tasks, min(cores, len(tasks)))
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": UNIT, "cores": min(cores, len(tasks)),
+def _oracle_worker(conn, task):
+    """Long-lived oracle worker: holds one request's data, runs it on command."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    while True:
+        msg = conn.recv()
+        if msg is None:
+            return
+        conn.send(_oracle_task(task[:-1] + (msg,)))
+
+
+class OraclePool:
+    """One spawned process per sampled request (one per core); the request data
+    is shipped once, then each `step(min_seconds)` runs every worker's request
+    for at least that long.  Returns (bytes processed, makespan seconds)."""
+
+    def __init__(self, tasks, nbytes):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        os.environ["OPENBLAS_NUM_THREADS"] = "1"
+        os.environ["OMP_NUM_THREADS"] = "1"
+        self.nbytes = nbytes
+        self.procs, self.conns = [], []
+        for t in tasks:
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(b, t), daemon=True)
+            p.start()
+            self.procs.append(p)
+            self.conns.append(a)
+
+    def step(self, min_seconds):
+        for c in self.conns:
+            c.send(min_seconds)
+        res = [c.recv() for c in self.conns]
+        done = sum(reps * nb for (sec, reps), nb in zip(res, self.nbytes))
+        return done, max(sec for sec, _ in res)
+
+    def close(self):
+        for c in self.conns:
+            c.send(None)
+        for p in self.procs:
+            p.join(timeout=10)
+
+
+def cpu_baseline(inp, min_seconds=10.0):
+    tasks, nbytes = oracle_sample_tasks(inp, cpu_cores())
+    pool = OraclePool(tasks, nbytes)
+    try:
+        done, secs = pool.step(min_seconds)
+    finally:
+        pool.close()
+    return {"value": round(done / secs / 1e9, 4), "unit": UNIT, "cores": len(tasks),
             "kind": "oracle",
-            "sample": f"fp64 oracle on the first {len(tasks)} requests of the same batch "
-                      f"({nbytes / 1e6:.0f} MB of K+V), one spawned process per core, "
-                      f"{secs:.1f} s makespan"}
+            "sample": f"fp64 oracle, one spawned process per core, each repeating one of the "
+                      f"first {len(tasks)} requests of the same batch for >= {min_seconds:.0f} s "
+                      f"({done / 1e9:.2f} GB of K+V in {secs:.1f} s)"}
 
 
 def emit(line):
@@ -363,16 +456,23 @@ def reference_arm(args, rank):
     import torch
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = wl.make_decode_inputs(wl.DECODE_WORKLOADS[HEADLINE], seed=args.seed, device=dev)
-    tasks, nbytes = oracle_sample_tasks(inp, 8)
-    cores = min(cpu_cores(), len(tasks))
-    for _ in range(min(args.warmup, 1)):
-        run_oracle_sample(tasks[:cores], cores)
-    secs = [run_oracle_sample(tasks, cores) for _ in range(args.steps)]
-    total = sum(secs)
-    value = nbytes * args.steps / total / 1e9
+    tasks, nbytes = oracle_sample_tasks(inp, cpu_cores())
+    cores = len(tasks)
+    # each step: every core runs its sampled request for a slice of a ~90 s budget
+    per_step = max(0.05, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
+    pool = OraclePool(tasks, nbytes)
+    try:
+        for _ in range(args.warmup):
+            pool.step(per_step)
+        runs = [pool.step(per_step) for _ in range(args.steps)]
+    finally:
+        pool.close()
+    total = sum(s for _, s in runs)
+    value = sum(d for d, _ in runs) / total / 1e9
     cpu = {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-           "sample": f"fp64 oracle, first {len(tasks)} requests of the "
-                     f"{wl.DECODE_WORKLOADS[HEADLINE].name} batch per step"}
+           "sample": f"fp64 oracle, one spawned process per core, each repeating one of the "
+                     f"first {cores} requests of the {wl.DECODE_WORKLOADS[HEADLINE].name} batch "
+                     f"for >= {per_step:.2f} s per step"}
     emit({"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
           "ms_per_step": round(total * 1e3 / args.steps, 2), "higher_is_better": True,
@@ -403,6 +503,13 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU for the CUDA path (no CPU fallback)")
     torch.cuda.set_device(local)
+    if args.mma_min_rows:
+        PLAN_OVERRIDES["mma_min_rows"] = args.mma_min_rows
+    if args.split_waves:
+        PLAN_OVERRIDES["split_waves"] = args.split_waves
+    if args.workload is not None:
+        profile_case(args)
+        return
     peak_gbs, peak_tf, peak_kind = measured_peaks()
 
     # ---- headline: Llama-3-8B-shaped decode ----
@@ -426,10 +533,10 @@ def main():
         plan_kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
                        page_size=w.page_size, max_pages_per_seq=inp["block_tables"].shape[1],
                        num_pages=inp["k_pages"].shape[0], return_lse=w.return_lse, q_len=1)
-        e2e_ms, bin_, bout = time_decode_e2e(inp, plan_kw, min(args.steps, 10),
+        e2e_ms, bin_, bout = time_decode_e2e(inp, plan_kw, min(args.steps, 50),
                                              max(3, min(args.warmup, 3)))
         e2e_val = head["kv_bytes"] * world / (e2e_ms * 1e-3) / 1e9
-        cpu = cpu_baseline(inp, 16) if world == 1 else None
+        cpu = cpu_baseline(inp) if (world == 1 and not args.no_cpu) else None
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
