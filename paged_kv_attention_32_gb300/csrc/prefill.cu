@@ -1,13 +1,338 @@
-// Ragged causal prefill kernel (tcgen05 / TMEM).  Not built yet: the launcher
-// reports PKA_ERR_UNSUPPORTED.
+// Ragged causal prefill on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// batch_prefill (packed qo_indptr / kv_indptr): for every request and query
+// head, O = softmax(sm_scale * Q K^T + causal mask) V * output_scale, with the
+// causal diagonal bottom-right aligned (row i sees keys 0 .. Lk - Lq + i).
+//
+// One CTA = one 128-row query tile of one request for two query heads that
+// share a KV head (GQA), so every K/V tile loaded serves both heads.
+//   warp 8      TMA producer: Q tiles once, then K (2 stages) and V (1 stage)
+//               tiles of 128 keys, 128-byte swizzled, completing on mbarriers;
+//   warp 9      allocates 512 TMEM columns and issues every tcgen05.mma from
+//               one thread: S_h = Q_h K^T (M=128, N=128, K=128) into TMEM,
+//               O_h += P_h V (A = P from shared memory, B = V MN-major);
+//               the two heads ping-pong so the tensor core works on one head
+//               while the softmax of the other runs;
+//   warps 0-3   softmax of head 0, warps 4-7 softmax of head 1: one thread
+//               per query row (TMEM lane), two passes over S in TMEM (row
+//               max, then exp2 / sum / bf16 P to shared memory), lazy
+//               rescaling of O in TMEM only when the row max grew by more
+//               than 2^8, final O / l and base-2 LSE.
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
+#include <cuda_bf16.h>
+
+#include "device_common.cuh"
 #include "host_common.h"
 #include "prefill.h"
+#include "tcgen05.cuh"
 
 namespace pka {
 
-int launch_prefill(const pka_prefill_plan&, const PrefillArgs&, const CUtensorMap&,
-                   const CUtensorMap&, const CUtensorMap&, cudaStream_t) {
-  return fail(PKA_ERR_UNSUPPORTED, "the prefill kernel is not built yet");
+using namespace dev;
+
+namespace {
+
+constexpr int kTile = 128;
+constexpr uint32_t kBox = 16384;            // 128 rows x 128 bytes
+constexpr uint32_t kOffQ = 0;               // 2 heads x 32 KB
+constexpr uint32_t kOffK = 65536;           // 2 stages x 32 KB
+constexpr uint32_t kOffV = 131072;          // 1 stage x 32 KB
+constexpr uint32_t kOffP = 163840;          // 2 heads x 32 KB
+constexpr uint32_t kOffBar = 229376;
+constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
+constexpr int kThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
+
+constexpr uint32_t kColS = 0, kColO = 256;
+
+enum {
+  B_Q = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 6, B_SFULL = 7, B_PFULL = 9,
+  B_ODONE = 11, B_MMADONE = 13, B_COUNT = 14
+};
+
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);   // A, B K-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);   // A K-major, B (V) MN-major
+
+// K-major operand of 128 rows x 128 columns stored as two 16 KB boxes of
+// 64 columns: descriptor for k-step kk (16 columns).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
+  return smem_desc_sw128(base + (uint32_t)(kk >> 2) * kBox + (uint32_t)(kk & 3) * 32u, 16u, 1024u);
+}
+// V tile (keys x D) as the MN-major B operand: k-step kk covers keys 16kk..16kk+15.
+__device__ __forceinline__ uint64_t vmn_desc(uint32_t base, int kk) {
+  return smem_desc_sw128(base + (uint32_t)kk * 2048u, kBox, 1024u);
+}
+
+// A bounded wait whose outcome is the same for every lane of the warp (the
+// warp-collective tcgen05.ld/st that follow must not diverge).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
+               const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + B_COUNT * 8);
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (uint32_t)i; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const PrefillTile tile = a.tiles[blockIdx.x];
+  const int b = tile.request, h0 = tile.head, mt = tile.q_tile, n_kv = tile.n_kv;
+  const int q0 = a.qo_indptr[b], Lq = a.qo_indptr[b + 1] - q0;
+  const int k0 = a.kv_indptr[b], Lk = a.kv_indptr[b + 1] - k0;
+  const int nh = a.heads_per_cta;
+  const int hk = h0 / a.group;
+
+  if (tid == 0) {
+    mbar_init(bar(B_Q), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_PFULL + s), 128);
+      mbar_init(bar(B_ODONE + s), 1);
+    }
+    mbar_init(bar(B_VFULL), 1);
+    mbar_init(bar(B_VEMPTY), 1);
+    mbar_init(bar(B_MMADONE), 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      const int qrow = q0 + mt * kTile;
+      mbar_arrive_expect_tx(bar(B_Q), (uint32_t)nh * 2u * kBox);
+      for (int hh = 0; hh < nh; ++hh)
+        for (int half = 0; half < 2; ++half)
+          tma_load_3d(sbase + kOffQ + (uint32_t)(hh * 2 + half) * kBox, &tmq, bar(B_Q), half * 64,
+                      h0 + hh, qrow);
+      int last_k = -1, last_v = -1;
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int st = j & 1;
+        if (j >= 2) ok = mbar_wait(bar(B_KEMPTY + st), (uint32_t)(((j >> 1) - 1) & 1), a.status);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(B_KFULL + st), 2u * kBox);
+        for (int half = 0; half < 2; ++half)
+          tma_load_3d(sbase + kOffK + (uint32_t)(st * 2 + half) * kBox, &tmk, bar(B_KFULL + st),
+                      half * 64, hk, k0 + j * kTile);
+        last_k = j;
+        if (j >= 1) ok = mbar_wait(bar(B_VEMPTY), (uint32_t)((j - 1) & 1), a.status);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(B_VFULL), 2u * kBox);
+        for (int half = 0; half < 2; ++half)
+          tma_load_3d(sbase + kOffV + (uint32_t)half * kBox, &tmv, bar(B_VFULL), half * 64, hk,
+                      k0 + j * kTile);
+        last_v = j;
+      }
+      if (!ok) {   // give the copies already issued a bounded chance to land
+        mbar_wait(bar(B_Q), 0, nullptr);
+        if (last_k >= 0) mbar_wait(bar(B_KFULL + (last_k & 1)), (uint32_t)((last_k >> 1) & 1), nullptr);
+        if (last_v >= 0) mbar_wait(bar(B_VFULL), (uint32_t)(last_v & 1), nullptr);
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer (one thread) ----------------
+    if (lane == 0) {
+      auto issue_qk = [&](int hh, int st) {
+        const uint32_t d = tmem + kColS + (uint32_t)hh * 128u;
+        const uint32_t qb = sbase + kOffQ + (uint32_t)hh * 2u * kBox;
+        const uint32_t kb = sbase + kOffK + (uint32_t)st * 2u * kBox;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16(d, kmajor_desc(qb, kk), kmajor_desc(kb, kk), kIdescQK, kk > 0 ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar(B_Q), 0, a.status) && mbar_wait(bar(B_KFULL), 0, a.status);
+      if (ok) {
+        tc_fence_after();
+        for (int hh = 0; hh < nh; ++hh) {
+          issue_qk(hh, 0);
+          umma_commit(bar(B_SFULL + hh));
+        }
+        umma_commit(bar(B_KEMPTY));
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        ok = mbar_wait(bar(B_VFULL), (uint32_t)(j & 1), a.status);
+        for (int hh = 0; ok && hh < nh; ++hh) {
+          ok = mbar_wait(bar(B_PFULL + hh), (uint32_t)(j & 1), a.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tmem + kColO + (uint32_t)hh * 128u;
+          const uint32_t pb = sbase + kOffP + (uint32_t)hh * 2u * kBox;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16(d, kmajor_desc(pb, kk), vmn_desc(sbase + kOffV, kk), kIdescPV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar(B_ODONE + hh));
+          if (hh == nh - 1) umma_commit(bar(B_VEMPTY));
+          if (j + 1 < n_kv) {
+            const int st = (j + 1) & 1;
+            if (hh == 0) {
+              ok = mbar_wait(bar(B_KFULL + st), (uint32_t)(((j + 1) >> 1) & 1), a.status);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_qk(hh, st);
+            umma_commit(bar(B_SFULL + hh));
+            if (hh == nh - 1) umma_commit(bar(B_KEMPTY + st));
+          }
+        }
+      }
+      umma_commit(bar(B_MMADONE));
+      mbar_wait(bar(B_MMADONE), 0, a.status);   // nothing of ours still runs on the tensor core
+    }
+  } else if ((warp >> 2) < nh) {
+    // ---------------- softmax: one thread per query row ----------------
+    const int hh = warp >> 2, q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const int t = mt * kTile + row;
+    const bool row_valid = t < Lq;
+    const int hi = a.causal ? min(Lk, Lk - Lq + t + 1) : Lk;   // keys [0, hi) visible
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t s_tm = tmem + lane_off + kColS + (uint32_t)hh * 128u;
+    const uint32_t o_tm = tmem + lane_off + kColO + (uint32_t)hh * 128u;
+    uint8_t* p_smem = smem + kOffP + (uint32_t)hh * 2u * kBox;
+    const float sl2 = a.scale_log2;
+    float m_ref = neg_inf(), l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!(ok = warp_wait(bar(B_SFULL + hh), (uint32_t)(j & 1), a.status))) break;
+      tc_fence_after();
+      const int key0 = j * kTile;
+      const bool masked = key0 + kTile > hi;
+      // pass 1: row max of the scaled scores
+      float mx = neg_inf();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32_sync(s_tm + (uint32_t)c * 32u, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float v = __uint_as_float(r[i]) * sl2;
+          if (masked && key0 + c * 32 + i >= hi) v = neg_inf();
+          mx = fmaxf(mx, v);
+        }
+      }
+      // lazy rescale: move the reference max only when it grew by more than 2^8
+      const bool grow = mx > m_ref + kRescaleThreshold;
+      const float m_new = grow ? mx : m_ref;
+      const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
+      if (j > 0) {
+        if (!(ok = warp_wait(bar(B_ODONE + hh), (uint32_t)((j - 1) & 1), a.status))) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld32_sync(o_tm + (uint32_t)c * 32u, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(o_tm + (uint32_t)c * 32u, r);
+          }
+          tmem_wait_st();
+        }
+      }
+      m_ref = m_new;
+      // pass 2: p = exp2(s * scale * log2e - m), row sum, bf16 P (K-major, swizzled)
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32_sync(s_tm + (uint32_t)c * 32u, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float v0 = __uint_as_float(r[2 * i]) * sl2;
+          float v1 = __uint_as_float(r[2 * i + 1]) * sl2;
+          if (masked) {
+            if (key0 + c * 32 + 2 * i >= hi) v0 = neg_inf();
+            if (key0 + c * 32 + 2 * i + 1 >= hi) v1 = neg_inf();
+          }
+          const float p0 = ex2(v0 - m_ref), p1 = ex2(v1 - m_ref);
+          sum += p0 + p1;
+          pk[i] = float2_to_bf16x2(p0, p1);
+        }
+        uint8_t* blk = p_smem + (uint32_t)(c >> 1) * kBox + (uint32_t)row * 128u;
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+          const uint32_t chunk = (uint32_t)((c & 1) * 4 + qd);
+          *reinterpret_cast<uint4*>(blk + ((chunk ^ (uint32_t)(row & 7)) << 4)) =
+              make_uint4(pk[4 * qd], pk[4 * qd + 1], pk[4 * qd + 2], pk[4 * qd + 3]);
+        }
+      }
+      l = l * alpha + sum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(B_PFULL + hh));
+    }
+    if (ok && warp_wait(bar(B_ODONE + hh), (uint32_t)((n_kv - 1) & 1), a.status)) {
+      tc_fence_after();
+      const int h = h0 + hh;
+      const float inv = l > 0.f ? a.output_scale / l : 0.f;
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.out) +
+                           ((int64_t)(q0 + t) * a.num_qo_heads + h) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32_sync(o_tm + (uint32_t)c * 32u, r);
+        if (row_valid) {
+#pragma unroll
+          for (int qd = 0; qd < 4; ++qd) {
+            uint4 w;
+            w.x = float2_to_bf16x2(__uint_as_float(r[8 * qd + 0]) * inv,
+                                   __uint_as_float(r[8 * qd + 1]) * inv);
+            w.y = float2_to_bf16x2(__uint_as_float(r[8 * qd + 2]) * inv,
+                                   __uint_as_float(r[8 * qd + 3]) * inv);
+            w.z = float2_to_bf16x2(__uint_as_float(r[8 * qd + 4]) * inv,
+                                   __uint_as_float(r[8 * qd + 5]) * inv);
+            w.w = float2_to_bf16x2(__uint_as_float(r[8 * qd + 6]) * inv,
+                                   __uint_as_float(r[8 * qd + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + qd * 8) = w;
+          }
+        }
+      }
+      if (row_valid && a.lse != nullptr)
+        a.lse[(int64_t)(q0 + t) * a.num_qo_heads + h] = l > 0.f ? m_ref + log2f(l) : neg_inf();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+int launch_prefill(const pka_prefill_plan& plan, const PrefillArgs& args, const CUtensorMap& qmap,
+                   const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream) {
+  (void)plan;
+  if (args.num_tiles == 0) return PKA_OK;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
+  prefill_kernel<<<args.num_tiles, kThreads, kSmemBytes, stream>>>(args, qmap, kmap, vmap);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "prefill_kernel launch");
+  return PKA_OK;
 }
 
 }  // namespace pka

@@ -1,0 +1,88 @@
+"""Ragged causal prefill (tcgen05 kernel) against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_32_gb300 import api
+from paged_kv_attention_32_gb300 import workloads as wl
+
+from helpers import LSE_ATOL, O_ATOL, O_RTOL
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand(shape, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return torch.randn(shape, generator=g, device="cuda", dtype=torch.bfloat16)
+
+
+def _indptr(lens):
+    return torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+
+
+def _check(out, lse, ref_o, ref_l):
+    o = out.float().cpu().numpy()
+    ok = np.abs(o - ref_o) <= O_ATOL + O_RTOL * np.abs(ref_o)
+    assert ok.all(), f"max err {np.abs(o - ref_o).max():.4g} at {np.argwhere(~ok)[:4].tolist()}"
+    if lse is not None:
+        l = lse.cpu().numpy().astype(np.float64)
+        assert (np.abs(l - ref_l) <= LSE_ATOL).all(), f"LSE err {np.abs(l - ref_l).max():.4g}"
+
+
+def _run(lq, lk, Hq, Hkv, causal=True, seed=0, **kw):
+    qi, ki = _indptr(lq), _indptr(lk)
+    q = _rand((int(qi[-1]), Hq, 128), seed + 1)
+    k, v = _rand((int(ki[-1]), Hkv, 128), seed + 2), _rand((int(ki[-1]), Hkv, 128), seed + 3)
+    plan = api.batch_prefill_plan(qi, ki, num_qo_heads=Hq, num_kv_heads=Hkv, causal=causal,
+                                  return_lse=True, **kw)
+    out, lse = api.batch_prefill_run(plan, q, k, v)
+    torch.cuda.synchronize()
+    plan.check()
+    ref_o, ref_l = oracle.batch_prefill(wl.bf16_bits(q), wl.bf16_bits(k), wl.bf16_bits(v),
+                                        qi.numpy(), ki.numpy(), Hkv, causal=causal, **kw)
+    _check(out, lse, ref_o, ref_l)
+
+
+def test_prefill_smallest():
+    _run([1, 5, 130], [1, 5, 130], 4, 2)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (6, 2)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_matches_oracle(Hq, Hkv, causal):
+    lens = [1, 5, 127, 128, 129, 300, 513]
+    _run(lens, lens, Hq, Hkv, causal=causal, seed=10, output_scale=0.75)
+
+
+def test_prefill_bottom_right_causal_with_longer_kv():
+    _run([3, 130, 64], [40, 200, 64], 4, 2, seed=20, sm_scale=0.05)
+
+
+def test_prefill_full_size_sampled():
+    """The ragged prefill workload at full size (as bench.py times it), sampled rows."""
+    w = wl.RAGGED_PREFILL
+    inp = wl.make_prefill_inputs(w, seed=0, device="cuda")
+    ind = inp["qo_indptr"].cpu()
+    plan = api.batch_prefill_plan(ind, ind, num_qo_heads=w.num_qo_heads,
+                                  num_kv_heads=w.num_kv_heads, return_lse=True)
+    out, lse = api.batch_prefill_run(plan, inp["q"], inp["k"], inp["v"])
+    torch.cuda.synchronize()
+    plan.check()
+    lens = inp["lens"].tolist()
+    b = int(np.argmax(lens))
+    n = lens[b]
+    rows = sorted({0, 1, 127, 128, n // 2, n - 129, n - 1})
+    heads = [0, 5, 31]
+    qb, kb, vb = wl.bf16_bits(inp["q"]), wl.bf16_bits(inp["k"]), wl.bf16_bits(inp["v"])
+    ro, rl = oracle.prefill_request(b, qb, kb, vb, ind.numpy(), ind.numpy(), w.num_kv_heads,
+                                    heads=heads, rows=rows)
+    base = int(ind[b])
+    got_o = out[base:base + n].float().cpu().numpy()
+    got_l = lse[base:base + n].cpu().numpy()
+    for h in heads:
+        d = np.abs(got_o[rows, h] - ro[rows, h])
+        assert (d <= O_ATOL + O_RTOL * np.abs(ro[rows, h])).all(), d.max()
+        assert (np.abs(got_l[rows, h] - rl[rows, h]) <= LSE_ATOL).all()
+    assert torch.isfinite(out.float()).all()
