@@ -116,7 +116,7 @@ const char* pka_version(void);
  *                    "bind a stable runtime seq_lens tensor or let the plan
  *                    retain fixed sequence lengths").
  * num_sms            SM count the planner balances for; 0 = the device's.
- * split_waves        target CTAs = split_waves * num_sms; 0 = default (4).
+ * split_waves        target CTAs = split_waves * num_sms; 0 = default (2).
  * min_chunk_tokens   smallest split chunk in tokens; 0 = default (256).
  * mma_min_rows       the tensor-core kernel is used when
  *                    (Hq/Hkv) * max_q_len >= mma_min_rows; 0 = default (16).

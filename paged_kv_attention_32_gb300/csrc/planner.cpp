@@ -21,7 +21,7 @@
 namespace pka {
 
 namespace {
-constexpr int32_t kDefaultWaves = 4;
+constexpr int32_t kDefaultWaves = 2;
 constexpr int32_t kDefaultMinChunkTokens = 256;
 constexpr int32_t kDefaultMmaMinRows = 16;
 constexpr int32_t kMaxCudaCoreRows = 8;   // rows one warp of the CUDA-core kernel holds
