@@ -188,7 +188,9 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
   float* pw = pbuf + warp * kUnit * R;
   for (int k = 0; k < my_units; ++k) {
     const int st = k % NSTAGE;
-    if (!mbar_wait(bar_u32 + st * 8, (uint32_t)((k / NSTAGE) & 1), a.status)) break;
+    // same outcome in every lane: the shuffles below need the whole warp
+    if (!__all_sync(FULL, mbar_wait(bar_u32 + st * 8, (uint32_t)((k / NSTAGE) & 1), a.status)))
+      break;
     const uint8_t* ks = my_stages + st * kStageBytes;
     const uint8_t* vs = ks + 2 * kBoxBytes;
     const int tok0 = (unit0 + warp + k * kWarps) * kUnit;
