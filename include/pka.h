@@ -119,7 +119,7 @@ const char* pka_version(void);
  * split_waves        target CTAs = split_waves * num_sms; 0 = default (2).
  * min_chunk_tokens   smallest split chunk in tokens; 0 = default (256).
  * mma_min_rows       the tensor-core kernel is used when
- *                    (Hq/Hkv) * max_q_len >= mma_min_rows; 0 = default (16).
+ *                    (Hq/Hkv) * max_q_len >= mma_min_rows; 0 = default (8).
  * flags              PKA_PLAN_HOST_ONLY or 0.
  */
 typedef struct pka_decode_desc {

@@ -23,7 +23,7 @@ namespace pka {
 namespace {
 constexpr int32_t kDefaultWaves = 2;
 constexpr int32_t kDefaultMinChunkTokens = 256;
-constexpr int32_t kDefaultMmaMinRows = 16;
+constexpr int32_t kDefaultMmaMinRows = 8;
 constexpr int32_t kMaxCudaCoreRows = 8;   // rows one warp of the CUDA-core kernel holds
 constexpr int32_t kMaxMmaRows = 64;       // four m16 tiles
 }  // namespace

@@ -71,7 +71,8 @@ def test_kernel_choice_follows_rows_per_kv_head():
                                   mma_min_rows=mma_min_rows, host_only=True)
         return p.info["kernel"], p.info["rows_per_cta"]
     assert kernel(4, 1) == (0, 4)
-    assert kernel(8, 1) == (0, 8)
+    assert kernel(8, 1) == (1, 8)       # default threshold: 8 rows per KV head
+    assert kernel(8, 1, mma_min_rows=16) == (0, 8)
     assert kernel(8, 2) == (1, 16)
-    assert kernel(4, 3) == (1, 12)      # 9..15 rows exceed one CUDA-core warp
+    assert kernel(4, 3, mma_min_rows=16) == (1, 12)   # 9..15 rows exceed one CUDA-core warp
     assert kernel(4, 1, mma_min_rows=4) == (1, 4)
