@@ -6,19 +6,21 @@
 //
 // One CTA = one 128-row query tile of one request for two query heads that
 // share a KV head (GQA), so every K/V tile loaded serves both heads.
-//   warp 8      TMA producer: Q tiles once, then K (2 stages) and V (1 stage)
-//               tiles of 128 keys, 128-byte swizzled, completing on mbarriers;
+//   warp 8      TMA producer: Q tiles once, then K and V tiles of 128 keys
+//               (two stages each), 128-byte swizzled, completing on mbarriers;
 //   warp 9      allocates 512 TMEM columns and issues every tcgen05.mma from
 //               one thread: S_h = Q_h K^T (M=128, N=128, K=128) into TMEM,
-//               O_h += P_h V (A = P from shared memory, B = V MN-major);
-//               the two heads ping-pong so the tensor core works on one head
-//               while the softmax of the other runs;
+//               O_h += P_h V with P_h read from TMEM and V (MN-major) from
+//               shared memory; the two heads ping-pong so the tensor core
+//               works on one head while the softmax of the other runs;
 //   warps 0-3   softmax of head 0, warps 4-7 softmax of head 1: one thread
 //               per query row (TMEM lane), two passes over S in TMEM (row
-//               max, then exp2 / sum / bf16 P to shared memory), lazy
-//               rescaling of O in TMEM only when the row max grew by more
-//               than 2^8, final O / l and base-2 LSE.
-// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
+//               max of the raw scores, then p = exp2(s*scale*log2e - m) as one
+//               FFMA + MUFU, row sum, bf16 P written back over the first 64
+//               columns of S), lazy rescaling of O in TMEM only when the row
+//               max grew by more than 2^8, final O / l and base-2 LSE.
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_h
+// occupies columns [0,64) of S_h (two bf16 per column).
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
@@ -36,9 +38,8 @@ constexpr int kTile = 128;
 constexpr uint32_t kBox = 16384;            // 128 rows x 128 bytes
 constexpr uint32_t kOffQ = 0;               // 2 heads x 32 KB
 constexpr uint32_t kOffK = 65536;           // 2 stages x 32 KB
-constexpr uint32_t kOffV = 131072;          // 1 stage x 32 KB
-constexpr uint32_t kOffP = 163840;          // 2 heads x 32 KB
-constexpr uint32_t kOffBar = 229376;
+constexpr uint32_t kOffV = 131072;          // 2 stages x 32 KB
+constexpr uint32_t kOffBar = 196608;
 constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
 constexpr int kThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
@@ -46,8 +47,8 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the ma
 constexpr uint32_t kColS = 0, kColO = 256;
 
 enum {
-  B_Q = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 6, B_SFULL = 7, B_PFULL = 9,
-  B_ODONE = 11, B_MMADONE = 13, B_COUNT = 14
+  B_Q = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 7, B_SFULL = 9, B_PFULL = 11,
+  B_ODONE = 13, B_MMADONE = 15, B_COUNT = 16
 };
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);   // A, B K-major
@@ -69,7 +70,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
 prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
                const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ uint8_t smem_raw[];
@@ -92,12 +93,12 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
       mbar_init(bar(B_SFULL + s), 1);
       mbar_init(bar(B_PFULL + s), 128);
       mbar_init(bar(B_ODONE + s), 1);
     }
-    mbar_init(bar(B_VFULL), 1);
-    mbar_init(bar(B_VEMPTY), 1);
     mbar_init(bar(B_MMADONE), 1);
     fence_barrier_init();
   }
@@ -133,18 +134,18 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
           tma_load_3d(sbase + kOffK + (uint32_t)(st * 2 + half) * kBox, &tmk, bar(B_KFULL + st),
                       half * 64, hk, k0 + j * kTile);
         last_k = j;
-        if (j >= 1) ok = mbar_wait(bar(B_VEMPTY), (uint32_t)((j - 1) & 1), a.status);
+        if (j >= 2) ok = mbar_wait(bar(B_VEMPTY + st), (uint32_t)(((j >> 1) - 1) & 1), a.status);
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(B_VFULL), 2u * kBox);
+        mbar_arrive_expect_tx(bar(B_VFULL + st), 2u * kBox);
         for (int half = 0; half < 2; ++half)
-          tma_load_3d(sbase + kOffV + (uint32_t)half * kBox, &tmv, bar(B_VFULL), half * 64, hk,
-                      k0 + j * kTile);
+          tma_load_3d(sbase + kOffV + (uint32_t)(st * 2 + half) * kBox, &tmv, bar(B_VFULL + st),
+                      half * 64, hk, k0 + j * kTile);
         last_v = j;
       }
       if (!ok) {   // give the copies already issued a bounded chance to land
         mbar_wait(bar(B_Q), 0, nullptr);
         if (last_k >= 0) mbar_wait(bar(B_KFULL + (last_k & 1)), (uint32_t)((last_k >> 1) & 1), nullptr);
-        if (last_v >= 0) mbar_wait(bar(B_VFULL), (uint32_t)(last_v & 1), nullptr);
+        if (last_v >= 0) mbar_wait(bar(B_VFULL + (last_v & 1)), (uint32_t)((last_v >> 1) & 1), nullptr);
       }
     }
   } else if (warp == 9) {
@@ -168,19 +169,21 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
         umma_commit(bar(B_KEMPTY));
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        ok = mbar_wait(bar(B_VFULL), (uint32_t)(j & 1), a.status);
+        const int vst = j & 1;
+        ok = mbar_wait(bar(B_VFULL + vst), (uint32_t)((j >> 1) & 1), a.status);
         for (int hh = 0; ok && hh < nh; ++hh) {
           ok = mbar_wait(bar(B_PFULL + hh), (uint32_t)(j & 1), a.status);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d = tmem + kColO + (uint32_t)hh * 128u;
-          const uint32_t pb = sbase + kOffP + (uint32_t)hh * 2u * kBox;
+          const uint32_t p_tm = tmem + kColS + (uint32_t)hh * 128u;   // P: 64 columns, lanes 0-127
+          const uint32_t vb = sbase + kOffV + (uint32_t)vst * 2u * kBox;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_bf16(d, kmajor_desc(pb, kk), vmn_desc(sbase + kOffV, kk), kIdescPV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(d, p_tm + (uint32_t)kk * 8u, vmn_desc(vb, kk), kIdescPV,
+                         (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(B_ODONE + hh));
-          if (hh == nh - 1) umma_commit(bar(B_VEMPTY));
+          if (hh == nh - 1) umma_commit(bar(B_VEMPTY + vst));
           if (j + 1 < n_kv) {
             const int st = (j + 1) & 1;
             if (hh == 0) {
@@ -207,8 +210,7 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + kColS + (uint32_t)hh * 128u;
     const uint32_t o_tm = tmem + lane_off + kColO + (uint32_t)hh * 128u;
-    uint8_t* p_smem = smem + kOffP + (uint32_t)hh * 2u * kBox;
-    const float sl2 = a.scale_log2;
+    const float sl2 = a.scale_log2;   // >= 0 (checked by the planner)
     float m_ref = neg_inf(), l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
@@ -216,20 +218,21 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
       tc_fence_after();
       const int key0 = j * kTile;
       const bool masked = key0 + kTile > hi;
-      // pass 1: row max of the scaled scores
-      float mx = neg_inf();
+      // pass 1: row max of the raw scores (scale >= 0 keeps the order)
+      float mraw = neg_inf();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tmem_ld32_sync(s_tm + (uint32_t)c * 32u, r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          float v = __uint_as_float(r[i]) * sl2;
+          float v = __uint_as_float(r[i]);
           if (masked && key0 + c * 32 + i >= hi) v = neg_inf();
-          mx = fmaxf(mx, v);
+          mraw = fmaxf(mraw, v);
         }
       }
       // lazy rescale: move the reference max only when it grew by more than 2^8
+      const float mx = mraw == neg_inf() ? neg_inf() : mraw * sl2;
       const bool grow = mx > m_ref + kRescaleThreshold;
       const float m_new = grow ? mx : m_ref;
       const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
@@ -249,7 +252,10 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
         }
       }
       m_ref = m_new;
-      // pass 2: p = exp2(s * scale * log2e - m), row sum, bf16 P (K-major, swizzled)
+      // pass 2: p = exp2(s * scale*log2e - m) (one FFMA + MUFU), row sum, and
+      // bf16 P written over columns [16c, 16c+16) of S -- columns of chunks
+      // this thread has already read.
+      const float neg_m = -m_ref;
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -258,26 +264,19 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float v0 = __uint_as_float(r[2 * i]) * sl2;
-          float v1 = __uint_as_float(r[2 * i + 1]) * sl2;
+          float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), sl2, neg_m));
+          float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), sl2, neg_m));
           if (masked) {
-            if (key0 + c * 32 + 2 * i >= hi) v0 = neg_inf();
-            if (key0 + c * 32 + 2 * i + 1 >= hi) v1 = neg_inf();
+            if (key0 + c * 32 + 2 * i >= hi) p0 = 0.f;
+            if (key0 + c * 32 + 2 * i + 1 >= hi) p1 = 0.f;
           }
-          const float p0 = ex2(v0 - m_ref), p1 = ex2(v1 - m_ref);
           sum += p0 + p1;
           pk[i] = float2_to_bf16x2(p0, p1);
         }
-        uint8_t* blk = p_smem + (uint32_t)(c >> 1) * kBox + (uint32_t)row * 128u;
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {
-          const uint32_t chunk = (uint32_t)((c & 1) * 4 + qd);
-          *reinterpret_cast<uint4*>(blk + ((chunk ^ (uint32_t)(row & 7)) << 4)) =
-              make_uint4(pk[4 * qd], pk[4 * qd + 1], pk[4 * qd + 2], pk[4 * qd + 3]);
-        }
+        tmem_st16(s_tm + (uint32_t)c * 16u, pk);
       }
+      tmem_wait_st();
       l = l * alpha + sum;
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + hh));
     }

@@ -36,6 +36,8 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
   if (std::isnan(d.sm_scale)) d.sm_scale = 1.0f / std::sqrt((float)d.head_dim);
   PKA_CHECK_ARG(std::isfinite(d.sm_scale) && std::isfinite(d.output_scale),
                 "sm_scale and output_scale must be finite");
+  if (d.sm_scale < 0.f)
+    return fail(PKA_ERR_UNSUPPORTED, "prefill sm_scale must be >= 0 (got %g)", (double)d.sm_scale);
   PKA_CHECK_ARG(qo[0] == 0 && kv[0] == 0, "indptr arrays must start at 0");
   const int32_t B = d.batch_size;
   p.desc = d;
