@@ -70,7 +70,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
 }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
                const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ uint8_t smem_raw[];
