@@ -218,18 +218,27 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
       tc_fence_after();
       const int key0 = j * kTile;
       const bool masked = key0 + kTile > hi;
-      // pass 1: row max of the raw scores (scale >= 0 keeps the order)
+      // pass 1: row max of the raw scores (scale >= 0 keeps the order); two
+      // 32-column loads in flight per wait, three-input max
       float mraw = neg_inf();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32_sync(s_tm + (uint32_t)c * 32u, r);
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(s_tm + (uint32_t)c * 32u, ra);
+        tmem_ld32(s_tm + (uint32_t)(c + 1) * 32u, rb);
+        tmem_wait_ld();
+        reg_fence32(ra);
+        reg_fence32(rb);
+        if (masked) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = __uint_as_float(r[i]);
-          if (masked && key0 + c * 32 + i >= hi) v = neg_inf();
-          mraw = fmaxf(mraw, v);
+          for (int i = 0; i < 32; ++i) {
+            if (key0 + c * 32 + i >= hi) ra[i] = __float_as_uint(neg_inf());
+            if (key0 + (c + 1) * 32 + i >= hi) rb[i] = __float_as_uint(neg_inf());
+          }
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          mraw = fmax3(mraw, __uint_as_float(ra[i]), __uint_as_float(rb[i]));
       }
       // lazy rescale: move the reference max only when it grew by more than 2^8
       const float mx = mraw == neg_inf() ? neg_inf() : mraw * sl2;
@@ -256,11 +265,8 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
       // bf16 P written over columns [16c, 16c+16) of S -- columns of chunks
       // this thread has already read.
       const float neg_m = -m_ref;
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32_sync(s_tm + (uint32_t)c * 32u, r);
+      float sum0 = 0.f, sum1 = 0.f;
+      auto exp_chunk = [&](const uint32_t* r, int c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -270,11 +276,31 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
             if (key0 + c * 32 + 2 * i >= hi) p0 = 0.f;
             if (key0 + c * 32 + 2 * i + 1 >= hi) p1 = 0.f;
           }
-          sum += p0 + p1;
+          sum0 += p0;
+          sum1 += p1;
           pk[i] = float2_to_bf16x2(p0, p1);
         }
         tmem_st16(s_tm + (uint32_t)c * 16u, pk);
+      };
+      {
+        // the next chunk's load is in flight while this one is exponentiated
+        uint32_t ra[32], rb[32];
+        tmem_ld32_sync(s_tm, ra);
+        tmem_ld32(s_tm + 32u, rb);
+        exp_chunk(ra, 0);
+        tmem_wait_ld();
+        reg_fence32(rb);
+        tmem_ld32(s_tm + 64u, ra);
+        exp_chunk(rb, 1);
+        tmem_wait_ld();
+        reg_fence32(ra);
+        tmem_ld32(s_tm + 96u, rb);
+        exp_chunk(ra, 2);
+        tmem_wait_ld();
+        reg_fence32(rb);
+        exp_chunk(rb, 3);
       }
+      const float sum = sum0 + sum1;
       tmem_wait_st();
       l = l * alpha + sum;
       tc_fence_before();

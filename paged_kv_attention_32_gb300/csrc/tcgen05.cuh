@@ -135,15 +135,27 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Loads 32 columns and waits for them; the empty asm after the wait ties
-// every register to the wait, so no use can be scheduled before it.
-__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t* r) {
-  tmem_ld32(taddr, r);
-  tmem_wait_ld();
+// Empty asm that "redefines" 32 registers: placed after tcgen05.wait::ld it
+// ties every loaded register to the wait, so no use is scheduled before it.
+__device__ __forceinline__ void reg_fence32(uint32_t* r) {
 #pragma unroll
   for (int i = 0; i < 32; i += 8)
     asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]),
                  "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+
+// Loads 32 columns and waits for them.
+__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t* r) {
+  tmem_ld32(taddr, r);
+  tmem_wait_ld();
+  reg_fence32(r);
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
