@@ -168,19 +168,28 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
       break;
     const uint32_t k_u32 = stage_u32 + st * kStageBytes;
     const uint32_t v_u32 = k_u32 + 2 * kBoxBytes;
-    // ---- S = Q K^T : two n-tiles of 8 keys ----
-    float s[2][4];
+    // ---- S = Q K^T : two n-tiles of 8 keys; even and odd k-steps accumulate
+    // separately, so four chains of four dependent mma run side by side ----
+    float s[2][4], s2[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+    }
 #pragma unroll
-      for (int kp = 0; kp < 4; ++kp) {
+    for (int kp = 0; kp < 4; ++kp) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(k_u32 + unit_chunk_offset(nt * 8 + lm_row, kp * 4 + lm_mat), b0, b1, b2, b3);
         mma_bf16_16816(s[nt], qa[2 * kp], b0, b1);
-        mma_bf16_16816(s[nt], qa[2 * kp + 1], b2, b3);
+        mma_bf16_16816(s2[nt], qa[2 * kp + 1], b2, b3);
       }
     }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) s[nt][c] += s2[nt][c];
     // ---- mask + online softmax (base 2) ----
     const int tok0 = (unit0 + warp + k * kWarps) * kUnit;
     const bool full_unit = tok0 >= all_lo && tok0 + kUnit <= all_hi;

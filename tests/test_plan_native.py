@@ -28,7 +28,7 @@ def _cases():
         cases.append(dict(kv=kv, ql=ql, packed=packed, Hq=G * Hkv, Hkv=Hkv, ps=ps, W=W,
                           sms=rnd.choice([8, 132, 152]), waves=rnd.choice([1, 2, 4]),
                           mct=rnd.choice([128, 256, 512]), frozen=rnd.random() < 0.8,
-                          causal=rnd.random() < 0.5))
+                          causal=rnd.random() < 0.5, mma_min_rows=rnd.choice([4, 8, 16])))
     return cases
 
 
@@ -48,11 +48,12 @@ def test_native_plan_matches_spec(c):
         c["kv"], num_qo_heads=c["Hq"], num_kv_heads=c["Hkv"], page_size=ps,
         max_pages_per_seq=C, num_pages=10 ** 6, qo_indptr=indptr, q_len=1,
         causal=c["causal"], window_left=c["W"], freeze_seq_lens=c["frozen"], num_sms=c["sms"],
-        split_waves=c["waves"], min_chunk_tokens=c["mct"], host_only=True)
+        split_waves=c["waves"], min_chunk_tokens=c["mct"], mma_min_rows=c["mma_min_rows"],
+        host_only=True)
     got = plan.export()
     info = plan.info
     want = plan_spec(c["kv"], c["ql"], c["Hq"], c["Hkv"], 128, ps, c["W"], c["sms"], c["waves"],
-                     c["mct"], c["frozen"])
+                     c["mct"], c["frozen"], c["mma_min_rows"])
     assert got["items"] == [tuple(x) for x in want["items"]]
     assert got["n_chunks"] == want["n_chunks"]
     assert got["part_base"] == want["part_base"]
