@@ -60,7 +60,7 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
     # a host-only plan whose split partials alone exceed the 16 MiB scratch
     plan = api.paged_decode_plan([131072] * 2, num_qo_heads=64, num_kv_heads=1, page_size=16,
                                  max_pages_per_seq=8192, num_pages=20000, q_len=1,
-                                 num_sms=152, split_waves=8, host_only=True)
+                                 num_sms=152, split_waves=32, host_only=True)
     assert plan.workspace_bytes > 16 << 20
     q = torch.zeros((2, 64, 128), dtype=torch.bfloat16, device="cuda")
     pages = torch.zeros((1, 1, 16, 128), dtype=torch.bfloat16, device="cuda")
