@@ -363,13 +363,9 @@ int launch_mma(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMa
 
 }  // namespace
 
-int launch_decode_mma_wide(const DecodeArgs& args, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, cudaStream_t stream);
-
 int launch_decode_mma(const pka_plan& plan, const DecodeArgs& args, const CUtensorMap& kmap,
                       const CUtensorMap& vmap, cudaStream_t stream) {
   (void)plan;
-  if (args.rows_per_cta > 16) return launch_decode_mma_wide(args, kmap, vmap, stream);
   return launch_mma<2>(args, kmap, vmap, stream);
 }
 

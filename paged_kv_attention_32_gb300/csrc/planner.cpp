@@ -135,15 +135,20 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
     npages[b] = p.page_hi[b] - p.page_lo[b];
   }
 
-  // ---- chunk choice (every item is one CTA) ----
+  // ---- chunk choice: count CTAs (the mma kernel runs one CTA per 16-row tile) ----
+  std::vector<int64_t> tiles(B, 1);
+  if (p.kernel == PKA_KERNEL_MMA)
+    for (int32_t b = 0; b < B; ++b) tiles[b] = ceil_div((int64_t)p.G * qlen[b], 16);
+  int64_t tiles_sum = 0;
+  for (int32_t b = 0; b < B; ++b) tiles_sum += tiles[b];
   const int64_t max_np = *std::max_element(npages.begin(), npages.end());
   const int64_t target = (int64_t)d.split_waves * d.num_sms;
   int64_t chunk = max_np;
-  if ((int64_t)B * Hkv < target) {
+  if (tiles_sum * Hkv < target) {
     const int64_t c_min = ceil_div(d.min_chunk_tokens, ps);
     for (int64_t c = std::min(c_min, max_np); c <= max_np; ++c) {
       int64_t cnt = 0;
-      for (int32_t b = 0; b < B; ++b) cnt += ceil_div(npages[b], c);
+      for (int32_t b = 0; b < B; ++b) cnt += tiles[b] * ceil_div(npages[b], c);
       if (cnt * Hkv <= target) {
         chunk = c;
         break;

@@ -53,7 +53,7 @@ def test_native_plan_matches_spec(c):
     got = plan.export()
     info = plan.info
     want = plan_spec(c["kv"], c["ql"], c["Hq"], c["Hkv"], 128, ps, c["W"], c["sms"], c["waves"],
-                     c["mct"], c["frozen"])
+                     c["mct"], c["frozen"], c["mma_min_rows"])
     assert got["items"] == [tuple(x) for x in want["items"]]
     assert got["n_chunks"] == want["n_chunks"]
     assert got["part_base"] == want["part_base"]
