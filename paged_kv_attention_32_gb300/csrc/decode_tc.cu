@@ -5,20 +5,19 @@
 //
 // Same work items, masks, softmax and outputs as the other decode kernels.
 // One CTA per (request, KV head, chunk) holds all of the group's rows (row
-// r = i * group + g, padded to M = 128), so each K/V unit is streamed once.
-// Keys move in 16-token units (TMA, 128-byte swizzle) and are consumed in
-// groups of four units (64 keys):
-//   warp 4     TMA producer; K and V go to separate NSTAGE-deep rings laid
-//              out so that four consecutive stages form one 64-row operand;
-//   warp 5     one thread issues tcgen05.mma: S_g = Q K_g^T (M=128, N=64,
-//              K=128) into one of two 64-column TMEM buffers, one group ahead
-//              of the softmax, and O += P_g V_g (M=128, N=128, one K=16 step
-//              per unit, P read from TMEM, V MN-major);
-//   warps 0-3  stage Q once; then one thread per row (TMEM lane): per group,
-//              read 64 S columns, mask, online softmax in base 2 with lazy
+// r = i * group + g, padded to M = 128) so each K/V unit is streamed once:
+//   warps 0-3  stage Q (bf16, 128-byte swizzle) once; then one thread per
+//              row (TMEM lane): for every 16-token unit, read S (16 fp32
+//              columns) from TMEM, mask, online softmax in base 2 with lazy
 //              rescaling of O (only when the row max grew by more than 2^8),
-//              write bf16 P over the group's first 32 S columns.
-// TMEM: S buffers [0, 128), O [128, 256); 256 columns, two CTAs per SM.
+//              write bf16 P over the unit's S columns;
+//   warp 4     TMA producer: 16-token K/V units (four 2 KB boxes) through an
+//              NSTAGE-deep ring, page ids from block_tables;
+//   warp 5     one thread issues tcgen05.mma: S_u = Q K_u^T (M=128, N=16,
+//              K=128) into one of NS TMEM buffers, running NS units ahead of
+//              the softmax, and O += P_u V_u (M=128, N=128, K=16, P read from
+//              TMEM, V MN-major from shared memory).
+// TMEM: S buffers [0, 16*NS), O [128, 256); 256 columns, so two CTAs share an SM.
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
@@ -32,16 +31,24 @@ using namespace dev;
 
 namespace {
 
-constexpr int kUnit = 16;                // tokens per TMA unit
-constexpr int kGroup = 4;                // units per softmax step (64 keys)
+constexpr int kUnit = 16;
+constexpr uint32_t kStageBytes = 8192;   // K (2 boxes) + V (2 boxes)
 constexpr uint32_t kBoxBytes = 2048;     // 16 rows x 128 bytes
 constexpr uint32_t kQBytes = 32768;      // 128 rows x 256 bytes
 constexpr int kThreads = 192;
+constexpr int NS = 4;                    // S buffers in TMEM
 constexpr uint32_t kColO = 128;
 constexpr uint32_t kTmemCols = 256;
 constexpr float kRescaleThreshold = 8.0f;
 
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, 0, 0);
+// barrier indices
+// KVFULL [NSTAGE], KVEMPTY [NSTAGE], SFULL [NS], PFULL [NS], PVDONE [NS], MMADONE.
+// PV completion has one barrier per S buffer: the softmax may run up to NS
+// units ahead of the PV stream, and a single barrier waited by phase parity
+// could then alias a phase two completions back.
+enum { B_KVFULL = 0 };
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 16, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);
 
 __device__ __forceinline__ void row_key_range(int kv_len, int q_len, int i, int causal, int window,
@@ -55,33 +62,45 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
 }
 
-// Barriers: KVFULL [NSTAGE], KVEMPTY [NSTAGE], SFULL [2], PFULL [2], PVDONE [2],
-// MMADONE.  Group buffers alternate; the softmax runs at most one group ahead
-// of the PV stream, so a per-buffer barrier waited by phase parity is exact.
-template <int NSTAGE>
-struct TcBars {
-  static constexpr int KVFULL = 0, KVEMPTY = NSTAGE, SFULL = 2 * NSTAGE, PFULL = SFULL + 2,
-                       PVDONE = PFULL + 2, MMADONE = PVDONE + 2, COUNT = MMADONE + 1;
-};
+// Registers -> TMEM: 32 lanes x 8 columns of 32 bits per warp.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
+// TMEM -> registers: 32 lanes x 16 columns, waited for.
+__device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  tmem_wait_ld();
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+               "+r"(r[6]), "+r"(r[7]));
+  asm volatile("" : "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+               "+r"(r[14]), "+r"(r[15]));
+}
 
 template <int NSTAGE>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv) {
-  static_assert(NSTAGE % kGroup == 0, "a group must occupy consecutive stages");
-  using BI = TcBars<NSTAGE>;
   constexpr unsigned FULL = 0xffffffffu;
-  constexpr uint32_t kHalf = NSTAGE * kBoxBytes;   // one 64-column half of a ring
+  constexpr int B_KVEMPTY = B_KVFULL + NSTAGE, B_SFULL = B_KVEMPTY + NSTAGE;
+  constexpr int B_PFULL = B_SFULL + NS, B_PVDONE = B_PFULL + NS, B_MMADONE = B_PVDONE + NS;
+  constexpr int B_COUNT = B_MMADONE + 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t q_u32 = sbase;
-  const uint32_t kring = sbase + kQBytes;            // [half][stage][16 rows x 128 B]
-  const uint32_t vring = kring + 2 * kHalf;
-  const uint32_t bar0 = vring + 2 * kHalf;
-  uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(smem + kQBytes + 4 * kHalf + BI::COUNT * 8);
+  const uint32_t q_u32 = sbase, stage0 = sbase + kQBytes;
+  const uint32_t bar0 = stage0 + NSTAGE * kStageBytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kQBytes + NSTAGE * kStageBytes + B_COUNT * 8);
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -102,12 +121,11 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
   const int unit0 = max(it.page_lo * upp, lo_first / kUnit);
   const int unit1 = min(it.page_hi * upp, (hi_last + kUnit - 1) / kUnit);
   const int n_units = max(0, unit1 - unit0);
-  const int n_groups = (n_units + kGroup - 1) / kGroup;
   const int all_lo = lo_last, all_hi = hi_first;
 
   if (tid == 0) {
-    for (int i = 0; i < BI::COUNT; ++i)
-      mbar_init(bar(i), (i == BI::PFULL || i == BI::PFULL + 1) ? 128u : 1u);
+    for (int i = 0; i < B_COUNT; ++i)
+      mbar_init(bar(i), (i >= B_PFULL && i < B_PFULL + NS) ? 128u : 1u);
     fence_barrier_init();
   }
   if (warp == 5) {
@@ -120,8 +138,8 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
     uint4 w[16];
     if (r < rows_b) {
       const uint4* src = reinterpret_cast<const uint4*>(
-          reinterpret_cast<const __nv_bfloat16*>(a.q) +
-          (int64_t)(rq.q_start + r / G) * a.q_stride_tok + (int64_t)(hk * G + r % G) * a.q_stride_head);
+          reinterpret_cast<const __nv_bfloat16*>(a.q) + (int64_t)(rq.q_start + r / G) * a.q_stride_tok +
+          (int64_t)(hk * G + r % G) * a.q_stride_head);
 #pragma unroll
       for (int c = 0; c < 16; ++c) w[c] = __ldg(src + c);
     } else {
@@ -163,17 +181,16 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
       if (lane == 0) {
         const int st = k % NSTAGE;
         if (k >= NSTAGE)
-          ok = mbar_wait(bar(BI::KVEMPTY + st), (uint32_t)(((k / NSTAGE) - 1) & 1), a.status);
+          ok = mbar_wait(bar(B_KVEMPTY + st), (uint32_t)(((k / NSTAGE) - 1) & 1), a.status);
         if (ok) {
           const int u = unit0 + k;
           const int slot = (u % upp) * kUnit;
-          const uint32_t fb = bar(BI::KVFULL + st);
-          const uint32_t off = (uint32_t)st * kBoxBytes;
-          mbar_arrive_expect_tx(fb, 4 * kBoxBytes);
-          tma_load_4d(kring + off, &tmk, fb, 0, slot, hk, pid);
-          tma_load_4d(kring + kHalf + off, &tmk, fb, 64, slot, hk, pid);
-          tma_load_4d(vring + off, &tmv, fb, 0, slot, hk, pid);
-          tma_load_4d(vring + kHalf + off, &tmv, fb, 64, slot, hk, pid);
+          const uint32_t dst = stage0 + st * kStageBytes;
+          mbar_arrive_expect_tx(bar(B_KVFULL + st), kStageBytes);
+          tma_load_4d(dst, &tmk, bar(B_KVFULL + st), 0, slot, hk, pid);
+          tma_load_4d(dst + kBoxBytes, &tmk, bar(B_KVFULL + st), 64, slot, hk, pid);
+          tma_load_4d(dst + 2 * kBoxBytes, &tmv, bar(B_KVFULL + st), 0, slot, hk, pid);
+          tma_load_4d(dst + 3 * kBoxBytes, &tmv, bar(B_KVFULL + st), 64, slot, hk, pid);
           ++issued;
         }
       }
@@ -181,52 +198,52 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
     }
     if (lane == 0 && !ok && issued > 0) {   // bounded drain of loads already issued
       const int k = issued - 1;
-      mbar_wait(bar(BI::KVFULL + k % NSTAGE), (uint32_t)((k / NSTAGE) & 1), nullptr);
+      mbar_wait(bar(B_KVFULL + k % NSTAGE), (uint32_t)((k / NSTAGE) & 1), nullptr);
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      // S of group g: wait for its units, then 8 k-steps of N = 64 keys
-      auto issue_s = [&](int g) -> bool {
-        const int u0 = g * kGroup, nu = min(kGroup, n_units - u0);
-        for (int k = 0; k < nu; ++k) {
-          const int u = u0 + k;
-          if (!mbar_wait(bar(BI::KVFULL + u % NSTAGE), (uint32_t)((u / NSTAGE) & 1), a.status))
-            return false;
-        }
-        tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(g & 1) * 64u;
-        const uint32_t kb = kring + (uint32_t)(u0 % NSTAGE) * kBoxBytes;
+      auto issue_s = [&](int u) {
+        const uint32_t d = tmem + (uint32_t)(u % NS) * 16u;
+        const uint32_t kb = stage0 + (uint32_t)(u % NSTAGE) * kStageBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t adesc =
               smem_desc_sw128(q_u32 + (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u, 16u, 1024u);
           const uint64_t bdesc =
-              smem_desc_sw128(kb + (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u, 16u, 1024u);
+              smem_desc_sw128(kb + (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u, 16u, 1024u);
           umma_bf16(d, adesc, bdesc, kIdescS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(BI::SFULL + (g & 1)));
-        return true;
       };
       bool ok = true;
-      for (int g = 0; ok && g < n_groups && g < 2; ++g) ok = issue_s(g);
-      for (int g = 0; ok && g < n_groups; ++g) {
-        ok = mbar_wait(bar(BI::PFULL + (g & 1)), (uint32_t)((g >> 1) & 1), a.status);
+      const int pre = n_units < NS ? n_units : NS;
+      for (int u = 0; ok && u < pre; ++u) {
+        ok = mbar_wait(bar(B_KVFULL + u % NSTAGE), (uint32_t)((u / NSTAGE) & 1), a.status);
         if (!ok) break;
         tc_fence_after();
-        const int u0 = g * kGroup, nu = min(kGroup, n_units - u0);
-        const uint32_t p_tm = tmem + (uint32_t)(g & 1) * 64u;
-        for (int k = 0; k < nu; ++k) {   // one K=16 step per unit present
-          const uint32_t vb = vring + (uint32_t)((u0 + k) % NSTAGE) * kBoxBytes;
-          umma_bf16_ts(tmem + kColO, p_tm + (uint32_t)k * 8u, smem_desc_sw128(vb, kHalf, 1024u),
-                       kIdescPV, (g > 0 || k > 0) ? 1u : 0u);
-        }
-        for (int k = 0; k < nu; ++k) umma_commit(bar(BI::KVEMPTY + (u0 + k) % NSTAGE));
-        umma_commit(bar(BI::PVDONE + (g & 1)));
-        if (g + 2 < n_groups) ok = issue_s(g + 2);
+        issue_s(u);
+        umma_commit(bar(B_SFULL + u % NS));
       }
-      umma_commit(bar(BI::MMADONE));
-      mbar_wait(bar(BI::MMADONE), 0, a.status);   // nothing of ours still runs on the tensor core
+      for (int j = 0; ok && j < n_units; ++j) {
+        ok = mbar_wait(bar(B_PFULL + j % NS), (uint32_t)((j / NS) & 1), a.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vb = stage0 + (uint32_t)(j % NSTAGE) * kStageBytes + 2 * kBoxBytes;
+        umma_bf16_ts(tmem + kColO, tmem + (uint32_t)(j % NS) * 16u, smem_desc_sw128(vb, kBoxBytes, 1024u),
+                     kIdescPV, j > 0 ? 1u : 0u);
+        umma_commit(bar(B_KVEMPTY + j % NSTAGE));
+        umma_commit(bar(B_PVDONE + j % NS));   // one barrier per S buffer
+        const int u = j + NS;
+        if (u < n_units) {
+          ok = mbar_wait(bar(B_KVFULL + u % NSTAGE), (uint32_t)((u / NSTAGE) & 1), a.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(u);
+          umma_commit(bar(B_SFULL + u % NS));
+        }
+      }
+      umma_commit(bar(B_MMADONE));
+      mbar_wait(bar(B_MMADONE), 0, a.status);   // nothing of ours still runs on the tensor core
     }
   } else {
     // ---------------- softmax: one thread per row (TMEM lane) ----------------
@@ -237,45 +254,31 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
     const float sl2 = a.scale_log2;
     float m_ref = neg_inf(), l = 0.f;
     bool ok = true;
-    for (int g = 0; g < n_groups; ++g) {
-      if (!(ok = warp_wait(bar(BI::SFULL + (g & 1)), (uint32_t)((g >> 1) & 1), a.status))) break;
+    for (int j = 0; j < n_units; ++j) {
+      if (!(ok = warp_wait(bar(B_SFULL + j % NS), (uint32_t)((j / NS) & 1), a.status))) break;
       tc_fence_after();
-      const uint32_t s_tm = tmem + lane_off + (uint32_t)(g & 1) * 64u;
-      uint32_t sa[32], sb[32];
-      tmem_ld32(s_tm, sa);
-      tmem_ld32(s_tm + 32u, sb);
-      tmem_wait_ld();
-      reg_fence32(sa);
-      reg_fence32(sb);
-      const int tok0 = (unit0 + g * kGroup) * kUnit;
-      const int tok_end = unit1 * kUnit;                 // keys past the item are not loaded
-      const bool full = tok0 >= all_lo && tok0 + kGroup * kUnit <= all_hi &&
-                        tok0 + kGroup * kUnit <= tok_end;
-      float v[64];
+      const uint32_t s_tm = tmem + lane_off + (uint32_t)(j % NS) * 16u;
+      uint32_t s[16];
+      tmem_ld16_sync(s_tm, s);
+      const int tok0 = (unit0 + j) * kUnit;
+      float v[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        v[c] = __uint_as_float(sa[c]) * sl2;
-        v[32 + c] = __uint_as_float(sb[c]) * sl2;
-      }
-      if (!full) {
+      for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(s[c]) * sl2;
+      if (!(tok0 >= all_lo && tok0 + kUnit <= all_hi)) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int tok = tok0 + c;
-          if (tok < lo || tok >= hi || tok >= tok_end) v[c] = neg_inf();
-        }
+        for (int c = 0; c < 16; ++c)
+          if (tok0 + c < lo || tok0 + c >= hi) v[c] = neg_inf();
       }
       float mx = fmax3(v[0], v[1], v[2]);
 #pragma unroll
-      for (int c = 3; c < 63; c += 2) mx = fmax3(mx, v[c], v[c + 1]);
-      mx = fmaxf(mx, v[63]);
+      for (int c = 3; c < 15; c += 2) mx = fmax3(mx, v[c], v[c + 1]);
+      mx = fmaxf(mx, v[15]);
       const bool grow = mx > m_ref + kRescaleThreshold;
       const float m_new = grow ? mx : m_ref;
       const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
-      if (g > 0 && __any_sync(FULL, grow)) {
-        // O holds the groups before g: wait for PV(g-1) before rescaling
-        if (!(ok = warp_wait(bar(BI::PVDONE + ((g - 1) & 1)), (uint32_t)(((g - 1) >> 1) & 1),
-                             a.status)))
-          break;
+      if (j > 0 && __any_sync(FULL, grow)) {
+        // O holds P_0..P_{j-1} V: wait for the last of them before rescaling
+        if (!(ok = warp_wait(bar(B_PVDONE + (j - 1) % NS), (uint32_t)(((j - 1) / NS) & 1), a.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -290,68 +293,80 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
       m_ref = m_new;
       // a row that has seen no key yet keeps m = -inf; its p are exactly 0
       const float m_use = m_ref == neg_inf() ? 0.f : m_ref;
-      float sum0 = 0.f, sum1 = 0.f;
-      uint32_t pk[32];
+      float sum = 0.f;
+      uint32_t pk[8];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < 8; ++c) {
         const float p0 = ex2(v[2 * c] - m_use), p1 = ex2(v[2 * c + 1] - m_use);
-        sum0 += p0;
-        sum1 += p1;
+        sum += p0 + p1;
         pk[c] = float2_to_bf16x2(p0, p1);
       }
-      tmem_st32(s_tm, pk);   // P (bf16 pairs) over S columns already read
+      tmem_st8(s_tm, pk);
       tmem_wait_st();
-      l = l * alpha + (sum0 + sum1);
+      l = l * alpha + sum;
       tc_fence_before();
-      mbar_arrive(bar(BI::PFULL + (g & 1)));
+      mbar_arrive(bar(B_PFULL + j % NS));
     }
     // ---- epilogue: O / l (+ sink), or an fp32 partial ----
-    const bool have_o = ok && n_groups > 0 && warp_wait(bar(BI::MMADONE), 0u, a.status);
+    const bool have_o = ok && n_units > 0 &&
+                        warp_wait(bar(B_MMADONE), 0u, a.status);   // every MMA of the item is done
     if (have_o) tc_fence_after();
-    const int i = r / G, h = hk * G + r % G;
-    const int t = rq.q_start + i;
-    float sc = 0.f;
     if (r < rows_b) {   // base-2 LSE of the row (final) or of the chunk (partial)
+      const int i = r / G, h = hk * G + r % G;
       const float lse2 = l > 0.f ? m_ref + log2f(l) : neg_inf();
       if (rq.part_base < 0) {
-        float denom = l;
-        if (a.sinks != nullptr && m_ref != neg_inf()) denom += ex2(__ldg(a.sinks + h) * kLog2e - m_ref);
-        sc = denom > 0.f ? a.bmm2_scale / denom : 0.f;
-        if (a.lse != nullptr) a.lse[(int64_t)t * a.num_qo_heads + h] = lse2;
+        if (a.lse != nullptr) a.lse[(int64_t)(rq.q_start + i) * a.num_qo_heads + h] = lse2;
       } else {
-        sc = l > 0.f ? 1.f / l : 0.f;
         a.ws_lse[rq.part_base + ((int64_t)chunk * L + i) * a.num_qo_heads + h] = lse2;
       }
     }
-    if (!have_o) sc = 0.f;   // no key reached the item (or a wait gave up): zeros
+    if (have_o) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t o[32];
-      if (have_o) {
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
         tmem_ld32_sync(tmem + lane_off + kColO + (uint32_t)c * 32u, o);
-      } else {
+        if (r < rows_b) {
+          const int i = r / G, h = hk * G + r % G;
+          const int t = rq.q_start + i;
+          if (rq.part_base < 0) {
+            float denom = l;
+            if (a.sinks != nullptr && m_ref != neg_inf())
+              denom += ex2(__ldg(a.sinks + h) * kLog2e - m_ref);
+            const float sc = denom > 0.f ? a.bmm2_scale / denom : 0.f;
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                                  ((int64_t)t * a.num_qo_heads + h) * 128 + c * 32);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) o[x] = 0u;
-      }
-      if (r < rows_b) {
-        if (rq.part_base < 0) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
-                                                ((int64_t)t * a.num_qo_heads + h) * 128 + c * 32);
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[q4] = make_uint4(
+                  float2_to_bf16x2(__uint_as_float(o[8 * q4]) * sc, __uint_as_float(o[8 * q4 + 1]) * sc),
+                  float2_to_bf16x2(__uint_as_float(o[8 * q4 + 2]) * sc, __uint_as_float(o[8 * q4 + 3]) * sc),
+                  float2_to_bf16x2(__uint_as_float(o[8 * q4 + 4]) * sc, __uint_as_float(o[8 * q4 + 5]) * sc),
+                  float2_to_bf16x2(__uint_as_float(o[8 * q4 + 6]) * sc, __uint_as_float(o[8 * q4 + 7]) * sc));
+          } else {
+            const float sc = l > 0.f ? 1.f / l : 0.f;
+            const int64_t prow = rq.part_base + ((int64_t)chunk * L + i) * a.num_qo_heads + h;
+            float4* dst = reinterpret_cast<float4*>(a.ws_o + prow * 128 + c * 32);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(
-                float2_to_bf16x2(__uint_as_float(o[8 * q4]) * sc, __uint_as_float(o[8 * q4 + 1]) * sc),
-                float2_to_bf16x2(__uint_as_float(o[8 * q4 + 2]) * sc, __uint_as_float(o[8 * q4 + 3]) * sc),
-                float2_to_bf16x2(__uint_as_float(o[8 * q4 + 4]) * sc, __uint_as_float(o[8 * q4 + 5]) * sc),
-                float2_to_bf16x2(__uint_as_float(o[8 * q4 + 6]) * sc, __uint_as_float(o[8 * q4 + 7]) * sc));
-        } else {
-          const int64_t prow = rq.part_base + ((int64_t)chunk * L + i) * a.num_qo_heads + h;
-          float4* dst = reinterpret_cast<float4*>(a.ws_o + prow * 128 + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * sc, __uint_as_float(o[4 * q4 + 1]) * sc,
-                                  __uint_as_float(o[4 * q4 + 2]) * sc, __uint_as_float(o[4 * q4 + 3]) * sc);
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * sc, __uint_as_float(o[4 * q4 + 1]) * sc,
+                                    __uint_as_float(o[4 * q4 + 2]) * sc, __uint_as_float(o[4 * q4 + 3]) * sc);
+          }
         }
+      }
+    } else if (r < rows_b) {
+      // no key reached this item (or a wait gave up): zeros
+      const int i = r / G, h = hk * G + r % G;
+      const int t = rq.q_start + i;
+      if (rq.part_base < 0) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                              ((int64_t)t * a.num_qo_heads + h) * 128);
+#pragma unroll
+        for (int q4 = 0; q4 < 16; ++q4) dst[q4] = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        const int64_t prow = rq.part_base + ((int64_t)chunk * L + i) * a.num_qo_heads + h;
+        float4* dst = reinterpret_cast<float4*>(a.ws_o + prow * 128);
+#pragma unroll
+        for (int q4 = 0; q4 < 32; ++q4) dst[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
   }
@@ -367,7 +382,7 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
 template <int NSTAGE>
 int launch_tc(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMap& vmap,
               cudaStream_t stream) {
-  const size_t smem = 1024 + kQBytes + (size_t)4 * NSTAGE * kBoxBytes + 256;
+  const size_t smem = 1024 + kQBytes + (size_t)NSTAGE * kStageBytes + 256;
   auto kern = decode_tc_kernel<NSTAGE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_tc)");
