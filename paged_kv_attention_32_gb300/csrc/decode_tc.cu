@@ -42,11 +42,7 @@ constexpr uint32_t kTmemCols = 256;
 constexpr float kRescaleThreshold = 8.0f;
 
 // barrier indices
-// KVFULL [NSTAGE], KVEMPTY [NSTAGE], SFULL [NS], PFULL [NS], PVDONE [NS], MMADONE.
-// PV completion has one barrier per S buffer: the softmax may run up to NS
-// units ahead of the PV stream, and a single barrier waited by phase parity
-// could then alias a phase two completions back.
-enum { B_KVFULL = 0 };
+enum { B_KVFULL = 0 };   // [NSTAGE], then KVEMPTY [NSTAGE], SFULL [NS], PFULL [NS], PVDONE, MMADONE
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 16, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);
@@ -92,7 +88,7 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
                  const __grid_constant__ CUtensorMap tmv) {
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int B_KVEMPTY = B_KVFULL + NSTAGE, B_SFULL = B_KVEMPTY + NSTAGE;
-  constexpr int B_PFULL = B_SFULL + NS, B_PVDONE = B_PFULL + NS, B_MMADONE = B_PVDONE + NS;
+  constexpr int B_PFULL = B_SFULL + NS, B_PVDONE = B_PFULL + NS, B_MMADONE = B_PVDONE + 1;
   constexpr int B_COUNT = B_MMADONE + 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -232,7 +228,7 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
         umma_bf16_ts(tmem + kColO, tmem + (uint32_t)(j % NS) * 16u, smem_desc_sw128(vb, kBoxBytes, 1024u),
                      kIdescPV, j > 0 ? 1u : 0u);
         umma_commit(bar(B_KVEMPTY + j % NSTAGE));
-        umma_commit(bar(B_PVDONE + j % NS));   // one barrier per S buffer
+        umma_commit(bar(B_PVDONE));
         const int u = j + NS;
         if (u < n_units) {
           ok = mbar_wait(bar(B_KVFULL + u % NSTAGE), (uint32_t)((u / NSTAGE) & 1), a.status);
@@ -278,7 +274,7 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
       const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
       if (j > 0 && __any_sync(FULL, grow)) {
         // O holds P_0..P_{j-1} V: wait for the last of them before rescaling
-        if (!(ok = warp_wait(bar(B_PVDONE + (j - 1) % NS), (uint32_t)(((j - 1) / NS) & 1), a.status))) break;
+        if (!(ok = warp_wait(bar(B_PVDONE), (uint32_t)((j - 1) & 1), a.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -309,7 +305,7 @@ decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
     }
     // ---- epilogue: O / l (+ sink), or an fp32 partial ----
     const bool have_o = ok && n_units > 0 &&
-                        warp_wait(bar(B_MMADONE), 0u, a.status);   // every MMA of the item is done
+                        warp_wait(bar(B_PVDONE), (uint32_t)((n_units - 1) & 1), a.status);
     if (have_o) tc_fence_after();
     if (r < rows_b) {   // base-2 LSE of the row (final) or of the chunk (partial)
       const int i = r / G, h = hk * G + r % G;
