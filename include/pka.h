@@ -68,7 +68,6 @@ extern "C" {
 
 #define PKA_KERNEL_CUDA_CORE 0  /* decode kernel on CUDA cores (FFMA2 + shuffles) */
 #define PKA_KERNEL_MMA 1        /* decode kernel on tensor cores (mma m16n8k16)   */
-#define PKA_KERNEL_TC 2         /* decode kernel on tcgen05 / TMEM (> 16 rows)     */
 
 /* Message of the last error raised on the calling thread ("" if none). */
 const char* pka_last_error(void);
@@ -119,10 +118,8 @@ const char* pka_version(void);
  * num_sms            SM count the planner balances for; 0 = the device's.
  * split_waves        target CTAs = split_waves * num_sms; 0 = default (2).
  * min_chunk_tokens   smallest split chunk in tokens; 0 = default (256).
- * mma_min_rows       with R = (Hq/Hkv) * max_q_len query rows per KV head (at
- *                    most 128): R > 16 runs the tcgen05 kernel; otherwise the
- *                    mma.sync kernel runs when R >= mma_min_rows or R > 8, and
- *                    the CUDA-core kernel below that; 0 = default (8).
+ * mma_min_rows       the tensor-core kernel is used when
+ *                    (Hq/Hkv) * max_q_len >= mma_min_rows; 0 = default (8).
  * flags              PKA_PLAN_HOST_ONLY or 0.
  */
 typedef struct pka_decode_desc {

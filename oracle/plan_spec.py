@@ -14,11 +14,13 @@ a design choice of this library, stated here:
    is on and the plan freezes the lengths, else 0 (the window's left edge of
    row 0 -- rows below see later keys only).  Pages visited:
    ``[kv_lo // ps, ceil(n / ps))``, ``np_b`` of them.
-2. Target CTA count ``T = waves * num_sms`` (every work item is one CTA).  If
-   ``B * Hkv >= T`` no request is split: the chunk is ``max_b np_b`` pages.
-   Otherwise the chunk ``c`` is the smallest integer in ``[min(c_min, max np),
-   max np]`` with ``Hkv * sum_b ceil(np_b / c) <= T``, where
-   ``c_min = ceil(min_chunk_tokens / ps)``.
+2. CTAs per work item: ``t_b = ceil(group * L_b / 16)`` when the tensor-core
+   kernel runs (one CTA per 16-row tile of the group's query rows; it runs when
+   ``group * max L >= mma_min_rows`` or ``> 8``), else 1.  Target CTA count
+   ``T = waves * num_sms``.  If ``Hkv * sum_b t_b >= T`` no request is split:
+   the chunk is ``max_b np_b`` pages.  Otherwise the chunk ``c`` is the smallest
+   integer in ``[min(c_min, max np), max np]`` with
+   ``Hkv * sum_b t_b * ceil(np_b / c) <= T``, where ``c_min = ceil(min_chunk_tokens / ps)``.
 3. ``n_chunks_b = ceil(np_b / c)``.  Requests are visited longest first
    (``np_b`` descending, ties by ``b`` ascending); for each, chunks in order,
    and for each chunk every KV head: one work item
@@ -37,7 +39,8 @@ def _ceil_div(a, b):
 
 
 def plan_spec(seq_lens_kv, q_lens, num_qo_heads, num_kv_heads, head_dim, page_size,
-              window_left, num_sms, waves, min_chunk_tokens, freeze_seq_lens=True):
+              window_left, num_sms, waves, min_chunk_tokens, freeze_seq_lens=True,
+              mma_min_rows=8):
     """Return the plan as a dict of plain Python lists and ints (see module docstring)."""
     B = len(seq_lens_kv)
     page_lo, page_hi, npages = [], [], []
@@ -49,15 +52,19 @@ def plan_spec(seq_lens_kv, q_lens, num_qo_heads, num_kv_heads, head_dim, page_si
         page_lo.append(lo)
         page_hi.append(hi)
         npages.append(hi - lo)
+    group = num_qo_heads // num_kv_heads
+    rows = group * max(int(x) for x in q_lens)
+    mma = rows >= mma_min_rows or rows > 8
+    tiles = [_ceil_div(group * int(q_lens[b]), 16) if mma else 1 for b in range(B)]
     max_np = max(npages)
     target = waves * num_sms
-    if B * num_kv_heads >= target:
+    if num_kv_heads * sum(tiles) >= target:
         chunk = max_np
     else:
         c_min = _ceil_div(min_chunk_tokens, page_size)
         chunk = max_np
         for c in range(min(c_min, max_np), max_np + 1):
-            if num_kv_heads * sum(_ceil_div(x, c) for x in npages) <= target:
+            if num_kv_heads * sum(t * _ceil_div(x, c) for t, x in zip(tiles, npages)) <= target:
                 chunk = c
                 break
     n_chunks = [_ceil_div(x, chunk) for x in npages]

@@ -429,15 +429,11 @@ int launch_cc(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMap
 
 int launch_decode_mma(const pka_plan& plan, const DecodeArgs& args, const CUtensorMap& kmap,
                       const CUtensorMap& vmap, cudaStream_t stream);
-int launch_decode_tc(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                     cudaStream_t stream);
 
 int launch_decode(const pka_plan& plan, const DecodeArgs& args, const CUtensorMap& kmap,
                   const CUtensorMap& vmap, cudaStream_t stream) {
   int rc;
-  if (plan.kernel == PKA_KERNEL_TC) {
-    rc = launch_decode_tc(args, kmap, vmap, stream);
-  } else if (plan.kernel == PKA_KERNEL_MMA) {
+  if (plan.kernel == PKA_KERNEL_MMA) {
     rc = launch_decode_mma(plan, args, kmap, vmap, stream);
   } else if (plan.rows_per_cta <= 4) {
     rc = launch_cc<4, 3>(args, kmap, vmap, stream);

@@ -25,8 +25,7 @@ constexpr int32_t kDefaultWaves = 2;
 constexpr int32_t kDefaultMinChunkTokens = 256;
 constexpr int32_t kDefaultMmaMinRows = 8;
 constexpr int32_t kMaxCudaCoreRows = 8;   // rows one warp of the CUDA-core kernel holds
-constexpr int32_t kMaxMmaRows = 16;       // one m16 tile per CTA for the mma.sync kernel
-constexpr int32_t kMaxRows = 128;         // M of the tcgen05 kernel
+constexpr int32_t kMaxMmaRows = 64;       // four m16 tiles
 }  // namespace
 
 int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* seq,
@@ -110,17 +109,13 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
 
   // ---- kernel choice ----
   const int64_t rows = (int64_t)p.G * max_q;
-  if (rows > kMaxRows)
+  if (rows > kMaxMmaRows)
     return fail(PKA_ERR_UNSUPPORTED,
                 "(Hq/Hkv) * max_q_len = %lld query rows per KV head exceeds %d", (long long)rows,
-                kMaxRows);
+                kMaxMmaRows);
   p.rows_per_cta = (int32_t)rows;
-  if (rows > kMaxMmaRows)
-    p.kernel = PKA_KERNEL_TC;
-  else if (rows >= d.mma_min_rows || rows > kMaxCudaCoreRows)
-    p.kernel = PKA_KERNEL_MMA;
-  else
-    p.kernel = PKA_KERNEL_CUDA_CORE;
+  p.kernel = (rows >= d.mma_min_rows || rows > kMaxCudaCoreRows) ? PKA_KERNEL_MMA
+                                                                    : PKA_KERNEL_CUDA_CORE;
 
   // ---- visited pages per request ----
   const bool windowed = d.window_left >= 0 && d.freeze_seq_lens;
@@ -140,15 +135,20 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
     npages[b] = p.page_hi[b] - p.page_lo[b];
   }
 
-  // ---- chunk choice (every item is one CTA) ----
+  // ---- chunk choice: count CTAs (the mma kernel runs one CTA per 16-row tile) ----
+  std::vector<int64_t> tiles(B, 1);
+  if (p.kernel == PKA_KERNEL_MMA)
+    for (int32_t b = 0; b < B; ++b) tiles[b] = ceil_div((int64_t)p.G * qlen[b], 16);
+  int64_t tiles_sum = 0;
+  for (int32_t b = 0; b < B; ++b) tiles_sum += tiles[b];
   const int64_t max_np = *std::max_element(npages.begin(), npages.end());
   const int64_t target = (int64_t)d.split_waves * d.num_sms;
   int64_t chunk = max_np;
-  if ((int64_t)B * Hkv < target) {
+  if (tiles_sum * Hkv < target) {
     const int64_t c_min = ceil_div(d.min_chunk_tokens, ps);
     for (int64_t c = std::min(c_min, max_np); c <= max_np; ++c) {
       int64_t cnt = 0;
-      for (int32_t b = 0; b < B; ++b) cnt += ceil_div(npages[b], c);
+      for (int32_t b = 0; b < B; ++b) cnt += tiles[b] * ceil_div(npages[b], c);
       if (cnt * Hkv <= target) {
         chunk = c;
         break;

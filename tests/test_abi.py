@@ -56,7 +56,7 @@ def _plan(**kw):
     (dict(qo_indptr=[1, 2, 5]), L.PKA_ERR_INVALID_ARG),
     (dict(qo_indptr=[0, 2, 2]), L.PKA_ERR_INVALID_ARG),                 # empty packed request
     (dict(window_left=-2), L.PKA_ERR_INVALID_ARG),
-    (dict(num_qo_heads=64, num_kv_heads=1, q_len=3), L.PKA_ERR_UNSUPPORTED),  # 192 rows
+    (dict(num_qo_heads=64, num_kv_heads=1, q_len=2), L.PKA_ERR_UNSUPPORTED),  # 128 rows
 ])
 def test_plan_rejects(kw, code):
     with pytest.raises(L.PkaError) as ei:

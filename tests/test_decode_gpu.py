@@ -62,7 +62,6 @@ def test_decode_tensor_core_kernel_on_narrow_groups(name):
     (8, 8, True, 100, True),     # 64 rows, four m16 tiles
     (4, 8, True, 33, True),      # 32 rows, two m16 tiles
     (8, 3, False, -1, False),    # 24 rows, dense mask
-    (16, 8, True, 50, True),     # 128 rows: the tcgen05 kernel's full M
     (4, 3, True, 17, False),     # 12 rows: mma kernel
 ])
 def test_decode_masks_and_groups(G, L, causal, W, sinks):

@@ -57,15 +57,21 @@ def test_plan_chunk_is_minimal_under_the_target(case):
     B, T = len(kv), waves * sms
     npg = [hi - lo for lo, hi in zip(p["page_lo"], p["page_hi"])]
     c = p["chunk_pages"]
-    if B * Hkv >= T:
+    G = Hq // Hkv
+    mma0 = G * max(ql) >= 8 or G * max(ql) > 8
+    tiles0 = [math.ceil(G * q / 16) if mma0 else 1 for q in ql]
+    if Hkv * sum(tiles0) >= T:
         assert c == max(npg) and all(x == 1 for x in p["n_chunks"])
         return
-    items = Hkv * sum(math.ceil(x / c) for x in npg)
-    assert items == len(p["items"]) and items <= T
+    G = Hq // Hkv
+    mma = G * max(ql) >= 8 or G * max(ql) > 8
+    tiles = [math.ceil(G * q / 16) if mma else 1 for q in ql]
+    ctas = Hkv * sum(t * math.ceil(x / c) for t, x in zip(tiles, npg))
+    assert Hkv * sum(math.ceil(x / c) for x in npg) == len(p["items"]) and ctas <= T
     c_lo = min(math.ceil(mct / ps), max(npg))
     assert c >= c_lo
     if c > c_lo:
-        assert Hkv * sum(math.ceil(x / (c - 1)) for x in npg) > T
+        assert Hkv * sum(t * math.ceil(x / (c - 1)) for t, x in zip(tiles, npg)) > T
 
 
 @pytest.mark.parametrize("case", _cases()[:20])
