@@ -12,9 +12,9 @@
 //    scale * log2(e) so that the softmax runs on exp2;
 //  * the item's keys are cut into 16-token units; warp w owns units
 //    w, w+4, ...  Each warp streams its units through its own ring of
-//    NSTAGE shared-memory stages with TMA tensor loads (four 2 KB boxes per
-//    unit: K and V, two 64-column halves each, 128-byte swizzle) completing
-//    on an mbarrier; the page id of each unit comes from block_tables,
+//    NSTAGE shared-memory stages with TMA tensor loads (one 4 KB copy each
+//    for K and V, stored as two 64-column halves, 128-byte swizzle)
+//    completing on an mbarrier; the page id of each unit comes from block_tables,
 //    prefetched 32 units ahead into registers;
 //  * q.k: 2R lanes share one key, each holding 64/R of its 128 dims; the R
 //    partial dot products are reduced with a halving butterfly (R shuffles
@@ -176,10 +176,8 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
       const int st = k % NSTAGE;
       const uint32_t dst = stage_u32 + st * kStageBytes, bar = bar_u32 + st * 8;
       mbar_arrive_expect_tx(bar, kStageBytes);
-      tma_load_4d(dst, &tmk, bar, 0, slot, hk, pid);
-      tma_load_4d(dst + kBoxBytes, &tmk, bar, 64, slot, hk, pid);
-      tma_load_4d(dst + 2 * kBoxBytes, &tmv, bar, 0, slot, hk, pid);
-      tma_load_4d(dst + 3 * kBoxBytes, &tmv, bar, 64, slot, hk, pid);
+      tma_load_kv_unit(dst, &tmk, bar, slot, hk, pid);
+      tma_load_kv_unit(dst + 2 * kBoxBytes, &tmv, bar, slot, hk, pid);
     }
   };
   const int pre = my_units < NSTAGE ? my_units : NSTAGE;

@@ -1,0 +1,267 @@
+// One warp's share of the tensor-core decode: a 16-row query tile against a
+// stream of 16-token K/V units staged in shared memory by TMA.
+//
+// Rows of a tile are r = i*group + g (token i of the request, head g of the
+// KV head's group), as cudnn_batch_decode_with_kv_cache's q_len_per_req rows
+// with their GQA heads.  Per unit:
+//   S = Q K^T          (mma.sync m16n8k16: 2 n-tiles of 8 keys x 8 k-steps,
+//                       Q kept as A fragments in registers)
+//   mask               (causal diagonal kv_len - q_len + i, window_left)
+//   online softmax     (base 2, the scale folded into one multiply)
+//   O += P V           (P re-packed to bf16 A fragments, V via ldmatrix.trans)
+// The units are four 2 KB boxes with 128-byte swizzle: K columns 0-63,
+// K 64-127, V 0-63, V 64-127, each 16 tokens x 128 bytes.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace pka {
+namespace dev {
+
+constexpr int kMmaUnitTok = 16;
+constexpr int kMmaBoxBytes = 2048;
+constexpr int kMmaUnitBytes = 4 * kMmaBoxBytes;
+constexpr int kMmaCombStride = 136;   // floats per row of a merge buffer (padded)
+
+// Keys [lo, hi) that query row i of a request sees.
+__device__ __forceinline__ void mma_row_key_range(int kv_len, int q_len, int i, int causal,
+                                                  int window, int& lo, int& hi) {
+  const int d = kv_len - q_len + i;
+  hi = causal ? d + 1 : kv_len;
+  lo = window >= 0 ? max(0, d - window) : 0;
+}
+
+// Byte offset of 16-byte chunk cg (0..15 over the 128 dims) of token j in a
+// K or V half of a unit.
+__device__ __forceinline__ uint32_t mma_unit_chunk_offset(int j, int cg) {
+  return (uint32_t)(cg >> 3) * kMmaBoxBytes + swz128((uint32_t)j, (uint32_t)(cg & 7));
+}
+
+struct MmaTileWarp {
+  uint32_t qa[8][4];    // Q A fragments, k-step ks
+  float acc[16][4];     // O accumulators, 16 n-tiles of 8 dims
+  float mA, mB, lA, lB; // running max / sum of rows g4 and g4 + 8
+  int loA, hiA, loB, hiB;
+
+  // Loads the tile's query rows (rows past rows_b are zero and see no key).
+  __device__ __forceinline__ void init(const DecodeArgs& a, const ReqInfo& rq, int kv_len, int hk,
+                                       int tile, int lane) {
+    const int G = a.group, L = rq.q_len, rows_b = G * L;
+    const int g4 = lane >> 2, t4 = lane & 3;
+    const int rA = tile * 16 + g4, rB = rA + 8;
+    loA = 0; hiA = 0x7fffffff; loB = 0; hiB = 0x7fffffff;
+    if (rA < rows_b) mma_row_key_range(kv_len, L, rA / G, a.causal, a.window_left, loA, hiA);
+    if (rB < rows_b) mma_row_key_range(kv_len, L, rB / G, a.causal, a.window_left, loB, hiB);
+    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* srcA = nullptr;
+    const __nv_bfloat16* srcB = nullptr;
+    if (rA < rows_b)
+      srcA = qb + (int64_t)(rq.q_start + rA / G) * a.q_stride_tok +
+             (int64_t)(hk * G + rA % G) * a.q_stride_head;
+    if (rB < rows_b)
+      srcB = qb + (int64_t)(rq.q_start + rB / G) * a.q_stride_tok +
+             (int64_t)(hk * G + rB % G) * a.q_stride_head;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int c0 = ks * 16 + t4 * 2;
+      qa[ks][0] = srcA ? __ldg(reinterpret_cast<const uint32_t*>(srcA + c0)) : 0u;
+      qa[ks][1] = srcB ? __ldg(reinterpret_cast<const uint32_t*>(srcB + c0)) : 0u;
+      qa[ks][2] = srcA ? __ldg(reinterpret_cast<const uint32_t*>(srcA + c0 + 8)) : 0u;
+      qa[ks][3] = srcB ? __ldg(reinterpret_cast<const uint32_t*>(srcB + c0 + 8)) : 0u;
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    mA = mB = neg_inf();
+    lA = lB = 0.f;
+  }
+
+  // One 16-token unit: K at k_u32, V at k_u32 + 2 boxes; its first token is
+  // tok0; full_unit = every row of the tile sees all 16 keys.
+  __device__ __forceinline__ void step(uint32_t k_u32, int tok0, bool full_unit, float sl2,
+                                       int lane) {
+    constexpr unsigned FULL = 0xffffffffu;
+    const uint32_t v_u32 = k_u32 + 2 * kMmaBoxBytes;
+    const int t4 = lane & 3, lm_mat = lane >> 3, lm_row = lane & 7;
+    // S = Q K^T; even and odd k-steps accumulate separately, so four chains
+    // of four dependent mma run side by side.
+    float s[2][4], s2[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+    }
+#pragma unroll
+    for (int kp = 0; kp < 4; ++kp) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(k_u32 + mma_unit_chunk_offset(nt * 8 + lm_row, kp * 4 + lm_mat), b0, b1, b2,
+                    b3);
+        mma_bf16_16816(s[nt], qa[2 * kp], b0, b1);
+        mma_bf16_16816(s2[nt], qa[2 * kp + 1], b2, b3);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) s[nt][c] += s2[nt][c];
+    // mask + online softmax (base 2)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v = s[nt][c] * sl2;
+        if (!full_unit) {
+          const int tok = tok0 + nt * 8 + t4 * 2 + (c & 1);
+          const int lo = c >= 2 ? loB : loA, hi = c >= 2 ? hiB : hiA;
+          if (tok < lo || tok >= hi) v = neg_inf();
+        }
+        s[nt][c] = v;
+      }
+    float pmA = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    float pmB = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+    pmA = fmaxf(pmA, __shfl_xor_sync(FULL, pmA, 1));
+    pmB = fmaxf(pmB, __shfl_xor_sync(FULL, pmB, 1));
+    pmA = fmaxf(pmA, __shfl_xor_sync(FULL, pmA, 2));
+    pmB = fmaxf(pmB, __shfl_xor_sync(FULL, pmB, 2));
+    const float mAn = fmaxf(mA, pmA), mBn = fmaxf(mB, pmB);
+    const float uA = mAn == neg_inf() ? 0.f : mAn, uB = mBn == neg_inf() ? 0.f : mBn;
+    const float alA = ex2(mA - uA), alB = ex2(mB - uB);
+    mA = mAn;
+    mB = mBn;
+    float sumA = 0.f, sumB = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = ex2(s[nt][0] - uA);
+      s[nt][1] = ex2(s[nt][1] - uA);
+      s[nt][2] = ex2(s[nt][2] - uB);
+      s[nt][3] = ex2(s[nt][3] - uB);
+      sumA += s[nt][0] + s[nt][1];
+      sumB += s[nt][2] + s[nt][3];
+    }
+    lA = lA * alA + sumA;
+    lB = lB * alB + sumB;
+    if (__any_sync(FULL, alA != 1.f || alB != 1.f)) {
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        acc[n][0] *= alA;
+        acc[n][1] *= alA;
+        acc[n][2] *= alB;
+        acc[n][3] *= alB;
+      }
+    }
+    uint32_t pa[4];
+    pa[0] = float2_to_bf16x2(s[0][0], s[0][1]);
+    pa[1] = float2_to_bf16x2(s[0][2], s[0][3]);
+    pa[2] = float2_to_bf16x2(s[1][0], s[1][1]);
+    pa[3] = float2_to_bf16x2(s[1][2], s[1][3]);
+    // O += P V : 16 n-tiles of 8 dims
+#pragma unroll
+    for (int np = 0; np < 8; ++np) {
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4_trans(v_u32 + mma_unit_chunk_offset((lm_mat & 1) * 8 + lm_row,
+                                                      np * 2 + (lm_mat >> 1)),
+                        b0, b1, b2, b3);
+      mma_bf16_16816(acc[2 * np], pa, b0, b1);
+      mma_bf16_16816(acc[2 * np + 1], pa, b2, b3);
+    }
+  }
+
+  // Sums l over the quad of lanes that share a row.
+  __device__ __forceinline__ void reduce_l() {
+    constexpr unsigned FULL = 0xffffffffu;
+    lA += __shfl_xor_sync(FULL, lA, 1);
+    lA += __shfl_xor_sync(FULL, lA, 2);
+    lB += __shfl_xor_sync(FULL, lB, 1);
+    lB += __shfl_xor_sync(FULL, lB, 2);
+  }
+
+  // Writes (O, m, l) of the 16 rows to merge slot `slot` of the buffers
+  // comb_o [slots][16][kMmaCombStride], comb_m / comb_l [slots][16].
+  __device__ __forceinline__ void store_comb(float* comb_o, float* comb_m, float* comb_l, int slot,
+                                             int lane) const {
+    const int g4 = lane >> 2, t4 = lane & 3;
+    float* oA = comb_o + (slot * 16 + g4) * kMmaCombStride + t4 * 2;
+    float* oB = oA + 8 * kMmaCombStride;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      *reinterpret_cast<float2*>(oA + n * 8) = make_float2(acc[n][0], acc[n][1]);
+      *reinterpret_cast<float2*>(oB + n * 8) = make_float2(acc[n][2], acc[n][3]);
+    }
+    if (t4 == 0) {
+      comb_m[slot * 16 + g4] = mA;
+      comb_l[slot * 16 + g4] = lA;
+      comb_m[slot * 16 + g4 + 8] = mB;
+      comb_l[slot * 16 + g4 + 8] = lB;
+    }
+  }
+};
+
+// Combines merge slots [slot0, slot0 + nslots) for row `row` of tile `tile`
+// (dims d0 .. d0+15) and writes the final bf16 O and base-2 LSE (sink added
+// to the denominator, bmm2_scale applied) or, for a split request, the fp32
+// partial (O/l, m + log2 l) of chunk `chunk`.
+__device__ __forceinline__ void mma_combine_store(const DecodeArgs& a, const ReqInfo& rq,
+                                                  const float* comb_o, const float* comb_m,
+                                                  const float* comb_l, int slot0, int nslots,
+                                                  int tile, int row, int d0, int hk, int chunk) {
+  const int G = a.group, L = rq.q_len;
+  const int r = tile * 16 + row;
+  if (r >= G * L) return;
+  float m = neg_inf();
+  for (int w = 0; w < nslots; ++w) m = fmaxf(m, comb_m[(slot0 + w) * 16 + row]);
+  float o[16];
+#pragma unroll
+  for (int x = 0; x < 16; ++x) o[x] = 0.f;
+  float lsum = 0.f;
+  if (m != neg_inf()) {
+    for (int w = 0; w < nslots; ++w) {
+      const float mw = comb_m[(slot0 + w) * 16 + row];
+      if (mw == neg_inf()) continue;
+      const float f = ex2(mw - m);
+      lsum += comb_l[(slot0 + w) * 16 + row] * f;
+      const float* src = comb_o + ((slot0 + w) * 16 + row) * kMmaCombStride + d0;
+#pragma unroll
+      for (int x = 0; x < 16; x += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src + x);
+        o[x] += v.x * f;
+        o[x + 1] += v.y * f;
+        o[x + 2] += v.z * f;
+        o[x + 3] += v.w * f;
+      }
+    }
+  }
+  const int i = r / G, h = hk * G + r % G;
+  const int t = rq.q_start + i;
+  if (rq.part_base < 0) {
+    float denom = lsum;
+    if (a.sinks != nullptr && m != neg_inf()) denom += ex2(__ldg(a.sinks + h) * kLog2e - m);
+    const float sc = denom > 0.f ? a.bmm2_scale / denom : 0.f;
+    uint4 w0, w1;
+    w0.x = float2_to_bf16x2(o[0] * sc, o[1] * sc);
+    w0.y = float2_to_bf16x2(o[2] * sc, o[3] * sc);
+    w0.z = float2_to_bf16x2(o[4] * sc, o[5] * sc);
+    w0.w = float2_to_bf16x2(o[6] * sc, o[7] * sc);
+    w1.x = float2_to_bf16x2(o[8] * sc, o[9] * sc);
+    w1.y = float2_to_bf16x2(o[10] * sc, o[11] * sc);
+    w1.z = float2_to_bf16x2(o[12] * sc, o[13] * sc);
+    w1.w = float2_to_bf16x2(o[14] * sc, o[15] * sc);
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                          ((int64_t)t * a.num_qo_heads + h) * 128 + d0);
+    dst[0] = w0;
+    dst[1] = w1;
+    if (a.lse != nullptr && d0 == 0)
+      a.lse[(int64_t)t * a.num_qo_heads + h] = lsum > 0.f ? m + log2f(lsum) : neg_inf();
+  } else {
+    const int64_t prow = rq.part_base + ((int64_t)chunk * L + i) * a.num_qo_heads + h;
+    const float sc = lsum > 0.f ? 1.f / lsum : 0.f;
+    float4* dst = reinterpret_cast<float4*>(a.ws_o + prow * 128 + d0);
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+      dst[x] = make_float4(o[4 * x] * sc, o[4 * x + 1] * sc, o[4 * x + 2] * sc, o[4 * x + 3] * sc);
+    if (d0 == 0) a.ws_lse[prow] = lsum > 0.f ? m + log2f(lsum) : neg_inf();
+  }
+}
+
+}  // namespace dev
+}  // namespace pka

@@ -91,6 +91,27 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 5-D tiled load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+                                            int32_t c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+      : "memory");
+}
+
+// Loads one 16-token unit of an HND K or V pool (map from encode_kv_pool_map)
+// into 4 KB at dst: two 2 KB halves (dims 0-63, then 64-127), each 16 rows of
+// 128 bytes with 128-byte swizzle.  One copy instruction per unit: the
+// issuing thread's cost is per instruction, not per byte.
+__device__ __forceinline__ void tma_load_kv_unit(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int32_t slot, int32_t head,
+                                                 int32_t page) {
+  tma_load_5d(dst, map, bar, 0, slot, 0, head, page);
+}
+
 // 3-D tiled load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t c0, int32_t c1, int32_t c2) {

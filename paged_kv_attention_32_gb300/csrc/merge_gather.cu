@@ -65,8 +65,8 @@ merge_states_kernel(const float* __restrict__ v, const float* __restrict__ s, in
 constexpr int kUnit = 16;
 constexpr int kBoxBytes = 2048;
 
-// One warp, one 16-token unit at a time: the same four-box TMA unit load and
-// swizzled reads the decode kernels use (here for one pool only).
+// One warp, one 16-token unit at a time: the same TMA unit load and swizzled
+// reads the decode kernels use (here for one pool only).
 __global__ void __launch_bounds__(32)
 paged_gather_kernel(const __grid_constant__ CUtensorMap map, const int32_t* __restrict__ table,
                     int page_size, int tok_begin, int tok_end, int kv_head,
@@ -88,8 +88,7 @@ paged_gather_kernel(const __grid_constant__ CUtensorMap map, const int32_t* __re
     if (lane == 0) {
       const uint32_t dst = smem_u32(buf);
       mbar_arrive_expect_tx(bar_u32, 2 * kBoxBytes);
-      tma_load_4d(dst, &map, bar_u32, 0, (u % upp) * kUnit, kv_head, pid);
-      tma_load_4d(dst + kBoxBytes, &map, bar_u32, 64, (u % upp) * kUnit, kv_head, pid);
+      tma_load_kv_unit(dst, &map, bar_u32, (u % upp) * kUnit, kv_head, pid);
     }
     if (!mbar_wait(bar_u32, phase, status)) return;
     phase ^= 1u;

@@ -56,14 +56,16 @@ int encode_kv_pool_map(CUtensorMap* map, const void* pool, int64_t num_pages, in
                        int32_t page_size, int32_t head_dim, int64_t stride_page,
                        int64_t stride_head) {
   PKA_CHECK_ARG(stride_head > 0 && stride_page > 0, "K/V strides must be positive");
-  const uint64_t dims[4] = {(uint64_t)head_dim, (uint64_t)page_size, (uint64_t)num_heads,
-                            (uint64_t)num_pages};
-  const uint64_t strides[3] = {(uint64_t)head_dim * 2, (uint64_t)stride_head * 2,
+  PKA_CHECK_ARG(head_dim == 128, "the K/V pool map takes head_dim 128 (got %d)", head_dim);
+  // The 128 columns are split as (d_lo 0..63, d_hi 0..1) and d_hi is placed
+  // after the slot dimension: (d_lo, slot, d_hi, head, page).  A box of
+  // {64, 16, 2, 1, 1} then lands in shared memory as the two 64-column halves
+  // of 16 token rows one after the other -- a whole 16-token unit in one copy.
+  const uint64_t dims[5] = {64, (uint64_t)page_size, 2, (uint64_t)num_heads, (uint64_t)num_pages};
+  const uint64_t strides[4] = {(uint64_t)head_dim * 2, 128, (uint64_t)stride_head * 2,
                                (uint64_t)stride_page * 2};
-  // box: 16 token slots x 64 columns of one (page, head) block; a page of
-  // page_size slots is read as page_size / 16 such units, two boxes per unit.
-  const uint32_t box[4] = {64, 16, 1, 1};
-  return encode_bf16_map(map, pool, 4, dims, strides, box);
+  const uint32_t box[5] = {64, 16, 2, 1, 1};
+  return encode_bf16_map(map, pool, 5, dims, strides, box);
 }
 
 }  // namespace pka

@@ -18,8 +18,9 @@ namespace pka {
 int encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                     const uint64_t* strides, const uint32_t* box);
 
-// Tensor map over an HND page pool (page, kv_head, slot, d): the box is 16
-// token slots x 64 columns of one (page, head) block; two boxes cover D=128.
+// Tensor map over an HND page pool (page, kv_head, slot, d), D = 128, as the
+// 5-D view (d_lo, slot, d_hi, head, page): one box is a 16-token unit of one
+// (page, head) block, 4 KB, stored as its two 64-column halves.
 int encode_kv_pool_map(CUtensorMap* map, const void* pool, int64_t num_pages, int32_t num_heads,
                        int32_t page_size, int32_t head_dim, int64_t stride_page,
                        int64_t stride_head);

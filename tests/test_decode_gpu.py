@@ -74,6 +74,28 @@ def test_decode_masks_and_groups(G, L, causal, W, sinks):
     assert_close(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("G,L,packed,split", [
+    (8, 3, False, False),   # 24 rows: two tiles, the second half empty
+    (8, 6, True, True),     # up to 48 rows, requests with 1..3 live tiles, split chunks
+    (8, 8, False, True),    # 64 rows: four tiles
+    (4, 5, True, False),    # 20 rows, packed lengths 1..5
+])
+def test_decode_wide_groups(G, L, packed, split):
+    """17-64 rows per KV head: one mma CTA per live 16-row tile of every item."""
+    w = wl.DecodeWorkload(name="wide", batch=7, num_qo_heads=2 * G, num_kv_heads=2, head_dim=128,
+                          page_size=16, kv_len_range=(L, 1500),
+                          q_len_range=(1, L) if packed else (L, L), packed_q=packed, causal=True,
+                          window_left=300 if split else -1, sinks=True)
+    inp = wl.make_decode_inputs(w, seed=12, device=DEV)
+    kw = dict(num_sms=48, split_waves=2, min_chunk_tokens=128) if split else {}
+    out, lse, plan = run_decode(inp, **kw)
+    assert plan.info["kernel"] == 1
+    if split:
+        assert plan.info["num_split"] > 0
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
 def test_decode_page_size_64_and_bmm2_scale():
     w = wl.DecodeWorkload(name="ps64", batch=4, num_qo_heads=8, num_kv_heads=2, head_dim=128,
                           page_size=64, kv_len_range=(1, 900), bmm2_scale=0.5)
