@@ -28,6 +28,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HEADLINE = "llama3_8b"
+# DRAM read + write bytes of one headline decode launch (decode_cc_kernel<4,3>,
+# seed 0, one GB300) from an ncu capture of this same command; the full
+# command and numbers are in profiles/decode_cc_kernel_llama3_8b_full_traffic.md.
+# Other seeds or ranks scale it by their algorithmic K+V bytes.
+NCU_TRAFFIC = {"kernel": "decode_cuda_core_kernel", "kv_bytes": 1128361984,
+               "dram_bytes": 1134495232}
 METRIC = "paged decode effective KV HBM GB/s"
 UNIT = "GB/s"
 
@@ -338,6 +344,14 @@ def time_decode_e2e(inp, plan_kw, steps, warmup):
     return (time.perf_counter() - t0) * 1e3 / steps, bytes_in, bytes_out
 
 
+def headline_traffic(head):
+    """DRAM bytes per headline launch from the ncu capture, scaled to this call's K+V bytes
+    (None when the plan runs another kernel than the one captured)."""
+    if f"decode_{head['kernel']}_kernel" != NCU_TRAFFIC["kernel"]:
+        return None
+    return int(round(NCU_TRAFFIC["dram_bytes"] * head["kv_bytes"] / NCU_TRAFFIC["kv_bytes"]))
+
+
 def measure_workload(name, seed, steps, warmup, peak_gbs, dist=None):
     """Inputs drawn on the GPU, plan, device timing; returns (result dict, inp, plan)."""
     from paged_kv_attention_32_gb300 import workloads as wl
@@ -551,7 +565,7 @@ def main():
             "roofline": {"bound": "hbm", "kernel": f"decode_{head['kernel']}_kernel",
                          "achieved": round(gbs_kernel, 1), "peak": peak_gbs, "unit": "GB/s",
                          "frac": round(gbs_kernel / peak_gbs, 4), "peak_source": peak_kind,
-                         "traffic": None},
+                         "traffic": headline_traffic(head)},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
                     "h2d_bytes_per_step": bin_, "d2h_bytes_per_step": bout,
