@@ -233,7 +233,7 @@ def merge_states(v_states, s_states):
 # ---------------------------------------------------------------------------
 
 def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads, causal=True,
-                    sm_scale=None, output_scale=1.0, heads=None, rows=None):
+                    sm_scale=None, output_scale=1.0, heads=None, rows=None, window_left=-1):
     """Prefill output of request ``b``: ``(O [Lq, Hq, D], LSE [Lq, Hq])``.
 
     Packed storage: request ``b`` owns query rows ``qo_indptr[b] ..
@@ -242,7 +242,10 @@ def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_head
     masking is bottom-right aligned, so query row ``i`` sees keys
     ``0 .. Lk - Lq + i``.  ``sm_scale`` defaults to ``1/sqrt(D)`` and
     ``output_scale`` multiplies the output.  ``heads``/``rows`` restrict the
-    computation to a subset (others are NaN).
+    computation to a subset (others are NaN).  ``window_left`` (``batch_prefill``
+    lists it; the page's head-paired policy for it is undefined, so this is the
+    plain sliding window of the decode pages): row ``i`` keeps the keys from
+    ``Lk - Lq + i - window_left`` on, as ``decode_row_key_range`` states.
     """
     Hq, D = q_bits.shape[1], q_bits.shape[2]
     group = Hq // num_kv_heads
@@ -256,10 +259,10 @@ def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_head
     O = np.full((Lq, Hq, D), np.nan)
     LSE = np.full((Lq, Hq), np.nan)
     keys = np.arange(Lk)
-    if causal:
-        allowed = np.stack([keys <= Lk - Lq + i for i in rows]) if len(rows) else np.zeros((0, Lk), bool)
-    else:
-        allowed = np.ones((len(rows), Lk), dtype=bool)
+    allowed = np.zeros((len(rows), Lk), dtype=bool)
+    for r, i in enumerate(rows):
+        lo, hi = decode_row_key_range(Lk, Lq, int(i), causal, window_left)
+        allowed[r] = (keys >= lo) & (keys < hi)
     for h in heads:
         hk = h // group
         Q = bf16_bits_to_f64(q_bits[q0 + rows, h, :])
@@ -272,7 +275,7 @@ def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_head
 
 
 def batch_prefill(q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads, causal=True,
-                  sm_scale=None, output_scale=1.0):
+                  sm_scale=None, output_scale=1.0, window_left=-1):
     """Ragged prefill over the whole batch: ``(O [total_q, Hq, D], LSE [total_q, Hq])``."""
     total_q, Hq, D = q_bits.shape
     O = np.zeros((total_q, Hq, D))
@@ -280,7 +283,7 @@ def batch_prefill(q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads, ca
     for b in range(len(qo_indptr) - 1):
         q0, q1 = int(qo_indptr[b]), int(qo_indptr[b + 1])
         o, lse = prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads,
-                                 causal, sm_scale, output_scale)
+                                 causal, sm_scale, output_scale, window_left=window_left)
         O[q0:q1] = o
         LSE[q0:q1] = lse
     return O, LSE

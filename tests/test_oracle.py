@@ -421,3 +421,52 @@ def test_prefill_row_and_head_subsets_agree_with_full():
                                   heads=[2], rows=[0, 44, 7])
     for r in (0, 44, 7):
         assert np.array_equal(o[r, 2], O[20 + r, 2]) and l[r, 2] == lse[20 + r, 2]
+
+
+@pytest.mark.parametrize("causal,W", [(True, 0), (True, 5), (True, 40), (False, 7)])
+def test_prefill_window_matches_torch_sdpa_band(causal, W):
+    """Prefill window_left: torch SDPA with a band mask built by tril/triu."""
+    lens_q, lens_k = [33, 1, 70], [40, 1, 70]
+    Hq, Hkv, D = 4, 2, 128
+    qi = np.concatenate([[0], np.cumsum(lens_q)])
+    ki = np.concatenate([[0], np.cumsum(lens_k)])
+    q = _rand_bf16((int(qi[-1]), Hq, D), 230)
+    k = _rand_bf16((int(ki[-1]), Hkv, D), 231)
+    v = _rand_bf16((int(ki[-1]), Hkv, D), 232)
+    O, lse = oracle.batch_prefill(_bits(q), _bits(k), _bits(v), qi, ki, Hkv, causal=causal,
+                                  window_left=W)
+    for b in range(3):
+        a, e, ka, kb = qi[b], qi[b + 1], ki[b], ki[b + 1]
+        L, n = e - a, kb - ka
+        mask = _bottom_right_mask(L, n, causal, W)
+        for h in range(Hq):
+            hk = h // 2
+            ref = F.scaled_dot_product_attention(
+                q.double()[a:e, h][None, None], k.double()[ka:kb, hk][None, None],
+                v.double()[ka:kb, hk][None, None], attn_mask=mask[None, None])[0, 0]
+            assert np.allclose(O[a:e, h], ref.numpy(), atol=1e-12)
+
+
+def test_prefill_window_zero_returns_diagonal_value_row():
+    """window_left = 0 with the causal mask: row i sees only key Lk - Lq + i."""
+    lq, lk = [5], [9]
+    q = _rand_bf16((5, 2, 128), 240)
+    k = _rand_bf16((9, 1, 128), 241)
+    v = _rand_bf16((9, 1, 128), 242)
+    O, lse = oracle.batch_prefill(_bits(q), _bits(k), _bits(v), np.array([0, 5]),
+                                  np.array([0, 9]), 1, causal=True, window_left=0)
+    for i in range(5):
+        assert np.array_equal(O[i, 0], v.double()[4 + i, 0].numpy())
+        s = float((q.double()[i, 1] @ k.double()[4 + i, 0])) / math.sqrt(128)
+        assert abs(lse[i, 1] - s * LOG2E) < 1e-12
+
+
+def test_prefill_window_at_least_kv_len_is_no_window():
+    lens = [20, 45]
+    ind = np.concatenate([[0], np.cumsum(lens)])
+    q = _rand_bf16((65, 2, 128), 250)
+    k = _rand_bf16((65, 1, 128), 251)
+    v = _rand_bf16((65, 1, 128), 252)
+    a = oracle.batch_prefill(_bits(q), _bits(k), _bits(v), ind, ind, 1, window_left=45)
+    b = oracle.batch_prefill(_bits(q), _bits(k), _bits(v), ind, ind, 1)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
