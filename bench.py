@@ -28,6 +28,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HEADLINE = "llama3_8b"
+PREFILL_WINDOW = 2047   # sliding-window variant of the ragged prefill (2048 keys per row)
 # DRAM read + write bytes of one headline decode launch (decode_cc_kernel<4,3>,
 # seed 0, one GB300) from an ncu capture of this same command; the full
 # command and numbers are in profiles/decode_cc_kernel_llama3_8b_full_traffic.md.
@@ -369,18 +370,26 @@ def measure_workload(name, seed, steps, warmup, peak_gbs, dist=None):
     return res, inp, plan
 
 
-def measure_prefill(seed, steps, warmup, peak_tflops):
+def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1):
+    """Ragged causal prefill; FLOPs = 4 * D per unmasked (query, key) pair per query head
+    (with a window, row i of a request keeps min(i + 1, window_left + 1) keys)."""
     import torch
     from paged_kv_attention_32_gb300 import api
     from paged_kv_attention_32_gb300 import workloads as wl
     w = wl.RAGGED_PREFILL
     inp = wl.make_prefill_inputs(w, seed=seed, device="cuda")
     lens = inp["lens"].tolist()
-    pairs = sum(n * (n + 1) // 2 for n in lens)
+    if window_left >= 0:
+        W1 = window_left + 1
+        pairs = sum(min(n, W1) * (min(n, W1) + 1) // 2 + max(0, n - W1) * W1 for n in lens)
+    else:
+        pairs = sum(n * (n + 1) // 2 for n in lens)
     flops = 4 * 128 * pairs * w.num_qo_heads
+    name = w.name + (f" window_left={window_left}" if window_left >= 0 else "")
     try:
         plan = api.batch_prefill_plan(inp["qo_indptr"].cpu(), inp["kv_indptr"].cpu(),
-                                      num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads)
+                                      num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
+                                      window_left=window_left)
         out = torch.empty_like(inp["q"])
         for _ in range(warmup):
             api.batch_prefill_run(plan, inp["q"], inp["k"], inp["v"], out=out)
@@ -394,9 +403,9 @@ def measure_prefill(seed, steps, warmup, peak_tflops):
         plan.check()
         ms = e0.elapsed_time(e1) / steps
     except Exception as exc:   # reported, not hidden: the line says why there is no number
-        return {"workload": w.name, "status": f"not measured: {exc}", "flops": flops}
+        return {"workload": name, "status": f"not measured: {exc}", "flops": flops}
     tf = flops / (ms * 1e-3) / 1e12
-    return {"workload": w.name, "ms_per_call": round(ms, 4), "flops": flops,
+    return {"workload": name, "ms_per_call": round(ms, 4), "flops": flops,
             "TFLOP_per_s": round(tf, 1), "frac_of_measured_bf16": round(tf / peak_tflops, 4),
             "tiles": plan.num_tiles}
 
@@ -585,6 +594,8 @@ def main():
             del i2, p2
             torch.cuda.empty_cache()
         extra["prefill"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf)
+        extra["prefill_window"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf,
+                                                  window_left=PREFILL_WINDOW)
         line["decode_headline"] = head
         line["other_workloads"] = extra
     if rank == 0:

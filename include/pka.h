@@ -311,7 +311,10 @@ int attn_merge_lse(const float* v_states, const float* s_states, int32_t num_sta
 /*
  * batch_size, num_qo_heads, num_kv_heads, head_dim (128) as for decode.
  * mask         PKA_MASK_CAUSAL (bottom-right aligned) or PKA_MASK_DENSE.
- * window_left  must be -1 (the page's windowed GQA policy is not built).
+ * window_left  -1 disables; W >= 0 keeps, for query row i of a request with
+ *              Lq rows and Lk keys, the keys from Lk - Lq + i - W on (the plain
+ *              sliding window of the decode entry points; batch_prefill lists
+ *              window_left, and its head-paired GQA policy is not built).
  * sm_scale     NaN selects 1/sqrt(D) (batch_prefill, sm_scale).
  * output_scale multiplies O (batch_prefill, output_scale).
  * return_lse   nonzero: batch_prefill_run writes the base-2 LSE.

@@ -378,6 +378,7 @@ int batch_prefill_run(const pka_prefill_plan* p, const void* q, int64_t q_stride
   a.num_kv_heads = p->Hkv;
   a.group = p->G;
   a.causal = p->desc.mask == PKA_MASK_CAUSAL;
+  a.window_left = p->desc.window_left;
   a.heads_per_cta = p->heads_per_cta;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.output_scale = p->desc.output_scale;

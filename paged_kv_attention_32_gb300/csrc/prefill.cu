@@ -2,7 +2,8 @@
 //
 // batch_prefill (packed qo_indptr / kv_indptr): for every request and query
 // head, O = softmax(sm_scale * Q K^T + causal mask) V * output_scale, with the
-// causal diagonal bottom-right aligned (row i sees keys 0 .. Lk - Lq + i).
+// causal diagonal bottom-right aligned (row i sees keys 0 .. Lk - Lq + i) and
+// an optional left window (window_left = W >= 0: keys from Lk - Lq + i - W on).
 //
 // One CTA = one 128-row query tile of one request for two query heads that
 // share a KV head (GQA), so every K/V tile loaded serves both heads.
@@ -83,6 +84,7 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PrefillTile tile = a.tiles[blockIdx.x];
   const int b = tile.request, h0 = tile.head, mt = tile.q_tile, n_kv = tile.n_kv;
+  const int kv0 = tile.kv0;
   const int q0 = a.qo_indptr[b], Lq = a.qo_indptr[b + 1] - q0;
   const int k0 = a.kv_indptr[b], Lk = a.kv_indptr[b + 1] - k0;
   const int nh = a.heads_per_cta;
@@ -132,14 +134,14 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
         mbar_arrive_expect_tx(bar(B_KFULL + st), 2u * kBox);
         for (int half = 0; half < 2; ++half)
           tma_load_3d(sbase + kOffK + (uint32_t)(st * 2 + half) * kBox, &tmk, bar(B_KFULL + st),
-                      half * 64, hk, k0 + j * kTile);
+                      half * 64, hk, k0 + (kv0 + j) * kTile);
         last_k = j;
         if (j >= 2) ok = mbar_wait(bar(B_VEMPTY + st), (uint32_t)(((j >> 1) - 1) & 1), a.status);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(B_VFULL + st), 2u * kBox);
         for (int half = 0; half < 2; ++half)
           tma_load_3d(sbase + kOffV + (uint32_t)(st * 2 + half) * kBox, &tmv, bar(B_VFULL + st),
-                      half * 64, hk, k0 + j * kTile);
+                      half * 64, hk, k0 + (kv0 + j) * kTile);
         last_v = j;
       }
       if (!ok) {   // give the copies already issued a bounded chance to land
@@ -206,7 +208,9 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
     const int row = q4 * 32 + lane;
     const int t = mt * kTile + row;
     const bool row_valid = t < Lq;
-    const int hi = a.causal ? min(Lk, Lk - Lq + t + 1) : Lk;   // keys [0, hi) visible
+    const int hi = a.causal ? min(Lk, Lk - Lq + t + 1) : Lk;   // keys [lo, hi) visible
+    const int lo = a.window_left >= 0 ? min(hi, max(0, Lk - Lq + t - a.window_left)) : 0;
+    const unsigned span = (unsigned)(hi - lo);   // key visible <=> (unsigned)(key - lo) < span
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + kColS + (uint32_t)hh * 128u;
     const uint32_t o_tm = tmem + lane_off + kColO + (uint32_t)hh * 128u;
@@ -216,8 +220,8 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
     for (int j = 0; j < n_kv; ++j) {
       if (!(ok = warp_wait(bar(B_SFULL + hh), (uint32_t)(j & 1), a.status))) break;
       tc_fence_after();
-      const int key0 = j * kTile;
-      const bool masked = key0 + kTile > hi;
+      const int key0 = (kv0 + j) * kTile;
+      const bool masked = key0 < lo || key0 + kTile > hi;
       // pass 1: row max of the raw scores (scale >= 0 keeps the order); two
       // 32-column loads in flight per wait, three-input max
       float mraw = neg_inf();
@@ -232,8 +236,8 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
         if (masked) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            if (key0 + c * 32 + i >= hi) ra[i] = __float_as_uint(neg_inf());
-            if (key0 + (c + 1) * 32 + i >= hi) rb[i] = __float_as_uint(neg_inf());
+            if ((unsigned)(key0 + c * 32 + i - lo) >= span) ra[i] = __float_as_uint(neg_inf());
+            if ((unsigned)(key0 + (c + 1) * 32 + i - lo) >= span) rb[i] = __float_as_uint(neg_inf());
           }
         }
 #pragma unroll
@@ -273,8 +277,8 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
           float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), sl2, neg_m));
           float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), sl2, neg_m));
           if (masked) {
-            if (key0 + c * 32 + 2 * i >= hi) p0 = 0.f;
-            if (key0 + c * 32 + 2 * i + 1 >= hi) p1 = 0.f;
+            if ((unsigned)(key0 + c * 32 + 2 * i - lo) >= span) p0 = 0.f;
+            if ((unsigned)(key0 + c * 32 + 2 * i + 1 - lo) >= span) p1 = 0.f;
           }
           sum0 += p0;
           sum1 += p1;

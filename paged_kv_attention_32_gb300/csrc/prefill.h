@@ -18,6 +18,7 @@ struct PrefillTile {
   int32_t head;     // first query head of the tile
   int32_t q_tile;   // 128-row tile index inside the request
   int32_t n_kv;     // KV tiles (128 keys) the tile visits
+  int32_t kv0;      // first of them (past 0 only with a window)
 };
 
 struct PrefillArgs {
@@ -35,6 +36,7 @@ struct PrefillArgs {
   int32_t num_kv_heads;
   int32_t group;
   int32_t causal;
+  int32_t window_left;   // -1: no window
   int32_t heads_per_cta;
   float scale_log2;
   float output_scale;

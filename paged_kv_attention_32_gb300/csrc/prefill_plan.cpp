@@ -1,8 +1,9 @@
 // Host tile schedule of the ragged causal prefill (batch_prefill with packed
 // qo_indptr / kv_indptr).  One tile = 128 query rows of one request for the
-// query heads one CTA serves; tiles are ordered heaviest first (most KV tiles
-// to visit), so that the hardware block scheduler hands the long causal rows
-// out before the short ones (longest-processing-time order).
+// query heads one CTA serves, with the run of 128-key tiles its rows can see
+// (causal diagonal, optional left window); tiles are ordered heaviest first
+// (most KV tiles to visit), so that the hardware block scheduler hands the
+// long causal rows out before the short ones (longest-processing-time order).
 #include <algorithm>
 #include <cmath>
 
@@ -31,8 +32,7 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
     return fail(PKA_ERR_UNSUPPORTED, "prefill head_dim must be 128 (got %d; 256 not built)",
                 d.head_dim);
   PKA_CHECK_ARG(d.mask == PKA_MASK_DENSE || d.mask == PKA_MASK_CAUSAL, "unknown mask %d", d.mask);
-  if (d.window_left != -1)
-    return fail(PKA_ERR_UNSUPPORTED, "prefill window_left must be -1");
+  PKA_CHECK_ARG(d.window_left >= -1, "window_left must be -1 or >= 0 (got %d)", d.window_left);
   if (std::isnan(d.sm_scale)) d.sm_scale = 1.0f / std::sqrt((float)d.head_dim);
   PKA_CHECK_ARG(std::isfinite(d.sm_scale) && std::isfinite(d.output_scale),
                 "sm_scale and output_scale must be finite");
@@ -59,12 +59,17 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
     PKA_CHECK_ARG(lq == 0 || lk > 0, "request %d has queries but no keys", b);
     const int64_t n_qt = ceil_div(lq, kTileQ);
     for (int64_t m = 0; m < n_qt; ++m) {
-      // keys seen by the tile's last row: bottom-right causal diagonal
+      // keys the tile's rows see: up to the last row's bottom-right causal
+      // diagonal, from the first row's window edge (plain sliding window)
+      const int64_t first_row = m * kTileQ;
       const int64_t last_row = std::min<int64_t>(lq, (m + 1) * kTileQ) - 1;
       const int64_t hi = d.mask == PKA_MASK_CAUSAL ? lk - lq + last_row + 1 : lk;
-      const int32_t n_kv = (int32_t)ceil_div(hi, kTileK);
+      const int64_t lo =
+          d.window_left >= 0 ? std::max<int64_t>(0, lk - lq + first_row - d.window_left) : 0;
+      const int32_t kv0 = (int32_t)(lo / kTileK);
+      const int32_t n_kv = (int32_t)(ceil_div(hi, kTileK) - kv0);
       for (int32_t h = 0; h < p.Hq; h += p.heads_per_cta)
-        p.tiles.push_back(PrefillTile{b, h, (int32_t)m, n_kv});
+        p.tiles.push_back(PrefillTile{b, h, (int32_t)m, n_kv, kv0});
     }
   }
   std::stable_sort(p.tiles.begin(), p.tiles.end(),

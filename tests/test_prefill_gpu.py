@@ -60,6 +60,20 @@ def test_prefill_bottom_right_causal_with_longer_kv():
     _run([3, 130, 64], [40, 200, 64], 4, 2, seed=20, sm_scale=0.05)
 
 
+@pytest.mark.parametrize("W", [0, 5, 127, 128, 300])
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_window_left(W, causal):
+    """Plain sliding window: row i keeps keys from Lk - Lq + i - W on; tiles left of
+    every row's window are skipped, partly covered ones masked per row."""
+    lq = [1, 130, 300, 513]
+    lk = [1, 200, 300, 700] if causal else [5, 130, 410, 513]
+    _run(lq, lk, 8, 2, causal=causal, seed=30 + W, window_left=W)
+
+
+def test_prefill_window_odd_group():
+    _run([257, 64], [400, 64], 6, 2, seed=40, window_left=60)
+
+
 def test_prefill_full_size_sampled():
     """The ragged prefill workload at full size (as bench.py times it), sampled rows."""
     w = wl.RAGGED_PREFILL
