@@ -233,7 +233,8 @@ def merge_states(v_states, s_states):
 # ---------------------------------------------------------------------------
 
 def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads, causal=True,
-                    sm_scale=None, output_scale=1.0, heads=None, rows=None, window_left=-1):
+                    sm_scale=None, output_scale=1.0, heads=None, rows=None, window_left=-1,
+                    window_bounds=None):
     """Prefill output of request ``b``: ``(O [Lq, Hq, D], LSE [Lq, Hq])``.
 
     Packed storage: request ``b`` owns query rows ``qo_indptr[b] ..
@@ -246,6 +247,9 @@ def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_head
     lists it; the page's head-paired policy for it is undefined, so this is the
     plain sliding window of the decode pages): row ``i`` keeps the keys from
     ``Lk - Lq + i - window_left`` on, as ``decode_row_key_range`` states.
+    ``window_bounds = (starts, ends)`` selects ``mask_type='variable_window'``
+    instead: row ``i`` sees exactly keys ``starts[i] .. ends[i]`` (inclusive
+    per-query bounds, ``variable_window_token_starts`` / ``_ends``).
     """
     Hq, D = q_bits.shape[1], q_bits.shape[2]
     group = Hq // num_kv_heads
@@ -261,7 +265,10 @@ def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_head
     keys = np.arange(Lk)
     allowed = np.zeros((len(rows), Lk), dtype=bool)
     for r, i in enumerate(rows):
-        lo, hi = decode_row_key_range(Lk, Lq, int(i), causal, window_left)
+        if window_bounds is not None:
+            lo, hi = int(window_bounds[0][i]), int(window_bounds[1][i]) + 1
+        else:
+            lo, hi = decode_row_key_range(Lk, Lq, int(i), causal, window_left)
         allowed[r] = (keys >= lo) & (keys < hi)
     for h in heads:
         hk = h // group
@@ -275,15 +282,25 @@ def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_head
 
 
 def batch_prefill(q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads, causal=True,
-                  sm_scale=None, output_scale=1.0, window_left=-1):
-    """Ragged prefill over the whole batch: ``(O [total_q, Hq, D], LSE [total_q, Hq])``."""
+                  sm_scale=None, output_scale=1.0, window_left=-1, window_starts=None,
+                  window_ends=None):
+    """Ragged prefill over the whole batch: ``(O [total_q, Hq, D], LSE [total_q, Hq])``.
+
+    ``window_starts`` / ``window_ends`` (``[B, Sq]``, fixed-shape batches only,
+    as ``batch_prefill`` restricts ``variable_window``) give each query row its
+    inclusive key bounds; ``causal`` and ``window_left`` are then unused.
+    """
     total_q, Hq, D = q_bits.shape
     O = np.zeros((total_q, Hq, D))
     LSE = np.zeros((total_q, Hq))
     for b in range(len(qo_indptr) - 1):
         q0, q1 = int(qo_indptr[b]), int(qo_indptr[b + 1])
+        bounds = None
+        if window_starts is not None:
+            bounds = (np.asarray(window_starts)[b], np.asarray(window_ends)[b])
         o, lse = prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads,
-                                 causal, sm_scale, output_scale, window_left=window_left)
+                                 causal, sm_scale, output_scale, window_left=window_left,
+                                 window_bounds=bounds)
         O[q0:q1] = o
         LSE[q0:q1] = lse
     return O, LSE

@@ -470,3 +470,60 @@ def test_prefill_window_at_least_kv_len_is_no_window():
     a = oracle.batch_prefill(_bits(q), _bits(k), _bits(v), ind, ind, 1, window_left=45)
     b = oracle.batch_prefill(_bits(q), _bits(k), _bits(v), ind, ind, 1)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def _variable_bounds(B, Sq, Sk, seed):
+    g = np.random.default_rng(seed)
+    a = g.integers(0, Sk, size=(B, Sq))
+    b = g.integers(0, Sk, size=(B, Sq))
+    return np.minimum(a, b), np.maximum(a, b)
+
+
+def test_prefill_variable_window_matches_torch_sdpa():
+    """variable_window: torch SDPA with a mask from comparisons against the bounds."""
+    B, Sq, Sk, Hq, Hkv = 2, 9, 14, 4, 2
+    q = _rand_bf16((B * Sq, Hq, 128), 260)
+    k = _rand_bf16((B * Sk, Hkv, 128), 261)
+    v = _rand_bf16((B * Sk, Hkv, 128), 262)
+    st, en = _variable_bounds(B, Sq, Sk, 263)
+    qi, ki = np.arange(B + 1) * Sq, np.arange(B + 1) * Sk
+    O, lse = oracle.batch_prefill(_bits(q), _bits(k), _bits(v), qi, ki, Hkv,
+                                  window_starts=st, window_ends=en)
+    j = torch.arange(Sk)
+    for b in range(B):
+        mask = (j[None, :] >= torch.tensor(st[b])[:, None]) & (j[None, :] <= torch.tensor(en[b])[:, None])
+        for h in range(Hq):
+            hk = h // 2
+            qq = q.double()[b * Sq:(b + 1) * Sq, h]
+            kk = k.double()[b * Sk:(b + 1) * Sk, hk]
+            ref = F.scaled_dot_product_attention(qq[None, None], kk[None, None],
+                                                 v.double()[b * Sk:(b + 1) * Sk, hk][None, None],
+                                                 attn_mask=mask[None, None])[0, 0]
+            assert np.allclose(O[b * Sq:(b + 1) * Sq, h], ref.numpy(), atol=1e-12)
+            s = (qq @ kk.T / math.sqrt(128)).masked_fill(~mask, -math.inf)
+            assert np.allclose(lse[b * Sq:(b + 1) * Sq, h], (torch.logsumexp(s, 1) * LOG2E).numpy(),
+                               atol=1e-11)
+
+
+def test_prefill_variable_window_special_cases():
+    """Full bounds reduce to the dense mask; bounds [0, Sk - Sq + i] to the causal one;
+    a single key start = end returns that value row."""
+    B, Sq, Sk = 2, 6, 10
+    q = _rand_bf16((B * Sq, 2, 128), 270)
+    k = _rand_bf16((B * Sk, 1, 128), 271)
+    v = _rand_bf16((B * Sk, 1, 128), 272)
+    qi, ki = np.arange(B + 1) * Sq, np.arange(B + 1) * Sk
+    args = (_bits(q), _bits(k), _bits(v), qi, ki, 1)
+    zeros, full = np.zeros((B, Sq), int), np.full((B, Sq), Sk - 1)
+    diag = np.tile(Sk - Sq + np.arange(Sq), (B, 1))
+    a = oracle.batch_prefill(*args, window_starts=zeros, window_ends=full)
+    d = oracle.batch_prefill(*args, causal=False)
+    assert np.array_equal(a[0], d[0]) and np.array_equal(a[1], d[1])
+    a = oracle.batch_prefill(*args, window_starts=zeros, window_ends=diag)
+    c = oracle.batch_prefill(*args, causal=True)
+    assert np.array_equal(a[0], c[0]) and np.array_equal(a[1], c[1])
+    one = np.tile(np.arange(Sq) + 2, (B, 1))
+    a = oracle.batch_prefill(*args, window_starts=one, window_ends=one)
+    for b in range(B):
+        for i in range(Sq):
+            assert np.array_equal(a[0][b * Sq + i, 0], v.double()[b * Sk + i + 2, 0].numpy())
