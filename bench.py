@@ -410,6 +410,50 @@ def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1):
             "tiles": plan.num_tiles}
 
 
+def measure_prefill_fixed(seed, steps, warmup, peak_tflops, variable_window=False):
+    """Fixed-shape [B, S, H, D] prefill, B=4, S=4096, Hq=32, Hkv=8: causal, or
+    variable_window with row i of each request seeing keys [s_i, i], s_i uniform in
+    [max(0, i - 2047), i] (seeded).  FLOPs = 4 * D per visible (query, key) pair per head."""
+    import numpy as np
+    import torch
+    from paged_kv_attention_32_gb300 import api
+    B, S, Hq, Hkv = 4, 4096, 32, 8
+    g = torch.Generator(device="cuda").manual_seed(seed + 7)
+    q = torch.randn((B, S, Hq, 128), generator=g, device="cuda", dtype=torch.bfloat16)
+    k = torch.randn((B, S, Hkv, 128), generator=g, device="cuda", dtype=torch.bfloat16)
+    v = torch.randn((B, S, Hkv, 128), generator=g, device="cuda", dtype=torch.bfloat16)
+    kw, name = {}, f"fixed-shape causal prefill B={B} S={S} Hq={Hq} Hkv={Hkv} D=128"
+    pairs = B * S * (S + 1) // 2
+    if variable_window:
+        rng = np.random.default_rng(seed + 8)
+        i = np.arange(S)
+        st = (i - rng.integers(0, 2048, size=(B, S))).clip(0, None).astype(np.int32)
+        en = np.tile(i, (B, 1)).astype(np.int32)
+        kw = dict(mask_type="variable_window", variable_window_token_starts=st,
+                  variable_window_token_ends=en)
+        pairs = int((en - st + 1).sum())
+        name = (f"fixed-shape variable_window prefill B={B} S={S} Hq={Hq} Hkv={Hkv} D=128, "
+                "row i sees [i - U(0, 2047), i]")
+    flops = 4 * 128 * pairs * Hq
+    plan = api.batch_prefill_plan_fixed(B, S, S, num_qo_heads=Hq, num_kv_heads=Hkv, **kw)
+    out = torch.empty_like(q)
+    for _ in range(warmup):
+        api.batch_prefill_run(plan, q, k, v, out=out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        api.batch_prefill_run(plan, q, k, v, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    plan.check()
+    ms = e0.elapsed_time(e1) / steps
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": name, "ms_per_call": round(ms, 4), "flops": flops,
+            "TFLOP_per_s": round(tf, 1), "frac_of_measured_bf16": round(tf / peak_tflops, 4),
+            "tiles": plan.num_tiles}
+
+
 def _oracle_worker(conn, task):
     """Long-lived oracle worker: holds one request's data, runs it on command."""
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
@@ -596,6 +640,10 @@ def main():
         extra["prefill"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf)
         extra["prefill_window"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf,
                                                   window_left=PREFILL_WINDOW)
+        extra["prefill_fixed"] = measure_prefill_fixed(args.seed, max(3, args.steps // 4), 3,
+                                                       peak_tf)
+        extra["prefill_variable_window"] = measure_prefill_fixed(
+            args.seed, max(3, args.steps // 4), 3, peak_tf, variable_window=True)
         line["decode_headline"] = head
         line["other_workloads"] = extra
     if rank == 0:

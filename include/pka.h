@@ -62,6 +62,8 @@ extern "C" {
 
 #define PKA_MASK_DENSE 0   /* mask_type 'dense': only padding is masked            */
 #define PKA_MASK_CAUSAL 1  /* mask_type 'causal': bottom-right aligned diagonal     */
+#define PKA_MASK_VARIABLE_WINDOW 2 /* prefill, fixed shape only: per-query inclusive key
+                                      bounds (batch_prefill, mask_type 'variable_window') */
 
 #define PKA_PLAN_HOST_ONLY 1  /* build the plan on the host only (no device copy);
                                  such a plan can be inspected but not run        */
@@ -338,7 +340,8 @@ typedef struct pka_prefill_desc {
 typedef struct pka_prefill_plan pka_prefill_plan; /* opaque prefill plan */
 
 /*
- * Build the tile schedule of a packed ragged prefill.
+ * Build the tile schedule of a packed ragged prefill (mask CAUSAL or DENSE;
+ * PKA_MASK_VARIABLE_WINDOW needs the fixed-shape planner below).
  * qo_indptr_host, kv_indptr_host  [B+1] int32 host arrays, cumulative offsets
  *           starting at 0 (batch_prefill, qo_indptr / kv_indptr).  For a
  *           causal mask every request needs kv_len >= q_len.
@@ -348,6 +351,26 @@ typedef struct pka_prefill_plan pka_prefill_plan; /* opaque prefill plan */
 int batch_prefill_plan(pka_prefill_plan** plan_out, const pka_prefill_desc* desc,
                        const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
                        size_t* workspace_bytes_out, int32_t* num_tiles_out, void* stream);
+
+/*
+ * Build the tile schedule of a fixed-shape prefill (batch_prefill with
+ * [B, S, H, D] storage and no offset tensors): q [B, seq_len_q, Hq, D] and k, v
+ * [B, seq_len_kv, Hkv, D], run by batch_prefill_run as a packed batch whose B
+ * requests all have seq_len_q queries and seq_len_kv keys (token t of request
+ * b is row b * seq_len + t).
+ * mask       PKA_MASK_CAUSAL, PKA_MASK_DENSE or PKA_MASK_VARIABLE_WINDOW.
+ * window_starts_host, window_ends_host  with PKA_MASK_VARIABLE_WINDOW: [B,
+ *            seq_len_q] int32 host arrays of inclusive key bounds, 0 <= start
+ *            <= end < seq_len_kv (batch_prefill, variable_window_token_starts /
+ *            _ends; query row q of request b sees keys start[b, q] .. end[b, q]);
+ *            the plan keeps a device copy.  NULL with the other masks.
+ * Errors: INVALID_ARG for bounds outside that range, a bound array missing or
+ * given with another mask, seq_len_q < 1, seq_len_kv < 1.
+ */
+int batch_prefill_plan_fixed(pka_prefill_plan** plan_out, const pka_prefill_desc* desc,
+                             int32_t seq_len_q, int32_t seq_len_kv,
+                             const int32_t* window_starts_host, const int32_t* window_ends_host,
+                             size_t* workspace_bytes_out, int32_t* num_tiles_out, void* stream);
 
 void batch_prefill_plan_destroy(pka_prefill_plan* plan);
 

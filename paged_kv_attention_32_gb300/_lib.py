@@ -19,7 +19,7 @@ PKA_ERR_DEVICE_BOUNDS = -5
 PKA_ERR_DEVICE_TIMEOUT = -6
 
 PKA_DTYPE_BF16, PKA_DTYPE_F16, PKA_DTYPE_F32 = 0, 1, 2
-PKA_MASK_DENSE, PKA_MASK_CAUSAL = 0, 1
+PKA_MASK_DENSE, PKA_MASK_CAUSAL, PKA_MASK_VARIABLE_WINDOW = 0, 1, 2
 PKA_PLAN_HOST_ONLY = 1
 PKA_KERNEL_CUDA_CORE, PKA_KERNEL_MMA = 0, 1
 
@@ -30,7 +30,7 @@ EXPORTED = (
     "paged_decode_plan_export", "paged_decode_run", "paged_decode_plan_check",
     "paged_decode_run_noalloc",
     "attn_merge_lse",
-    "batch_prefill_plan", "batch_prefill_plan_destroy", "batch_prefill_plan_check",
+    "batch_prefill_plan", "batch_prefill_plan_fixed", "batch_prefill_plan_destroy", "batch_prefill_plan_check",
     "batch_prefill_run",
     "paged_kv_gather",
 )
@@ -91,6 +91,9 @@ _SIGS = {
     "attn_merge_lse": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]),
     "batch_prefill_plan": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.POINTER(PrefillDesc),
                                           _pi32, _pi32, ctypes.POINTER(_sz), _pi32, _vp]),
+    "batch_prefill_plan_fixed": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.POINTER(PrefillDesc),
+                                                _i32, _i32, _pi32, _pi32, ctypes.POINTER(_sz),
+                                                _pi32, _vp]),
     "batch_prefill_plan_destroy": (None, [_vp]),
     "batch_prefill_plan_check": (ctypes.c_int, [_vp, _vp]),
     "batch_prefill_run": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _vp,

@@ -170,8 +170,51 @@ def batch_prefill_plan(qo_indptr, kv_indptr, *, num_qo_heads, num_kv_heads, caus
     return PrefillPlan(h, d, nt.value)
 
 
+def batch_prefill_plan_fixed(batch_size, seq_len_q, seq_len_kv, *, num_qo_heads, num_kv_heads,
+                             mask_type="causal", window_left=-1,
+                             variable_window_token_starts=None, variable_window_token_ends=None,
+                             sm_scale=None, output_scale=1.0, return_lse=False, head_dim=128,
+                             host_only=False, stream=None):
+    """Plan a fixed-shape prefill: q ``[B, Sq, Hq, D]``, k/v ``[B, Sk, Hkv, D]`` (run it with
+    ``batch_prefill_run`` on the tensors viewed as ``[B*S, H, D]``).  ``mask_type``:
+    ``'causal'``, ``'dense'`` or ``'variable_window'`` (inclusive per-query key bounds
+    ``[B, Sq]``; host copies are taken here for planning)."""
+    masks = {"dense": L.PKA_MASK_DENSE, "causal": L.PKA_MASK_CAUSAL,
+             "variable_window": L.PKA_MASK_VARIABLE_WINDOW}
+    st_t, st_p = _host_i32(variable_window_token_starts)
+    en_t, en_p = _host_i32(variable_window_token_ends)
+    d = L.PrefillDesc(
+        batch_size=batch_size, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+        head_dim=head_dim, dtype=L.PKA_DTYPE_BF16, mask=masks[mask_type], window_left=window_left,
+        sm_scale=float("nan") if sm_scale is None else sm_scale, output_scale=output_scale,
+        return_lse=int(bool(return_lse)), num_sms=0,
+        flags=L.PKA_PLAN_HOST_ONLY if host_only else 0)
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    nt = ctypes.c_int32()
+    rc = L.lib().batch_prefill_plan_fixed(ctypes.byref(h), ctypes.byref(d), seq_len_q, seq_len_kv,
+                                          st_p, en_p, ctypes.byref(ws), ctypes.byref(nt),
+                                          _stream(stream) if not host_only else None)
+    L.check(rc, "batch_prefill_plan_fixed")
+    return PrefillPlan(h, d, nt.value)
+
+
 def batch_prefill_run(plan, q, k, v, out=None, lse=None, stream=None):
-    """Run a planned prefill; returns ``out`` (and ``lse`` when the plan returns it)."""
+    """Run a planned prefill; returns ``out`` (and ``lse`` when the plan returns it).
+    Packed ``[total, H, D]`` tensors, or fixed-shape ``[B, S, H, D]`` ones (viewed as
+    ``[B*S, H, D]``; ``out``/``lse`` then come back as ``[B, Sq, Hq, D]``/``[B, Sq, Hq]``)."""
+    fixed = q.dim() == 4
+    if fixed:
+        B, Sq = q.shape[0], q.shape[1]
+        q, k, v = q.flatten(0, 1), k.flatten(0, 1), v.flatten(0, 1)
+        if out is not None:
+            out = out.view(B * Sq, *out.shape[2:])
+        if lse is not None:
+            lse = lse.view(B * Sq, lse.shape[2])
+        res = batch_prefill_run(plan, q, k, v, out=out, lse=lse, stream=stream)
+        if plan.desc.return_lse:
+            return res[0].view(B, Sq, *res[0].shape[1:]), res[1].view(B, Sq, res[1].shape[1])
+        return res.view(B, Sq, *res.shape[1:])
     total_q, Hq, D = q.shape
     if out is None:
         out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=q.device)

@@ -1,6 +1,8 @@
 // extern "C" entry points of pka.h: argument checks, plan ownership, launch
 // dispatch.  Nothing here computes attention; every step of the path runs in
 // the kernels.
+#include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -75,9 +77,12 @@ int upload_decode_plan(pka_plan& p, cudaStream_t stream) {
 int upload_prefill_plan(pka_prefill_plan& p, cudaStream_t stream) {
   const size_t n_tiles = p.tiles.size() * sizeof(PrefillTile);
   const size_t n_ind = p.qo.size() * sizeof(int32_t);
+  const size_t n_win = p.win_lo.size() * sizeof(int32_t);
   const size_t off_qo = up256(n_tiles);
   const size_t off_kv = off_qo + up256(n_ind);
-  const size_t off_status = off_kv + up256(n_ind);
+  const size_t off_wlo = off_kv + up256(n_ind);
+  const size_t off_whi = off_wlo + up256(n_win);
+  const size_t off_status = off_whi + up256(n_win);
   const size_t total = off_status + 256;
   PKA_CUDA_TRY(cudaGetDevice(&p.device), "cudaGetDevice");
   PKA_CUDA_TRY(cudaMalloc(&p.dev_buf, total), "cudaMalloc(prefill plan)");
@@ -93,6 +98,16 @@ int upload_prefill_plan(pka_prefill_plan& p, cudaStream_t stream) {
                "cudaMemcpyAsync(qo_indptr)");
   PKA_CUDA_TRY(cudaMemcpyAsync(base + off_kv, p.kv.data(), n_ind, cudaMemcpyHostToDevice, stream),
                "cudaMemcpyAsync(kv_indptr)");
+  if (n_win) {
+    p.d_win_lo = reinterpret_cast<const int32_t*>(base + off_wlo);
+    p.d_win_hi = reinterpret_cast<const int32_t*>(base + off_whi);
+    PKA_CUDA_TRY(cudaMemcpyAsync(base + off_wlo, p.win_lo.data(), n_win, cudaMemcpyHostToDevice,
+                                 stream),
+                 "cudaMemcpyAsync(window starts)");
+    PKA_CUDA_TRY(cudaMemcpyAsync(base + off_whi, p.win_hi.data(), n_win, cudaMemcpyHostToDevice,
+                                 stream),
+                 "cudaMemcpyAsync(window ends)");
+  }
   PKA_CUDA_TRY(cudaMemsetAsync(base + off_status, 0, 256, stream), "cudaMemsetAsync(status)");
   return PKA_OK;
 }
@@ -321,6 +336,38 @@ int batch_prefill_plan(pka_prefill_plan** plan_out, const pka_prefill_desc* desc
   return PKA_OK;
 }
 
+int batch_prefill_plan_fixed(pka_prefill_plan** plan_out, const pka_prefill_desc* desc,
+                             int32_t seq_len_q, int32_t seq_len_kv,
+                             const int32_t* window_starts_host, const int32_t* window_ends_host,
+                             size_t* workspace_bytes_out, int32_t* num_tiles_out, void* stream) {
+  clear_error();
+  PKA_CHECK_ARG(plan_out != nullptr && desc != nullptr, "plan_out and desc must not be NULL");
+  *plan_out = nullptr;
+  PKA_CHECK_ARG(desc->batch_size >= 1, "batch_size must be >= 1");
+  PKA_CHECK_ARG(seq_len_q >= 1 && seq_len_kv >= 1, "seq_len_q and seq_len_kv must be >= 1");
+  PKA_CHECK_ARG((int64_t)desc->batch_size * std::max(seq_len_q, seq_len_kv) <= INT32_MAX,
+                "batch_size * seq_len exceeds 2^31 - 1 rows");
+  std::vector<int32_t> qo(desc->batch_size + 1), kv(desc->batch_size + 1);
+  for (int32_t b = 0; b <= desc->batch_size; ++b) {
+    qo[b] = b * seq_len_q;
+    kv[b] = b * seq_len_kv;
+  }
+  pka_prefill_plan* p = new (std::nothrow) pka_prefill_plan();
+  if (p == nullptr) return fail(PKA_ERR_INVALID_ARG, "out of host memory");
+  int rc = build_prefill_plan(*p, *desc, qo.data(), kv.data(), window_starts_host,
+                              window_ends_host);
+  if (rc == PKA_OK && !(desc->flags & PKA_PLAN_HOST_ONLY))
+    rc = upload_prefill_plan(*p, static_cast<cudaStream_t>(stream));
+  if (rc != PKA_OK) {
+    batch_prefill_plan_destroy(p);
+    return rc;
+  }
+  if (workspace_bytes_out) *workspace_bytes_out = 0;
+  if (num_tiles_out) *num_tiles_out = (int32_t)p->tiles.size();
+  *plan_out = p;
+  return PKA_OK;
+}
+
 void batch_prefill_plan_destroy(pka_prefill_plan* plan) {
   if (plan == nullptr) return;
   if (plan->dev_buf != nullptr) cudaFree(plan->dev_buf);
@@ -379,6 +426,8 @@ int batch_prefill_run(const pka_prefill_plan* p, const void* q, int64_t q_stride
   a.group = p->G;
   a.causal = p->desc.mask == PKA_MASK_CAUSAL;
   a.window_left = p->desc.window_left;
+  a.window_lo = p->d_win_lo;
+  a.window_hi = p->d_win_hi;
   a.heads_per_cta = p->heads_per_cta;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.output_scale = p->desc.output_scale;

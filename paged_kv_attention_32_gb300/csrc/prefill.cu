@@ -3,7 +3,8 @@
 // batch_prefill (packed qo_indptr / kv_indptr): for every request and query
 // head, O = softmax(sm_scale * Q K^T + causal mask) V * output_scale, with the
 // causal diagonal bottom-right aligned (row i sees keys 0 .. Lk - Lq + i) and
-// an optional left window (window_left = W >= 0: keys from Lk - Lq + i - W on).
+// an optional left window (window_left = W >= 0: keys from Lk - Lq + i - W on),
+// or, for fixed-shape batches, per-row inclusive bounds (variable_window).
 //
 // One CTA = one 128-row query tile of one request for two query heads that
 // share a KV head (GQA), so every K/V tile loaded serves both heads.
@@ -208,8 +209,12 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
     const int row = q4 * 32 + lane;
     const int t = mt * kTile + row;
     const bool row_valid = t < Lq;
-    const int hi = a.causal ? min(Lk, Lk - Lq + t + 1) : Lk;   // keys [lo, hi) visible
-    const int lo = a.window_left >= 0 ? min(hi, max(0, Lk - Lq + t - a.window_left)) : 0;
+    int hi = a.causal ? min(Lk, Lk - Lq + t + 1) : Lk;   // keys [lo, hi) visible
+    int lo = a.window_left >= 0 ? min(hi, max(0, Lk - Lq + t - a.window_left)) : 0;
+    if (a.window_lo != nullptr) {   // variable_window: the row's inclusive bounds
+      lo = row_valid ? __ldg(a.window_lo + q0 + t) : 0;
+      hi = row_valid ? __ldg(a.window_hi + q0 + t) + 1 : 0;
+    }
     const unsigned span = (unsigned)(hi - lo);   // key visible <=> (unsigned)(key - lo) < span
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + kColS + (uint32_t)hh * 128u;

@@ -37,6 +37,8 @@ struct PrefillArgs {
   int32_t group;
   int32_t causal;
   int32_t window_left;   // -1: no window
+  const int32_t* window_lo;   // variable_window: first key of each query row, else nullptr
+  const int32_t* window_hi;   // variable_window: last key (inclusive) of each query row
   int32_t heads_per_cta;
   float scale_log2;
   float output_scale;
@@ -50,20 +52,26 @@ struct pka_prefill_plan {
   int32_t total_q = 0, total_kv = 0, heads_per_cta = 1;
   float scale = 0.f;
   std::vector<int32_t> qo, kv;
+  std::vector<int32_t> win_lo, win_hi;   // variable_window bounds per query row (host)
   std::vector<pka::PrefillTile> tiles;
   void* dev_buf = nullptr;
   const pka::PrefillTile* d_tiles = nullptr;
   const int32_t* d_qo = nullptr;
   const int32_t* d_kv = nullptr;
+  const int32_t* d_win_lo = nullptr;
+  const int32_t* d_win_hi = nullptr;
   int32_t* d_status = nullptr;
   int device = -1;
 };
 
 namespace pka {
 
-// Builds the host tile schedule (heaviest tiles first).
+// Builds the host tile schedule (heaviest tiles first).  win_lo / win_hi:
+// per-query-row inclusive key bounds of mask PKA_MASK_VARIABLE_WINDOW (one
+// entry per packed query row), nullptr with the other masks.
 int build_prefill_plan(pka_prefill_plan& plan, const pka_prefill_desc& desc, const int32_t* qo,
-                       const int32_t* kv);
+                       const int32_t* kv, const int32_t* win_lo = nullptr,
+                       const int32_t* win_hi = nullptr);
 
 // Launches the prefill kernel over the plan's tiles.
 int launch_prefill(const pka_prefill_plan& plan, const PrefillArgs& args, const CUtensorMap& qmap,

@@ -18,7 +18,7 @@ constexpr int kTileK = 128;
 }  // namespace
 
 int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const int32_t* qo,
-                       const int32_t* kv) {
+                       const int32_t* kv, const int32_t* win_lo, const int32_t* win_hi) {
   pka_prefill_desc d = d_in;
   PKA_CHECK_ARG(qo != nullptr && kv != nullptr, "qo_indptr_host and kv_indptr_host are required");
   PKA_CHECK_ARG(d.batch_size >= 1, "batch_size must be >= 1");
@@ -31,7 +31,13 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
   if (d.head_dim != 128)
     return fail(PKA_ERR_UNSUPPORTED, "prefill head_dim must be 128 (got %d; 256 not built)",
                 d.head_dim);
-  PKA_CHECK_ARG(d.mask == PKA_MASK_DENSE || d.mask == PKA_MASK_CAUSAL, "unknown mask %d", d.mask);
+  PKA_CHECK_ARG(d.mask == PKA_MASK_DENSE || d.mask == PKA_MASK_CAUSAL ||
+                    d.mask == PKA_MASK_VARIABLE_WINDOW,
+                "unknown mask %d", d.mask);
+  const bool varwin = d.mask == PKA_MASK_VARIABLE_WINDOW;
+  PKA_CHECK_ARG(varwin == (win_lo != nullptr && win_hi != nullptr),
+                varwin ? "variable_window needs both bound arrays (fixed-shape planner)"
+                       : "window bounds are given only with mask variable_window");
   PKA_CHECK_ARG(d.window_left >= -1, "window_left must be -1 or >= 0 (got %d)", d.window_left);
   if (std::isnan(d.sm_scale)) d.sm_scale = 1.0f / std::sqrt((float)d.head_dim);
   PKA_CHECK_ARG(std::isfinite(d.sm_scale) && std::isfinite(d.output_scale),
@@ -50,6 +56,12 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
   p.heads_per_cta = (p.G % 2 == 0) ? 2 : 1;
   p.qo.assign(qo, qo + B + 1);
   p.kv.assign(kv, kv + B + 1);
+  p.win_lo.clear();
+  p.win_hi.clear();
+  if (varwin) {
+    p.win_lo.assign(win_lo, win_lo + qo[B]);
+    p.win_hi.assign(win_hi, win_hi + qo[B]);
+  }
   p.tiles.clear();
   for (int32_t b = 0; b < B; ++b) {
     const int64_t lq = (int64_t)qo[b + 1] - qo[b], lk = (int64_t)kv[b + 1] - kv[b];
@@ -63,9 +75,21 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
       // diagonal, from the first row's window edge (plain sliding window)
       const int64_t first_row = m * kTileQ;
       const int64_t last_row = std::min<int64_t>(lq, (m + 1) * kTileQ) - 1;
-      const int64_t hi = d.mask == PKA_MASK_CAUSAL ? lk - lq + last_row + 1 : lk;
-      const int64_t lo =
+      int64_t hi = d.mask == PKA_MASK_CAUSAL ? lk - lq + last_row + 1 : lk;
+      int64_t lo =
           d.window_left >= 0 ? std::max<int64_t>(0, lk - lq + first_row - d.window_left) : 0;
+      if (varwin) {   // the union of the tile's rows' bounds
+        lo = lk;
+        hi = 0;
+        for (int64_t r = first_row; r <= last_row; ++r) {
+          const int32_t s = win_lo[qo[b] + r], e = win_hi[qo[b] + r];
+          PKA_CHECK_ARG(s >= 0 && s <= e && e < lk,
+                        "request %d row %lld: window bounds [%d, %d] outside 0 <= start <= end < %lld",
+                        b, (long long)r, s, e, (long long)lk);
+          lo = std::min<int64_t>(lo, s);
+          hi = std::max<int64_t>(hi, (int64_t)e + 1);
+        }
+      }
       const int32_t kv0 = (int32_t)(lo / kTileK);
       const int32_t n_kv = (int32_t)(ceil_div(hi, kTileK) - kv0);
       for (int32_t h = 0; h < p.Hq; h += p.heads_per_cta)

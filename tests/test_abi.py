@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from paged_kv_attention_32_gb300 import _lib as L
@@ -104,3 +105,26 @@ def test_prefill_tiles_heaviest_first():
 def test_merge_rejects_bad_head_dim():
     rc = L.lib().attn_merge_lse(None, None, 1, 1, 1, 6, None, 0, None, None)
     assert rc == L.PKA_ERR_INVALID_ARG
+
+
+def test_prefill_fixed_plan_tiles_and_bound_checks():
+    """Fixed-shape prefill: B * ceil(Sq / 128) q-tiles per head pair; variable_window
+    bounds must satisfy 0 <= start <= end < Sk and come only with that mask."""
+    p = api.batch_prefill_plan_fixed(2, 200, 300, num_qo_heads=8, num_kv_heads=2, host_only=True)
+    assert p.num_tiles == 2 * 2 * 4
+    st = np.zeros((2, 200), np.int32)
+    en = np.full((2, 200), 299, np.int32)
+    api.batch_prefill_plan_fixed(2, 200, 300, num_qo_heads=8, num_kv_heads=2,
+                                 mask_type="variable_window", variable_window_token_starts=st,
+                                 variable_window_token_ends=en, host_only=True)
+    bad = [dict(mask_type="variable_window", variable_window_token_starts=st,
+                variable_window_token_ends=en + 1),
+           dict(mask_type="variable_window", variable_window_token_starts=st + 5,
+                variable_window_token_ends=en * 0 + 4),
+           dict(mask_type="variable_window"),
+           dict(mask_type="causal", variable_window_token_starts=st, variable_window_token_ends=en)]
+    for kw in bad:
+        with pytest.raises(L.PkaError) as ei:
+            api.batch_prefill_plan_fixed(2, 200, 300, num_qo_heads=8, num_kv_heads=2,
+                                         host_only=True, **kw)
+        assert ei.value.code == L.PKA_ERR_INVALID_ARG

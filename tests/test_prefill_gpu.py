@@ -74,6 +74,46 @@ def test_prefill_window_odd_group():
     _run([257, 64], [400, 64], 6, 2, seed=40, window_left=60)
 
 
+def _fixed_case(B, Sq, Sk, Hq, Hkv, seed, **kw):
+    q = _rand((B, Sq, Hq, 128), seed + 1)
+    k, v = _rand((B, Sk, Hkv, 128), seed + 2), _rand((B, Sk, Hkv, 128), seed + 3)
+    plan = api.batch_prefill_plan_fixed(B, Sq, Sk, num_qo_heads=Hq, num_kv_heads=Hkv,
+                                        return_lse=True, **kw)
+    out, lse = api.batch_prefill_run(plan, q, k, v)
+    torch.cuda.synchronize()
+    plan.check()
+    assert out.shape == (B, Sq, Hq, 128) and lse.shape == (B, Sq, Hq)
+    mask = kw.get("mask_type", "causal")
+    okw = dict(causal=mask == "causal", window_left=kw.get("window_left", -1))
+    if mask == "variable_window":
+        okw = dict(window_starts=kw["variable_window_token_starts"],
+                   window_ends=kw["variable_window_token_ends"])
+    ref_o, ref_l = oracle.batch_prefill(wl.bf16_bits(q.flatten(0, 1)), wl.bf16_bits(k.flatten(0, 1)),
+                                        wl.bf16_bits(v.flatten(0, 1)), np.arange(B + 1) * Sq,
+                                        np.arange(B + 1) * Sk, Hkv, **okw)
+    _check(out.flatten(0, 1), lse.flatten(0, 1), ref_o, ref_l)
+
+
+@pytest.mark.parametrize("mask,W", [("causal", -1), ("dense", -1), ("causal", 100),
+                                    ("dense", 37)])
+def test_prefill_fixed_shape(mask, W):
+    """[B, S, H, D] storage without offset tensors, Sq < Sk (bottom-right diagonal)."""
+    _fixed_case(3, 200, 333, 8, 2, seed=50, mask_type=mask, window_left=W)
+
+
+@pytest.mark.parametrize("Hq,Hkv,seed", [(8, 2, 60), (6, 2, 61)])
+def test_prefill_variable_window(Hq, Hkv, seed):
+    """Per-query inclusive key bounds: random spans, some of a single key, some far
+    left of the diagonal, over several 128-key tiles."""
+    B, Sq, Sk = 3, 260, 400
+    g = np.random.default_rng(seed)
+    a, b = g.integers(0, Sk, size=(B, Sq)), g.integers(0, Sk, size=(B, Sq))
+    st, en = np.minimum(a, b).astype(np.int32), np.maximum(a, b).astype(np.int32)
+    en[:, ::7] = st[:, ::7]                      # single-key rows
+    _fixed_case(B, Sq, Sk, Hq, Hkv, seed=seed, mask_type="variable_window",
+                variable_window_token_starts=st, variable_window_token_ends=en)
+
+
 def test_prefill_full_size_sampled():
     """The ragged prefill workload at full size (as bench.py times it), sampled rows."""
     w = wl.RAGGED_PREFILL
