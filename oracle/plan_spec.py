@@ -21,7 +21,15 @@ a design choice of this library, stated here:
    the chunk is ``max_b np_b`` pages.  Otherwise the chunk ``c`` is the smallest
    integer in ``[min(c_min, max np), max np]`` with
    ``Hkv * sum_b t_b * ceil(np_b / c) <= T``, where ``c_min = ceil(min_chunk_tokens / ps)``.
-3. ``n_chunks_b = ceil(np_b / c)``.  Requests are visited longest first
+3. ``n_chunks_b = ceil(np_b / c)``, except for the tail of a launch that does
+   not split (``Hkv * sum_b t_b >= T``): with ``S = r * num_sms`` resident CTAs
+   (``r`` = 3 for the tensor-core kernel, 2 for the CUDA-core kernel), walk the
+   requests longest first and let the prefix whose CTAs ``Hkv * t_b`` sum to at
+   most ``S`` be the first wave; the remaining requests (``R`` CTAs) start only
+   as the first wave ends, so each is cut into ``k = S // R`` chunks of
+   ``c_b = max(ceil(np_b / k), min(c_min, np_b))`` pages (``n_chunks_b =
+   ceil(np_b / c_b)``) when ``k > 1``, so that they run as one short round on
+   all SMs.  Requests are visited longest first
    (``np_b`` descending, ties by ``b`` ascending); for each, chunks in order,
    and for each chunk every KV head: one work item
    ``(b, kv_head, chunk, page_lo, page_hi)``.
@@ -67,13 +75,28 @@ def plan_spec(seq_lens_kv, q_lens, num_qo_heads, num_kv_heads, head_dim, page_si
             if num_kv_heads * sum(t * _ceil_div(x, c) for t, x in zip(tiles, npages)) <= target:
                 chunk = c
                 break
-    n_chunks = [_ceil_div(x, chunk) for x in npages]
     order = sorted(range(B), key=lambda b: (-npages[b], b))
+    cb = [chunk] * B
+    if num_kv_heads * sum(tiles) >= target:
+        slots = (3 if mma else 2) * num_sms
+        acc, tail = 0, []
+        for b in order:
+            if not tail and acc + num_kv_heads * tiles[b] <= slots:
+                acc += num_kv_heads * tiles[b]
+            else:
+                tail.append(b)
+        rest = num_kv_heads * sum(tiles[b] for b in tail)
+        k = slots // rest if rest else 1
+        if k > 1:
+            c_min = _ceil_div(min_chunk_tokens, page_size)
+            for b in tail:
+                cb[b] = max(_ceil_div(npages[b], k), min(c_min, npages[b]))
+    n_chunks = [_ceil_div(x, c) for x, c in zip(npages, cb)]
     items = []
     for b in order:
         for ci in range(n_chunks[b]):
-            lo = page_lo[b] + ci * chunk
-            hi = min(page_lo[b] + (ci + 1) * chunk, page_hi[b])
+            lo = page_lo[b] + ci * cb[b]
+            hi = min(page_lo[b] + (ci + 1) * cb[b], page_hi[b])
             for hk in range(num_kv_heads):
                 items.append((b, hk, ci, lo, hi))
     part_base, rows = [], 0

@@ -9,6 +9,12 @@
 //   - with T = split_waves * num_sms target CTAs, no request is split when
 //     B * Hkv >= T; otherwise the chunk c is the smallest page count in
 //     [min(c_min, max np), max np] with Hkv * sum_b ceil(np_b / c) <= T;
+//   - when nothing is split that way, the requests past the first wave of
+//     resident CTAs (S = 3 per SM for the mma kernel, 2 for the CUDA-core
+//     one; longest-first prefix with at most S CTAs) start only as that wave
+//     ends, so they are cut into k = S / R chunks (R = their CTAs) of
+//     max(ceil(np / k), min(c_min, np)) pages when k > 1: one short round on
+//     every SM instead of a long one on a few;
 //   - items run longest request first, then chunk, then KV head.
 #include <algorithm>
 #include <climits>
@@ -157,13 +163,36 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
   }
   p.chunk_pages = (int32_t)chunk;
 
-  // ---- items, longest request first ----
-  std::vector<int32_t> nch(B);
-  for (int32_t b = 0; b < B; ++b) nch[b] = (int32_t)ceil_div(npages[b], chunk);
+  // ---- longest request first; chunk length per request ----
   p.order.resize(B);
   std::iota(p.order.begin(), p.order.end(), 0);
   std::stable_sort(p.order.begin(), p.order.end(),
                    [&](int32_t a, int32_t b) { return npages[a] > npages[b]; });
+  std::vector<int64_t> cb(B, chunk);
+  if (tiles_sum * Hkv >= target) {
+    const int64_t slots = (int64_t)(p.kernel == PKA_KERNEL_MMA ? 3 : 2) * d.num_sms;
+    int64_t acc = 0, rest = 0;
+    bool in_tail = false;
+    std::vector<int32_t> tail;
+    for (int32_t b : p.order) {
+      if (!in_tail && acc + Hkv * tiles[b] <= slots) {
+        acc += Hkv * tiles[b];
+      } else {
+        in_tail = true;
+        tail.push_back(b);
+        rest += Hkv * tiles[b];
+      }
+    }
+    const int64_t k = rest ? slots / rest : 1;
+    if (k > 1) {
+      const int64_t c_min = ceil_div(d.min_chunk_tokens, ps);
+      for (int32_t b : tail) cb[b] = std::max(ceil_div(npages[b], k), std::min(c_min, npages[b]));
+    }
+  }
+
+  // ---- items ----
+  std::vector<int32_t> nch(B);
+  for (int32_t b = 0; b < B; ++b) nch[b] = (int32_t)ceil_div(npages[b], cb[b]);
   int64_t n_items = 0;
   for (int32_t b = 0; b < B; ++b) n_items += (int64_t)nch[b] * Hkv;
   PKA_CHECK_ARG(n_items <= (int64_t)INT32_MAX, "too many work items");
@@ -174,8 +203,8 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
   p.items.reserve((size_t)n_items);
   for (int32_t b : p.order) {
     for (int32_t ci = 0; ci < nch[b]; ++ci) {
-      const int32_t lo = p.page_lo[b] + (int32_t)(ci * chunk);
-      const int32_t hi = (int32_t)std::min<int64_t>(p.page_lo[b] + (ci + 1) * chunk, p.page_hi[b]);
+      const int32_t lo = p.page_lo[b] + (int32_t)(ci * cb[b]);
+      const int32_t hi = (int32_t)std::min<int64_t>(p.page_lo[b] + (ci + 1) * cb[b], p.page_hi[b]);
       for (int32_t hk = 0; hk < Hkv; ++hk) p.items.push_back(WorkItem{b, (ci << 16) | hk, lo, hi});
     }
   }

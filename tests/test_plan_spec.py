@@ -57,21 +57,41 @@ def test_plan_chunk_is_minimal_under_the_target(case):
     B, T = len(kv), waves * sms
     npg = [hi - lo for lo, hi in zip(p["page_lo"], p["page_hi"])]
     c = p["chunk_pages"]
+    c_min = math.ceil(mct / ps)
     G = Hq // Hkv
-    mma0 = G * max(ql) >= 8 or G * max(ql) > 8
-    tiles0 = [math.ceil(G * q / 16) if mma0 else 1 for q in ql]
-    if Hkv * sum(tiles0) >= T:
-        assert c == max(npg) and all(x == 1 for x in p["n_chunks"])
-        return
-    G = Hq // Hkv
-    mma = G * max(ql) >= 8 or G * max(ql) > 8
+    mma = G * max(ql) >= 8
     tiles = [math.ceil(G * q / 16) if mma else 1 for q in ql]
-    ctas = Hkv * sum(t * math.ceil(x / c) for t, x in zip(tiles, npg))
-    assert Hkv * sum(math.ceil(x / c) for x in npg) == len(p["items"]) and ctas <= T
-    c_lo = min(math.ceil(mct / ps), max(npg))
+    ctas = [Hkv * t for t in tiles]
+    if sum(ctas) >= T:
+        # no uniform split: only requests past the first wave of resident CTAs are
+        # cut, into at most k = slots // (their CTAs) chunks of >= min(c_min, np) pages
+        assert c == max(npg)
+        slots = (3 if mma else 2) * sms
+        order, first, acc = p["order"], 0, 0
+        while first < B and acc + ctas[order[first]] <= slots:
+            acc += ctas[order[first]]
+            first += 1
+        tail = order[first:]
+        rest = sum(ctas[b] for b in tail)
+        k = slots // rest if rest else 1
+        assert all(p["n_chunks"][b] == 1 for b in order[:first])
+        for b in tail:
+            n = p["n_chunks"][b]
+            if k <= 1:
+                assert n == 1
+                continue
+            assert 1 <= n <= k
+            lens = [hi - lo for (bb, hk, ci, lo, hi) in p["items"] if bb == b and hk == 0]
+            assert all(x >= min(c_min, npg[b]) for x in lens[:-1])
+            if n < k:   # fewer pages than k, or the c_min floor bound the chunk
+                assert npg[b] < k or math.ceil(npg[b] / k) < min(c_min, npg[b])
+        return
+    ctas_at = lambda cc: Hkv * sum(t * math.ceil(x / cc) for t, x in zip(tiles, npg))
+    assert Hkv * sum(math.ceil(x / c) for x in npg) == len(p["items"]) and ctas_at(c) <= T
+    c_lo = min(c_min, max(npg))
     assert c >= c_lo
     if c > c_lo:
-        assert Hkv * sum(t * math.ceil(x / (c - 1)) for t, x in zip(tiles, npg)) > T
+        assert ctas_at(c - 1) > T
 
 
 @pytest.mark.parametrize("case", _cases()[:20])
@@ -95,6 +115,25 @@ def test_plan_order_partials_and_workspace(case):
         assert p["workspace_bytes"] == math.ceil(rows * 128 * 4 / 256) * 256 + rows * 4
     else:
         assert p["workspace_bytes"] == 0
+
+
+def test_plan_tail_requests_are_cut_into_one_round():
+    """32 requests of ~4096 keys with 1-3 tiles: the longest-first prefix fills the
+    3 x 152 resident slots, the rest is cut into 456 // (its CTAs) chunks each."""
+    ql = [1 + (b % 6) for b in range(32)]
+    kv = [4096 + 16 * (31 - b) for b in range(32)]
+    p = plan_spec(kv, ql, 64, 8, 128, 16, 4095, 152, 2, 256)
+    ctas = [8 * math.ceil(8 * q / 16) for q in ql]
+    acc, first = 0, 0
+    for b in p["order"]:
+        if acc + ctas[b] > 456:
+            break
+        acc += ctas[b]
+        first += 1
+    tail = p["order"][first:]
+    k = 456 // sum(ctas[b] for b in tail)
+    assert k > 1 and all(p["n_chunks"][b] == k for b in tail)
+    assert all(p["n_chunks"][b] == 1 for b in p["order"][:first])
 
 
 def test_plan_skewed_long_request_is_split():
