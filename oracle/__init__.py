@@ -10,13 +10,16 @@ which holds no attention arithmetic.
 Every function follows a definition printed on the FlashInfer API pages
 ``batch_decode_with_paged_kv_cache`` (prims_ts), ``cudnn_batch_decode_with_kv_cache``
 and ``batch_prefill`` (prims_ts); the docstrings cite the page and parameter.
-bf16 inputs are taken as raw uint16 bit patterns and widened to float64
-exactly, so the oracle needs no bf16 support from any library.
+bf16 and fp16 inputs are taken as raw uint16 bit patterns and widened to
+float64 exactly (from each format's definition), so the oracle needs no
+16-bit float support from any library.
 """
 
 from .attention import (  # noqa: F401
     LOG2E,
     bf16_bits_to_f64,
+    f16_bits_to_f64,
+    bits_to_f64,
     gather_kv,
     decode_row_key_range,
     attention_rows,

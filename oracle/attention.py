@@ -45,11 +45,39 @@ def bf16_bits_to_f64(bits):
         return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
+def f16_bits_to_f64(bits):
+    """Widen IEEE binary16 values, given as uint16 bit patterns, to float64.
+
+    ``cudnn_batch_decode_with_kv_cache`` takes ``torch.float16`` as well as
+    ``torch.bfloat16`` inputs.  Written from the format's definition: sign bit
+    15, exponent bits 10-14 (bias 15), fraction bits 0-9; exponent 0 is
+    subnormal ``f / 2^10 * 2^-14``, exponent 31 is infinity (f = 0) or NaN.
+    """
+    b = np.asarray(bits).astype(np.int64)
+    sign = np.where((b >> 15) & 1, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    f = (b & 0x3FF).astype(np.float64)
+    normal = np.ldexp(1.0 + f / 1024.0, (e - 15).astype(np.int64))
+    sub = np.ldexp(f / 1024.0, -14)
+    out = np.where(e == 0, sub, normal)
+    out = np.where(e == 31, np.where(f == 0, np.inf, np.nan), out)
+    return sign * out
+
+
+def bits_to_f64(bits, dtype="bf16"):
+    """Input values of dtype ``'bf16'`` or ``'f16'`` (uint16 bit patterns) as float64."""
+    if dtype == "bf16":
+        return bf16_bits_to_f64(bits)
+    if dtype == "f16":
+        return f16_bits_to_f64(bits)
+    raise ValueError(f"unknown input dtype {dtype!r}")
+
+
 # ---------------------------------------------------------------------------
 # Paged K/V addressing
 # ---------------------------------------------------------------------------
 
-def gather_kv(pages_bits, block_table_row, page_size, kv_head, start, stop):
+def gather_kv(pages_bits, block_table_row, page_size, kv_head, start, stop, dtype="bf16"):
     """Rows ``start .. stop-1`` of one request's K (or V) for one KV head, float64.
 
     ``pages_bits`` is the HND page pool ``[num_pages, num_kv_heads, page_size,
@@ -60,7 +88,7 @@ def gather_kv(pages_bits, block_table_row, page_size, kv_head, start, stop):
     """
     t = np.arange(start, stop, dtype=np.int64)
     page = np.asarray(block_table_row, dtype=np.int64)[t // page_size]
-    return bf16_bits_to_f64(pages_bits[page, kv_head, t % page_size, :])
+    return bits_to_f64(pages_bits[page, kv_head, t % page_size, :], dtype)
 
 
 def decode_row_key_range(kv_len, q_len, i, causal, window_left):
@@ -130,10 +158,11 @@ def attention_rows(q_rows, keys, values, allowed, scale, sink=None, out_scale=1.
 
 def paged_decode_request(b, q_bits, k_pages_bits, v_pages_bits, block_tables, seq_lens_kv,
                          q_start, q_len, num_kv_heads, page_size, causal=False,
-                         window_left=-1, scale=None, bmm2_scale=1.0, sinks=None):
+                         window_left=-1, scale=None, bmm2_scale=1.0, sinks=None, dtype="bf16"):
     """Decode output of request ``b``: ``(O [q_len, Hq, D], LSE [q_len, Hq])``.
 
-    ``q_bits`` is the packed query ``[total_q, Hq, D]`` (bf16 bits); the
+    ``q_bits`` is the packed query ``[total_q, Hq, D]`` (bit patterns of
+    ``dtype``, ``'bf16'`` or ``'f16'``, like the K/V pools); the
     request's rows are ``q_start .. q_start + q_len - 1``
     (``batch_decode_with_paged_kv_cache``, parameter ``qo_indptr``).  Query
     head ``h`` reads KV head ``h // (Hq // Hkv)`` (GQA,
@@ -149,15 +178,15 @@ def paged_decode_request(b, q_bits, k_pages_bits, v_pages_bits, block_tables, se
         raise ValueError("every request needs kv_len >= q_len")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    q = bf16_bits_to_f64(q_bits[q_start:q_start + q_len])          # [L, Hq, D]
+    q = bits_to_f64(q_bits[q_start:q_start + q_len], dtype)        # [L, Hq, D]
     O = np.zeros((q_len, Hq, D), dtype=np.float64)
     LSE = np.zeros((q_len, Hq), dtype=np.float64)
     ranges = [decode_row_key_range(kv_len, q_len, i, causal, window_left) for i in range(q_len)]
     first = min(lo for lo, _ in ranges)
     last = max(hi for _, hi in ranges)
     for hk in range(num_kv_heads):
-        K = gather_kv(k_pages_bits, block_tables[b], page_size, hk, first, last)
-        V = gather_kv(v_pages_bits, block_tables[b], page_size, hk, first, last)
+        K = gather_kv(k_pages_bits, block_tables[b], page_size, hk, first, last, dtype)
+        V = gather_kv(v_pages_bits, block_tables[b], page_size, hk, first, last, dtype)
         keys = np.arange(first, last)
         allowed = np.stack([(keys >= lo) & (keys < hi) for lo, hi in ranges])   # [L, n]
         for g in range(group):
@@ -171,7 +200,7 @@ def paged_decode_request(b, q_bits, k_pages_bits, v_pages_bits, block_tables, se
 
 def paged_decode(q_bits, k_pages_bits, v_pages_bits, block_tables, seq_lens_kv, num_kv_heads,
                  page_size, qo_indptr=None, q_len=1, causal=False, window_left=-1, scale=None,
-                 bmm2_scale=1.0, sinks=None, requests=None):
+                 bmm2_scale=1.0, sinks=None, requests=None, dtype="bf16"):
     """Paged decode over a batch: ``(O [total_q, Hq, D], LSE [total_q, Hq])``.
 
     Without ``qo_indptr`` every request has ``q_len`` consecutive rows
@@ -190,7 +219,7 @@ def paged_decode(q_bits, k_pages_bits, v_pages_bits, block_tables, seq_lens_kv, 
         s0, s1 = int(qo_indptr[b]), int(qo_indptr[b + 1])
         o, lse = paged_decode_request(b, q_bits, k_pages_bits, v_pages_bits, block_tables,
                                       seq_lens_kv, s0, s1 - s0, num_kv_heads, page_size,
-                                      causal, window_left, scale, bmm2_scale, sinks)
+                                      causal, window_left, scale, bmm2_scale, sinks, dtype)
         O[s0:s1] = o
         LSE[s0:s1] = lse
     return O, LSE
@@ -234,7 +263,7 @@ def merge_states(v_states, s_states):
 
 def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads, causal=True,
                     sm_scale=None, output_scale=1.0, heads=None, rows=None, window_left=-1,
-                    window_bounds=None):
+                    window_bounds=None, dtype="bf16"):
     """Prefill output of request ``b``: ``(O [Lq, Hq, D], LSE [Lq, Hq])``.
 
     Packed storage: request ``b`` owns query rows ``qo_indptr[b] ..
@@ -272,9 +301,9 @@ def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_head
         allowed[r] = (keys >= lo) & (keys < hi)
     for h in heads:
         hk = h // group
-        Q = bf16_bits_to_f64(q_bits[q0 + rows, h, :])
-        K = bf16_bits_to_f64(k_bits[k0:k1, hk, :])
-        V = bf16_bits_to_f64(v_bits[k0:k1, hk, :])
+        Q = bits_to_f64(q_bits[q0 + rows, h, :], dtype)
+        K = bits_to_f64(k_bits[k0:k1, hk, :], dtype)
+        V = bits_to_f64(v_bits[k0:k1, hk, :], dtype)
         o, lse = attention_rows(Q, K, V, allowed, sm_scale, None, output_scale)
         O[rows, h, :] = o
         LSE[rows, h] = lse
@@ -283,7 +312,7 @@ def prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_head
 
 def batch_prefill(q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads, causal=True,
                   sm_scale=None, output_scale=1.0, window_left=-1, window_starts=None,
-                  window_ends=None):
+                  window_ends=None, dtype="bf16"):
     """Ragged prefill over the whole batch: ``(O [total_q, Hq, D], LSE [total_q, Hq])``.
 
     ``window_starts`` / ``window_ends`` (``[B, Sq]``, fixed-shape batches only,
@@ -300,7 +329,7 @@ def batch_prefill(q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads, ca
             bounds = (np.asarray(window_starts)[b], np.asarray(window_ends)[b])
         o, lse = prefill_request(b, q_bits, k_bits, v_bits, qo_indptr, kv_indptr, num_kv_heads,
                                  causal, sm_scale, output_scale, window_left=window_left,
-                                 window_bounds=bounds)
+                                 window_bounds=bounds, dtype=dtype)
         O[q0:q1] = o
         LSE[q0:q1] = lse
     return O, LSE

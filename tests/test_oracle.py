@@ -527,3 +527,37 @@ def test_prefill_variable_window_special_cases():
     for b in range(B):
         for i in range(Sq):
             assert np.array_equal(a[0][b * Sq + i, 0], v.double()[b * Sk + i + 2, 0].numpy())
+
+
+def test_f16_widening_matches_numpy_on_every_pattern():
+    """The binary16 definition written out in the oracle against numpy's float16."""
+    bits = np.arange(65536, dtype=np.uint16)
+    ours = oracle.f16_bits_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_f16_and_bf16_inputs_agree_on_shared_values():
+    """Values both formats hold exactly (small integers / 8) give one result either way."""
+    g = np.random.default_rng(5)
+    B, Hq, Hkv, ps, D = 2, 4, 2, 16, 128
+    vals = g.integers(-16, 17, size=(6, Hq, D)) / 8.0
+    kv = g.integers(-16, 17, size=(8, Hkv, ps, D)) / 8.0
+    vv = g.integers(-16, 17, size=(8, Hkv, ps, D)) / 8.0
+    as_f16 = lambda x: np.asarray(x, np.float16).view(np.uint16)
+    as_bf16 = lambda x: (np.asarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    bt = np.array([[3, 1, 5, 7], [0, 2, 4, 6]])
+    seq = np.array([50, 33])
+    kw = dict(qo_indptr=[0, 3, 6], causal=True, window_left=20)
+    a = oracle.paged_decode(as_f16(vals), as_f16(kv), as_f16(vv), bt, seq, Hkv, ps, dtype="f16", **kw)
+    b = oracle.paged_decode(as_bf16(vals), as_bf16(kv), as_bf16(vv), bt, seq, Hkv, ps, **kw)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    qp = g.integers(-16, 17, size=(40, Hq, D)) / 8.0
+    kp = g.integers(-16, 17, size=(40, Hkv, D)) / 8.0
+    ind = np.array([0, 15, 40])
+    a = oracle.batch_prefill(as_f16(qp), as_f16(kp), as_f16(kp), ind, ind, Hkv, dtype="f16")
+    b = oracle.batch_prefill(as_bf16(qp), as_bf16(kp), as_bf16(kp), ind, ind, Hkv)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
