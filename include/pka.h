@@ -28,8 +28,10 @@
  *   - Device pointers are raw CUDA device addresses of the current device.
  *     `stream` is a cudaStream_t (NULL = legacy default stream).
  *   - Element strides are in elements, not bytes.
- *   - Only bf16 (PKA_DTYPE_BF16) q/K/V/out are supported; f16 returns
- *     PKA_ERR_UNSUPPORTED.  head_dim must be 128.
+ *   - q/K/V are bf16 (PKA_DTYPE_BF16) or IEEE half (PKA_DTYPE_F16), one type
+ *     for all three (cudnn_batch_decode_with_kv_cache, q: float16 or
+ *     bfloat16); the output is bf16, f16 or fp32 (out_dtype of
+ *     batch_decode_with_paged_kv_cache and batch_prefill).  head_dim must be 128.
  *   - The caller owns every device buffer (q, pools, tables, lengths, out,
  *     lse, workspace).  The library owns only the opaque plan objects.
  *   - *_run entry points allocate nothing, never synchronise and never read
@@ -92,7 +94,7 @@ const char* pka_version(void);
  * page_size          tokens per page: a multiple of 16 in [16, 256].
  * max_pages_per_seq  C, the number of entries in each block_tables row.
  * num_pages          pages in each of the K and V pools.
- * dtype              PKA_DTYPE_BF16.
+ * dtype              PKA_DTYPE_BF16 or PKA_DTYPE_F16: q and the K/V pools.
  * q_len              fixed query rows per request, used when the plan gets no
  *                    qo_indptr (batch_decode_with_paged_kv_cache, seq_len_q).
  * max_q_len          packed mode: per-request capacity (0 = derive from
@@ -123,6 +125,9 @@ const char* pka_version(void);
  * mma_min_rows       the tensor-core kernel is used when
  *                    (Hq/Hkv) * max_q_len >= mma_min_rows; 0 = default (8).
  * flags              PKA_PLAN_HOST_ONLY or 0.
+ * out_dtype          PKA_DTYPE_BF16, PKA_DTYPE_F16 or PKA_DTYPE_F32: O of
+ *                    paged_decode_run (batch_decode_with_paged_kv_cache,
+ *                    out_dtype; a zeroed descriptor means bf16).
  */
 typedef struct pka_decode_desc {
   int32_t batch_size;
@@ -146,6 +151,7 @@ typedef struct pka_decode_desc {
   int32_t min_chunk_tokens;
   int32_t mma_min_rows;
   int32_t flags;
+  int32_t out_dtype;
 } pka_decode_desc;
 
 typedef struct pka_plan pka_plan; /* opaque decode plan */
@@ -296,7 +302,7 @@ int paged_decode_run_noalloc(const pka_plan* plan, const void* q, int64_t q_stri
  * s_states   fp32 [num_states, num_rows, num_heads] contiguous: each state's
  *            base-2 LSE (-inf for an empty subset).
  * v_out      [num_rows, num_heads, head_dim] contiguous, out_dtype
- *            PKA_DTYPE_BF16 or PKA_DTYPE_F32:
+ *            PKA_DTYPE_BF16, PKA_DTYPE_F16 or PKA_DTYPE_F32:
  *            sum_i 2^(s_i - m) v_i / sum_i 2^(s_i - m), m = max_i s_i.
  * s_out      NULL or fp32 [num_rows, num_heads]: m + log2 sum_i 2^(s_i - m).
  * Rows whose states are all -inf get v = 0 and s = -inf.
@@ -321,6 +327,9 @@ int attn_merge_lse(const float* v_states, const float* s_states, int32_t num_sta
  * output_scale multiplies O (batch_prefill, output_scale).
  * return_lse   nonzero: batch_prefill_run writes the base-2 LSE.
  * num_sms      0 = the device's.   flags  PKA_PLAN_HOST_ONLY or 0.
+ * dtype        PKA_DTYPE_BF16 or PKA_DTYPE_F16: q, k and v.
+ * out_dtype    PKA_DTYPE_BF16, PKA_DTYPE_F16 or PKA_DTYPE_F32: O (batch_prefill,
+ *              out_dtype; a zeroed descriptor means bf16).
  */
 typedef struct pka_prefill_desc {
   int32_t batch_size;
@@ -335,6 +344,7 @@ typedef struct pka_prefill_desc {
   int32_t return_lse;
   int32_t num_sms;
   int32_t flags;
+  int32_t out_dtype;
 } pka_prefill_desc;
 
 typedef struct pka_prefill_plan pka_prefill_plan; /* opaque prefill plan */

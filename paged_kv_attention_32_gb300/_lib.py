@@ -47,7 +47,7 @@ class DecodeDesc(ctypes.Structure):
         ("return_lse", ctypes.c_int32), ("freeze_seq_lens", ctypes.c_int32),
         ("num_sms", ctypes.c_int32), ("split_waves", ctypes.c_int32),
         ("min_chunk_tokens", ctypes.c_int32), ("mma_min_rows", ctypes.c_int32),
-        ("flags", ctypes.c_int32),
+        ("flags", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
     ]
 
 
@@ -69,6 +69,7 @@ class PrefillDesc(ctypes.Structure):
         ("dtype", ctypes.c_int32), ("mask", ctypes.c_int32), ("window_left", ctypes.c_int32),
         ("sm_scale", ctypes.c_float), ("output_scale", ctypes.c_float),
         ("return_lse", ctypes.c_int32), ("num_sms", ctypes.c_int32), ("flags", ctypes.c_int32),
+        ("out_dtype", ctypes.c_int32),
     ]
 
 

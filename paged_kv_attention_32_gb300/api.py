@@ -25,6 +25,28 @@ def _ptr(t):
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
+_DTYPES = {torch.bfloat16: L.PKA_DTYPE_BF16, torch.float16: L.PKA_DTYPE_F16,
+           torch.float32: L.PKA_DTYPE_F32}
+_TORCH = {v: k for k, v in _DTYPES.items()}
+
+
+def _dtype_codes(dtype, out_dtype):
+    """(input code, output code) of torch dtypes; the output defaults to the input type."""
+    if dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError(f"q/K/V dtype must be bfloat16 or float16, got {dtype}")
+    out_dtype = dtype if out_dtype is None else out_dtype
+    if out_dtype not in _DTYPES:
+        raise ValueError(f"out_dtype must be bfloat16, float16 or float32, got {out_dtype}")
+    return _DTYPES[dtype], _DTYPES[out_dtype]
+
+
+def _check_inputs(plan, *tensors):
+    want = _TORCH[plan.desc.dtype]
+    for t in tensors:
+        if t.dtype != want:
+            raise ValueError(f"the plan was made for {want} inputs, got {t.dtype}")
+
+
 def _host_i32(x):
     """Contiguous host int32 array (kept alive by the caller) and its pointer."""
     if x is None:
@@ -74,14 +96,18 @@ def paged_decode_plan(seq_lens_kv, *, num_qo_heads, num_kv_heads, page_size, max
                       num_pages, qo_indptr=None, q_len=1, max_q_len=0, causal=False,
                       window_left=-1, scale=None, bmm2_scale=1.0, return_lse=False,
                       freeze_seq_lens=True, num_sms=0, split_waves=0, min_chunk_tokens=0,
-                      mma_min_rows=0, host_only=False, head_dim=128, stream=None):
-    """Plan a batched paged decode from host copies of the lengths (see pka.h)."""
+                      mma_min_rows=0, host_only=False, head_dim=128, dtype=torch.bfloat16,
+                      out_dtype=None, stream=None):
+    """Plan a batched paged decode from host copies of the lengths (see pka.h).
+    ``dtype``: q and the K/V pools (bfloat16 or float16); ``out_dtype``: O (bfloat16,
+    float16 or float32; default ``dtype``)."""
+    in_code, out_code = _dtype_codes(dtype, out_dtype)
     seq_t, seq_p = _host_i32(seq_lens_kv)
     ind_t, ind_p = _host_i32(qo_indptr)
     d = L.DecodeDesc(
         batch_size=seq_t.numel(), num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
         head_dim=head_dim, page_size=page_size, max_pages_per_seq=max_pages_per_seq,
-        num_pages=num_pages, dtype=L.PKA_DTYPE_BF16, q_len=q_len, max_q_len=max_q_len,
+        num_pages=num_pages, dtype=in_code, out_dtype=out_code, q_len=q_len, max_q_len=max_q_len,
         mask=L.PKA_MASK_CAUSAL if causal else L.PKA_MASK_DENSE, window_left=window_left,
         scale=float("nan") if scale is None else scale, bmm2_scale=bmm2_scale,
         return_lse=int(bool(return_lse)), freeze_seq_lens=int(bool(freeze_seq_lens)),
@@ -98,9 +124,12 @@ def paged_decode_plan(seq_lens_kv, *, num_qo_heads, num_kv_heads, page_size, max
 def paged_decode_run(plan, q, k_pages, v_pages, block_tables, seq_lens_kv=None, sinks=None,
                      out=None, lse=None, workspace=None, stream=None):
     """Run a planned decode; returns ``out`` (and ``lse`` when the plan returns it)."""
+    _check_inputs(plan, q, k_pages, v_pages)
+    if out is not None and out.dtype != _TORCH[plan.desc.out_dtype]:
+        raise ValueError(f"out must be {_TORCH[plan.desc.out_dtype]} (the plan's out_dtype)")
     total_q, Hq, D = q.shape
     if out is None:
-        out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((total_q, Hq, D), dtype=_TORCH[plan.desc.out_dtype], device=q.device)
     if plan.desc.return_lse and lse is None:
         lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
     if workspace is None and plan.workspace_bytes > 0:
@@ -123,7 +152,7 @@ def attn_merge_lse(v_states, s_states, out_dtype=torch.bfloat16, v_out=None, s_o
         v_out = torch.empty((S, H, D), dtype=out_dtype, device=v_states.device)
     if s_out is None:
         s_out = torch.empty((S, H), dtype=torch.float32, device=v_states.device)
-    code = L.PKA_DTYPE_BF16 if v_out.dtype == torch.bfloat16 else L.PKA_DTYPE_F32
+    code = _DTYPES[v_out.dtype]
     rc = L.lib().attn_merge_lse(_ptr(v_states), _ptr(s_states), N, S, H, D, _ptr(v_out), code,
                                 _ptr(s_out), _stream(stream))
     L.check(rc, "attn_merge_lse")
@@ -149,13 +178,16 @@ class PrefillPlan:
 
 def batch_prefill_plan(qo_indptr, kv_indptr, *, num_qo_heads, num_kv_heads, causal=True,
                        sm_scale=None, output_scale=1.0, return_lse=False, head_dim=128,
-                       window_left=-1, host_only=False, stream=None):
-    """Plan a packed ragged prefill from host copies of the indptr arrays."""
+                       window_left=-1, host_only=False, dtype=torch.bfloat16, out_dtype=None,
+                       stream=None):
+    """Plan a packed ragged prefill from host copies of the indptr arrays (``dtype`` /
+    ``out_dtype`` as for ``paged_decode_plan``)."""
+    in_code, out_code = _dtype_codes(dtype, out_dtype)
     qo_t, qo_p = _host_i32(qo_indptr)
     kv_t, kv_p = _host_i32(kv_indptr)
     d = L.PrefillDesc(
         batch_size=qo_t.numel() - 1, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
-        head_dim=head_dim, dtype=L.PKA_DTYPE_BF16,
+        head_dim=head_dim, dtype=in_code, out_dtype=out_code,
         mask=L.PKA_MASK_CAUSAL if causal else L.PKA_MASK_DENSE, window_left=window_left,
         sm_scale=float("nan") if sm_scale is None else sm_scale, output_scale=output_scale,
         return_lse=int(bool(return_lse)), num_sms=0,
@@ -174,18 +206,20 @@ def batch_prefill_plan_fixed(batch_size, seq_len_q, seq_len_kv, *, num_qo_heads,
                              mask_type="causal", window_left=-1,
                              variable_window_token_starts=None, variable_window_token_ends=None,
                              sm_scale=None, output_scale=1.0, return_lse=False, head_dim=128,
-                             host_only=False, stream=None):
+                             host_only=False, dtype=torch.bfloat16, out_dtype=None, stream=None):
     """Plan a fixed-shape prefill: q ``[B, Sq, Hq, D]``, k/v ``[B, Sk, Hkv, D]`` (run it with
     ``batch_prefill_run`` on the tensors viewed as ``[B*S, H, D]``).  ``mask_type``:
     ``'causal'``, ``'dense'`` or ``'variable_window'`` (inclusive per-query key bounds
     ``[B, Sq]``; host copies are taken here for planning)."""
     masks = {"dense": L.PKA_MASK_DENSE, "causal": L.PKA_MASK_CAUSAL,
              "variable_window": L.PKA_MASK_VARIABLE_WINDOW}
+    in_code, out_code = _dtype_codes(dtype, out_dtype)
     st_t, st_p = _host_i32(variable_window_token_starts)
     en_t, en_p = _host_i32(variable_window_token_ends)
     d = L.PrefillDesc(
         batch_size=batch_size, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
-        head_dim=head_dim, dtype=L.PKA_DTYPE_BF16, mask=masks[mask_type], window_left=window_left,
+        head_dim=head_dim, dtype=in_code, out_dtype=out_code, mask=masks[mask_type],
+        window_left=window_left,
         sm_scale=float("nan") if sm_scale is None else sm_scale, output_scale=output_scale,
         return_lse=int(bool(return_lse)), num_sms=0,
         flags=L.PKA_PLAN_HOST_ONLY if host_only else 0)
@@ -215,9 +249,12 @@ def batch_prefill_run(plan, q, k, v, out=None, lse=None, stream=None):
         if plan.desc.return_lse:
             return res[0].view(B, Sq, *res[0].shape[1:]), res[1].view(B, Sq, res[1].shape[1])
         return res.view(B, Sq, *res.shape[1:])
+    _check_inputs(plan, q, k, v)
+    if out is not None and out.dtype != _TORCH[plan.desc.out_dtype]:
+        raise ValueError(f"out must be {_TORCH[plan.desc.out_dtype]} (the plan's out_dtype)")
     total_q, Hq, D = q.shape
     if out is None:
-        out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((total_q, Hq, D), dtype=_TORCH[plan.desc.out_dtype], device=q.device)
     if plan.desc.return_lse and lse is None:
         lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
     rc = L.lib().batch_prefill_run(plan.handle, _ptr(q), q.stride(0), q.stride(1), _ptr(k),

@@ -281,6 +281,8 @@ int paged_decode_run(const pka_plan* p, const void* q, int64_t q_stride_tok,
   a.rows_per_cta = p->rows_per_cta;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.bmm2_scale = p->desc.bmm2_scale;
+  a.in_f16 = p->desc.dtype == PKA_DTYPE_F16;
+  a.out_dtype = p->desc.out_dtype;
   return launch_decode(*p, a, kmap, vmap, static_cast<cudaStream_t>(stream));
 }
 
@@ -303,8 +305,8 @@ int attn_merge_lse(const float* v_states, const float* s_states, int32_t num_sta
   PKA_CHECK_ARG(num_rows >= 0 && num_heads >= 1, "bad row/head counts");
   PKA_CHECK_ARG(head_dim >= 4 && head_dim % 4 == 0 && head_dim <= 1024,
                 "head_dim must be a multiple of 4 in [4, 1024]");
-  if (out_dtype != PKA_DTYPE_BF16 && out_dtype != PKA_DTYPE_F32)
-    return fail(PKA_ERR_UNSUPPORTED, "out_dtype must be bf16 or f32");
+  if (out_dtype != PKA_DTYPE_BF16 && out_dtype != PKA_DTYPE_F16 && out_dtype != PKA_DTYPE_F32)
+    return fail(PKA_ERR_UNSUPPORTED, "out_dtype must be bf16, f16 or f32");
   PKA_CHECK_ARG(aligned(v_states, 16) && aligned(v_out, 16),
                 "v_states and v_out must be 16-byte aligned");
   return launch_merge_states(v_states, s_states, num_states, num_rows, num_heads, head_dim, v_out,
@@ -431,6 +433,7 @@ int batch_prefill_run(const pka_prefill_plan* p, const void* q, int64_t q_stride
   a.heads_per_cta = p->heads_per_cta;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.output_scale = p->desc.output_scale;
+  a.out_dtype = p->desc.out_dtype;
   return launch_prefill(*p, a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream));
 }
 

@@ -23,7 +23,7 @@
 //  * p.v: the same lanes accumulate p * v for all R rows over their dims;
 //    probabilities go through a 16 x R shared buffer;
 //  * the four warps' (m, l, acc) are merged through shared memory; the CTA
-//    then writes the final bf16 O and LSE (sink added here), or an fp32
+//    then writes the final O (bf16, f16 or fp32) and LSE (sink added here), or an fp32
 //    partial (O/l, m + log2 l) for the merge kernel when the request was
 //    split.
 #include <cuda_bf16.h>
@@ -56,7 +56,8 @@ __device__ __forceinline__ uint32_t unit_chunk_offset(int j, int cg) {
   return (uint32_t)(cg >> 3) * kBoxBytes + swz128((uint32_t)j, (uint32_t)(cg & 7));
 }
 
-template <int R, int NSTAGE>
+// F16: q/K/V are IEEE half (else bf16).
+template <int R, int NSTAGE, bool F16>
 __global__ void __launch_bounds__(128, 2)
 decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmv) {
@@ -116,13 +117,13 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
   // ---- q in registers, slot s holding row s ^ my_row, scaled by scale*log2(e) ----
   float2 q2[R][DL / 2];
   {
-    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    const uint16_t* qb = static_cast<const uint16_t*>(a.q);   // 16-bit elements
 #pragma unroll
     for (int s = 0; s < R; ++s) {
       const int r = s ^ my_row;
       if (r < rows_b) {
         const int t = rq.q_start + r / G, h = hk * G + r % G;
-        const __nv_bfloat16* src = qb + (int64_t)t * a.q_stride_tok + (int64_t)h * a.q_stride_head;
+        const uint16_t* src = qb + (int64_t)t * a.q_stride_tok + (int64_t)h * a.q_stride_head;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
           const int cg = e + c * LK;
@@ -130,7 +131,7 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            float2 f = bf16x2_to_float2(ws[x]);
+            float2 f = unpack2<F16>(ws[x]);
             q2[s][c * 4 + x] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
           }
         }
@@ -203,10 +204,10 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         const uint4 w = *reinterpret_cast<const uint4*>(ks + unit_chunk_offset(j, e + c * LK));
-        k2[c * 4 + 0] = bf16x2_to_float2(w.x);
-        k2[c * 4 + 1] = bf16x2_to_float2(w.y);
-        k2[c * 4 + 2] = bf16x2_to_float2(w.z);
-        k2[c * 4 + 3] = bf16x2_to_float2(w.w);
+        k2[c * 4 + 0] = unpack2<F16>(w.x);
+        k2[c * 4 + 1] = unpack2<F16>(w.y);
+        k2[c * 4 + 2] = unpack2<F16>(w.z);
+        k2[c * 4 + 3] = unpack2<F16>(w.w);
       }
       float part[R];
 #pragma unroll
@@ -279,10 +280,10 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         const uint4 w = *reinterpret_cast<const uint4*>(vs + unit_chunk_offset(j, e + c * LK));
-        v2[c * 4 + 0] = bf16x2_to_float2(w.x);
-        v2[c * 4 + 1] = bf16x2_to_float2(w.y);
-        v2[c * 4 + 2] = bf16x2_to_float2(w.z);
-        v2[c * 4 + 3] = bf16x2_to_float2(w.w);
+        v2[c * 4 + 0] = unpack2<F16>(w.x);
+        v2[c * 4 + 1] = unpack2<F16>(w.y);
+        v2[c * 4 + 2] = unpack2<F16>(w.z);
+        v2[c * 4 + 3] = unpack2<F16>(w.w);
       }
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -333,7 +334,6 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
   __syncthreads();
 
   const int d = tid;   // 128 threads <-> 128 dims
-  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
   for (int r = 0; r < rows_b && r < R; ++r) {
     float m = neg_inf();
 #pragma unroll
@@ -355,7 +355,7 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
       float denom = lsum;
       if (a.sinks != nullptr && m != neg_inf()) denom += ex2(__ldg(a.sinks + h) * kLog2e - m);
       const float ov = denom > 0.f ? a.bmm2_scale * o / denom : 0.f;
-      out[((int64_t)t * a.num_qo_heads + h) * 128 + d] = __float2bfloat16_rn(ov);
+      store_out1(a.out, ((int64_t)t * a.num_qo_heads + h) * 128 + d, ov, a.out_dtype);
       if (a.lse != nullptr && d == 0)
         a.lse[(int64_t)t * a.num_qo_heads + h] = lsum > 0.f ? m + log2f(lsum) : neg_inf();
     } else {
@@ -399,22 +399,19 @@ decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
   if (a.sinks != nullptr && m != neg_inf()) denom += ex2(__ldg(a.sinks + h) * kLog2e - m);
   const float sc = denom > 0.f ? a.bmm2_scale / denom : 0.f;
   const int64_t t = rq.q_start + row.row;
-  uint2 packed;
-  packed.x = float2_to_bf16x2(o.x * sc, o.y * sc);
-  packed.y = float2_to_bf16x2(o.z * sc, o.w * sc);
-  *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
-                            (t * a.num_qo_heads + h) * 128 + lane * 4) = packed;
+  const float ov[4] = {o.x, o.y, o.z, o.w};
+  store_out<4>(a.out, (t * a.num_qo_heads + h) * 128 + lane * 4, ov, sc, a.out_dtype);
   if (a.lse != nullptr && lane == 0)
     a.lse[t * a.num_qo_heads + h] = wsum > 0.f ? m + log2f(wsum) : neg_inf();
 }
 
-template <int R, int NSTAGE>
+template <int R, int NSTAGE, bool F16>
 int launch_cc(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMap& vmap,
               cudaStream_t stream) {
   const size_t smem = 1024 + (size_t)kWarps * NSTAGE * kStageBytes +
                       (size_t)kWarps * kUnit * R * sizeof(float) + kWarps * NSTAGE * 8;
   static_assert(kWarps * R * 130 * 4 <= kWarps * NSTAGE * kStageBytes, "combine area too small");
-  auto kern = decode_cc_kernel<R, NSTAGE>;
+  auto kern = decode_cc_kernel<R, NSTAGE, F16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_cc)");
   kern<<<args.num_items, 128, smem, stream>>>(args, kmap, vmap);
@@ -434,9 +431,11 @@ int launch_decode(const pka_plan& plan, const DecodeArgs& args, const CUtensorMa
   if (plan.kernel == PKA_KERNEL_MMA) {
     rc = launch_decode_mma(plan, args, kmap, vmap, stream);
   } else if (plan.rows_per_cta <= 4) {
-    rc = launch_cc<4, 3>(args, kmap, vmap, stream);
+    rc = args.in_f16 ? launch_cc<4, 3, true>(args, kmap, vmap, stream)
+                     : launch_cc<4, 3, false>(args, kmap, vmap, stream);
   } else {
-    rc = launch_cc<8, 3>(args, kmap, vmap, stream);
+    rc = args.in_f16 ? launch_cc<8, 3, true>(args, kmap, vmap, stream)
+                     : launch_cc<8, 3, false>(args, kmap, vmap, stream);
   }
   if (rc != PKA_OK) return rc;
   if (args.num_merge_rows > 0) {

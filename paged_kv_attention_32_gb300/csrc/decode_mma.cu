@@ -4,7 +4,7 @@
 // cudnn_batch_decode_with_kv_cache's q_len_per_req rows).
 //
 // Same work items, masks, softmax and outputs as the CUDA-core kernel; the
-// two contractions run on mma.sync m16n8k16 (bf16 in, fp32 accumulate):
+// two contractions run on mma.sync m16n8k16 (bf16 or f16 in, fp32 accumulate):
 //  * a CTA handles one 16-row tile of the item's query rows (row r = i*group
 //    + g: token i, head g of the group); blockIdx.x = item * MT + tile, so
 //    the MT tiles of one item run side by side and all but the first read its
@@ -15,7 +15,7 @@
 //    its own copies: copies of one issuing thread complete at roughly one
 //    per microsecond whatever their size, so many issuers are needed;
 //  * per unit: S = Q K^T (2 n-tiles x 8 k-steps, Q in A-fragment registers),
-//    mask, online softmax in base 2 on the fragments, P re-packed to bf16
+//    mask, online softmax in base 2 on the fragments, P re-packed to 16-bit
 //    A fragments in registers, O += P V (16 n-tiles, V via ldmatrix.trans);
 //  * the four warps' (m, l, O) are merged through shared memory and the CTA
 //    writes final O/LSE (sink added) or an fp32 partial for the merge kernel.
@@ -39,7 +39,7 @@ constexpr int kUnit = kMmaUnitTok;
 constexpr int kStageBytes = kMmaUnitBytes;
 constexpr int kBoxBytes = kMmaBoxBytes;
 
-template <int NSTAGE>
+template <int NSTAGE, bool F16>
 __global__ void __launch_bounds__(kWarps * 32, 3)
 decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
@@ -84,7 +84,7 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   }
   __syncthreads();
 
-  MmaTileWarp tw;
+  MmaTileWarp<F16> tw;
   tw.init(a, rq, kv_len, hk, mt, lane);
   const float sl2 = a.scale_log2;
 
@@ -145,13 +145,13 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
                     chunk);
 }
 
-template <int NSTAGE>
+template <int NSTAGE, bool F16>
 int launch_mma(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMap& vmap,
                cudaStream_t stream) {
   const size_t smem = 1024 + (size_t)kWarps * NSTAGE * kStageBytes + kWarps * NSTAGE * 8;
   static_assert(kWarps * 16 * (kMmaCombStride + 2) * 4 <= kWarps * NSTAGE * kStageBytes,
                 "merge buffer does not fit in the stage area");
-  auto kern = decode_mma_kernel<NSTAGE>;
+  auto kern = decode_mma_kernel<NSTAGE, F16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_mma)");
   const int mt = (args.rows_per_cta + 15) / 16;
@@ -168,7 +168,8 @@ int launch_mma(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMa
 int launch_decode_mma(const pka_plan& plan, const DecodeArgs& args, const CUtensorMap& kmap,
                       const CUtensorMap& vmap, cudaStream_t stream) {
   (void)plan;
-  return launch_mma<2>(args, kmap, vmap, stream);
+  return args.in_f16 ? launch_mma<2, true>(args, kmap, vmap, stream)
+                     : launch_mma<2, false>(args, kmap, vmap, stream);
 }
 
 }  // namespace pka

@@ -8,9 +8,10 @@
 //                       Q kept as A fragments in registers)
 //   mask               (causal diagonal kv_len - q_len + i, window_left)
 //   online softmax     (base 2, the scale folded into one multiply)
-//   O += P V           (P re-packed to bf16 A fragments, V via ldmatrix.trans)
-// The units are four 2 KB boxes with 128-byte swizzle: K columns 0-63,
-// K 64-127, V 0-63, V 64-127, each 16 tokens x 128 bytes.
+//   O += P V           (P re-packed to A fragments of the input type, V via
+//                       ldmatrix.trans)
+// A unit is four 2 KB blocks with 128-byte swizzle: K columns 0-63, K 64-127,
+// V 0-63, V 64-127, each 16 tokens x 128 bytes.  q/K/V are bf16 or IEEE half.
 #pragma once
 
 #include "device_common.cuh"
@@ -37,6 +38,8 @@ __device__ __forceinline__ uint32_t mma_unit_chunk_offset(int j, int cg) {
   return (uint32_t)(cg >> 3) * kMmaBoxBytes + swz128((uint32_t)j, (uint32_t)(cg & 7));
 }
 
+// F16: q/K/V are IEEE half (else bf16); P is packed in the same type.
+template <bool F16>
 struct MmaTileWarp {
   uint32_t qa[8][4];    // Q A fragments, k-step ks
   float acc[16][4];     // O accumulators, 16 n-tiles of 8 dims
@@ -52,9 +55,9 @@ struct MmaTileWarp {
     loA = 0; hiA = 0x7fffffff; loB = 0; hiB = 0x7fffffff;
     if (rA < rows_b) mma_row_key_range(kv_len, L, rA / G, a.causal, a.window_left, loA, hiA);
     if (rB < rows_b) mma_row_key_range(kv_len, L, rB / G, a.causal, a.window_left, loB, hiB);
-    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* srcA = nullptr;
-    const __nv_bfloat16* srcB = nullptr;
+    const uint16_t* qb = static_cast<const uint16_t*>(a.q);   // 16-bit elements
+    const uint16_t* srcA = nullptr;
+    const uint16_t* srcB = nullptr;
     if (rA < rows_b)
       srcA = qb + (int64_t)(rq.q_start + rA / G) * a.q_stride_tok +
              (int64_t)(hk * G + rA % G) * a.q_stride_head;
@@ -97,8 +100,8 @@ struct MmaTileWarp {
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(k_u32 + mma_unit_chunk_offset(nt * 8 + lm_row, kp * 4 + lm_mat), b0, b1, b2,
                     b3);
-        mma_bf16_16816(s[nt], qa[2 * kp], b0, b1);
-        mma_bf16_16816(s2[nt], qa[2 * kp + 1], b2, b3);
+        mma_16816<F16>(s[nt], qa[2 * kp], b0, b1);
+        mma_16816<F16>(s2[nt], qa[2 * kp + 1], b2, b3);
       }
     }
 #pragma unroll
@@ -151,10 +154,10 @@ struct MmaTileWarp {
       }
     }
     uint32_t pa[4];
-    pa[0] = float2_to_bf16x2(s[0][0], s[0][1]);
-    pa[1] = float2_to_bf16x2(s[0][2], s[0][3]);
-    pa[2] = float2_to_bf16x2(s[1][0], s[1][1]);
-    pa[3] = float2_to_bf16x2(s[1][2], s[1][3]);
+    pa[0] = pack2<F16>(s[0][0], s[0][1]);
+    pa[1] = pack2<F16>(s[0][2], s[0][3]);
+    pa[2] = pack2<F16>(s[1][0], s[1][1]);
+    pa[3] = pack2<F16>(s[1][2], s[1][3]);
     // O += P V : 16 n-tiles of 8 dims
 #pragma unroll
     for (int np = 0; np < 8; ++np) {
@@ -162,8 +165,8 @@ struct MmaTileWarp {
       ldmatrix_x4_trans(v_u32 + mma_unit_chunk_offset((lm_mat & 1) * 8 + lm_row,
                                                       np * 2 + (lm_mat >> 1)),
                         b0, b1, b2, b3);
-      mma_bf16_16816(acc[2 * np], pa, b0, b1);
-      mma_bf16_16816(acc[2 * np + 1], pa, b2, b3);
+      mma_16816<F16>(acc[2 * np], pa, b0, b1);
+      mma_16816<F16>(acc[2 * np + 1], pa, b2, b3);
     }
   }
 
@@ -198,7 +201,7 @@ struct MmaTileWarp {
 };
 
 // Combines merge slots [slot0, slot0 + nslots) for row `row` of tile `tile`
-// (dims d0 .. d0+15) and writes the final bf16 O and base-2 LSE (sink added
+// (dims d0 .. d0+15) and writes the final O (out_dtype) and base-2 LSE (sink added
 // to the denominator, bmm2_scale applied) or, for a split request, the fp32
 // partial (O/l, m + log2 l) of chunk `chunk`.
 __device__ __forceinline__ void mma_combine_store(const DecodeArgs& a, const ReqInfo& rq,
@@ -237,19 +240,7 @@ __device__ __forceinline__ void mma_combine_store(const DecodeArgs& a, const Req
     float denom = lsum;
     if (a.sinks != nullptr && m != neg_inf()) denom += ex2(__ldg(a.sinks + h) * kLog2e - m);
     const float sc = denom > 0.f ? a.bmm2_scale / denom : 0.f;
-    uint4 w0, w1;
-    w0.x = float2_to_bf16x2(o[0] * sc, o[1] * sc);
-    w0.y = float2_to_bf16x2(o[2] * sc, o[3] * sc);
-    w0.z = float2_to_bf16x2(o[4] * sc, o[5] * sc);
-    w0.w = float2_to_bf16x2(o[6] * sc, o[7] * sc);
-    w1.x = float2_to_bf16x2(o[8] * sc, o[9] * sc);
-    w1.y = float2_to_bf16x2(o[10] * sc, o[11] * sc);
-    w1.z = float2_to_bf16x2(o[12] * sc, o[13] * sc);
-    w1.w = float2_to_bf16x2(o[14] * sc, o[15] * sc);
-    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
-                                          ((int64_t)t * a.num_qo_heads + h) * 128 + d0);
-    dst[0] = w0;
-    dst[1] = w1;
+    store_out<16>(a.out, ((int64_t)t * a.num_qo_heads + h) * 128 + d0, o, sc, a.out_dtype);
     if (a.lse != nullptr && d0 == 0)
       a.lse[(int64_t)t * a.num_qo_heads + h] = lsum > 0.f ? m + log2f(lsum) : neg_inf();
   } else {

@@ -140,5 +140,7 @@ extern "C" int paged_decode_run_noalloc(const pka_plan* p, const void* q, int64_
   a.rows_per_cta = p->rows_per_cta;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.bmm2_scale = p->desc.bmm2_scale;
+  a.in_f16 = p->desc.dtype == PKA_DTYPE_F16;
+  a.out_dtype = p->desc.out_dtype;
   return launch_decode(*p, a, kmap, vmap, s);
 }

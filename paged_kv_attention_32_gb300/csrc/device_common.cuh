@@ -6,7 +6,9 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
+#include "pka.h"
 #include "plan.h"
 
 namespace pka {
@@ -145,6 +147,70 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// ---- the two 16-bit input formats (F16 = false: bf16, true: IEEE half) ------
+template <bool F16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (F16) {
+    __half2 h;
+    memcpy(&h, &w, 4);
+    return __half22float2(h);
+  } else {
+    return bf16x2_to_float2(w);
+  }
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (F16) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    uint32_t w;
+    memcpy(&w, &h, 4);
+    return w;
+  } else {
+    return float2_to_bf16x2(lo, hi);
+  }
+}
+
+// ---- outputs: PKA_DTYPE_BF16, PKA_DTYPE_F16 or PKA_DTYPE_F32 ------------------
+// v[0..N) * sc to N consecutive elements at element offset `off` of `out`
+// (N = 4, 8 or 16; off a multiple of 4, so every store is 8- or 16-byte aligned).
+template <int N>
+__device__ __forceinline__ void store_out(void* out, int64_t off, const float* v, float sc,
+                                          int dtype) {
+  static_assert(N == 4 || N == 8 || N == 16, "4, 8 or 16 values");
+  if (dtype == PKA_DTYPE_F32) {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(out) + off);
+#pragma unroll
+    for (int x = 0; x < N / 4; ++x)
+      d[x] = make_float4(v[4 * x] * sc, v[4 * x + 1] * sc, v[4 * x + 2] * sc, v[4 * x + 3] * sc);
+    return;
+  }
+  uint32_t w[N / 2];
+#pragma unroll
+  for (int x = 0; x < N / 2; ++x)
+    w[x] = dtype == PKA_DTYPE_F16 ? pack2<true>(v[2 * x] * sc, v[2 * x + 1] * sc)
+                                  : pack2<false>(v[2 * x] * sc, v[2 * x + 1] * sc);
+  uint16_t* base = static_cast<uint16_t*>(out) + off;
+  if constexpr (N == 4) {
+    *reinterpret_cast<uint2*>(base) = make_uint2(w[0], w[1]);
+  } else {
+#pragma unroll
+    for (int x = 0; x < N / 8; ++x)
+      reinterpret_cast<uint4*>(base)[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+  }
+}
+
+// One value to element `off` of `out`.
+__device__ __forceinline__ void store_out1(void* out, int64_t off, float v, int dtype) {
+  if (dtype == PKA_DTYPE_F32) {
+    static_cast<float*>(out)[off] = v;
+  } else if (dtype == PKA_DTYPE_F16) {
+    static_cast<__half*>(out)[off] = __float2half_rn(v);
+  } else {
+    static_cast<__nv_bfloat16*>(out)[off] = __float2bfloat16_rn(v);
+  }
+}
+
 // ---- fast exp2 (hardware MUFU.EX2) -------------------------------------------
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -179,6 +245,24 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// As mma_bf16_16816 with IEEE half A and B.
+__device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <bool F16>
+__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  if constexpr (F16)
+    mma_f16_16816(d, a, b0, b1);
+  else
+    mma_bf16_16816(d, a, b0, b1);
 }
 
 }  // namespace dev

@@ -22,10 +22,10 @@ using namespace dev;
 
 namespace {
 
-template <bool OUT_BF16>
 __global__ void __launch_bounds__(256)
 merge_states_kernel(const float* __restrict__ v, const float* __restrict__ s, int n, int rows,
-                    int heads, int d, void* __restrict__ v_out, float* __restrict__ s_out) {
+                    int heads, int d, void* __restrict__ v_out, int out_dtype,
+                    float* __restrict__ s_out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t idx = (int64_t)blockIdx.x * 8 + warp;
   const int64_t per_state = (int64_t)rows * heads;
@@ -49,15 +49,8 @@ merge_states_kernel(const float* __restrict__ v, const float* __restrict__ s, in
         o.w += w * x.w;
       }
     }
-    if (OUT_BF16) {
-      uint2 p;
-      p.x = float2_to_bf16x2(o.x * inv, o.y * inv);
-      p.y = float2_to_bf16x2(o.z * inv, o.w * inv);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(v_out) + idx * d + c) = p;
-    } else {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(v_out) + idx * d + c) =
-          make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-    }
+    const float ov[4] = {o.x, o.y, o.z, o.w};
+    store_out<4>(v_out, idx * d + c, ov, inv, out_dtype);
   }
   if (s_out != nullptr && lane == 0) s_out[idx] = wsum > 0.f ? m + log2f(wsum) : neg_inf();
 }
@@ -113,12 +106,8 @@ int launch_merge_states(const float* v_states, const float* s_states, int32_t n,
   const int64_t rows = (int64_t)s * h;
   if (rows == 0) return PKA_OK;
   const int64_t blocks = (rows + 7) / 8;
-  if (out_dtype == PKA_DTYPE_BF16)
-    merge_states_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(v_states, s_states, n, s, h, d,
-                                                                   v_out, s_out);
-  else
-    merge_states_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(v_states, s_states, n, s, h,
-                                                                    d, v_out, s_out);
+  merge_states_kernel<<<(unsigned)blocks, 256, 0, stream>>>(v_states, s_states, n, s, h, d, v_out,
+                                                           out_dtype, s_out);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "merge_states_kernel launch");
   return PKA_OK;

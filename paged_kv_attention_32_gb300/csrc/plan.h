@@ -63,6 +63,8 @@ struct DecodeArgs {
   int32_t rows_per_cta;          // group * max_q_len
   float scale_log2;              // scale * log2(e), folded into q
   float bmm2_scale;
+  int32_t in_f16;                // q/K/V are IEEE half (else bf16)
+  int32_t out_dtype;             // PKA_DTYPE_BF16 / F16 / F32
 };
 
 // Device error word bits (OR-ed by kernels, read by paged_decode_status).

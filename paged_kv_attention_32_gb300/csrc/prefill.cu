@@ -53,8 +53,9 @@ enum {
   B_ODONE = 13, B_MMADONE = 15, B_COUNT = 16
 };
 
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);   // A, B K-major
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);   // A K-major, B (V) MN-major
+// A, B K-major (QK) / A K-major, B = V MN-major (PV); operands bf16 or f16
+template <bool F16> constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0, F16);
+template <bool F16> constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1, F16);
 
 // K-major operand of 128 rows x 128 columns stored as two 16 KB boxes of
 // 64 columns: descriptor for k-step kk (16 columns).
@@ -72,6 +73,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
 }
 
+// F16: q/K/V (and P) are IEEE half, else bf16.
+template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
                const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -160,7 +163,7 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
         const uint32_t kb = sbase + kOffK + (uint32_t)st * 2u * kBox;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_bf16(d, kmajor_desc(qb, kk), kmajor_desc(kb, kk), kIdescQK, kk > 0 ? 1u : 0u);
+          umma_bf16(d, kmajor_desc(qb, kk), kmajor_desc(kb, kk), kIdescQK<F16>, kk > 0 ? 1u : 0u);
       };
       bool ok = mbar_wait(bar(B_Q), 0, a.status) && mbar_wait(bar(B_KFULL), 0, a.status);
       if (ok) {
@@ -183,7 +186,7 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
           const uint32_t vb = sbase + kOffV + (uint32_t)vst * 2u * kBox;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_ts(d, p_tm + (uint32_t)kk * 8u, vmn_desc(vb, kk), kIdescPV,
+            umma_bf16_ts(d, p_tm + (uint32_t)kk * 8u, vmn_desc(vb, kk), kIdescPV<F16>,
                          (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(B_ODONE + hh));
           if (hh == nh - 1) umma_commit(bar(B_VEMPTY + vst));
@@ -287,7 +290,7 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
           }
           sum0 += p0;
           sum1 += p1;
-          pk[i] = float2_to_bf16x2(p0, p1);
+          pk[i] = pack2<F16>(p0, p1);
         }
         tmem_st16(s_tm + (uint32_t)c * 16u, pk);
       };
@@ -319,25 +322,18 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
       tc_fence_after();
       const int h = h0 + hh;
       const float inv = l > 0.f ? a.output_scale / l : 0.f;
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.out) +
-                           ((int64_t)(q0 + t) * a.num_qo_heads + h) * 128;
+      const int64_t dst = ((int64_t)(q0 + t) * a.num_qo_heads + h) * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tmem_ld32_sync(o_tm + (uint32_t)c * 32u, r);
         if (row_valid) {
 #pragma unroll
-          for (int qd = 0; qd < 4; ++qd) {
-            uint4 w;
-            w.x = float2_to_bf16x2(__uint_as_float(r[8 * qd + 0]) * inv,
-                                   __uint_as_float(r[8 * qd + 1]) * inv);
-            w.y = float2_to_bf16x2(__uint_as_float(r[8 * qd + 2]) * inv,
-                                   __uint_as_float(r[8 * qd + 3]) * inv);
-            w.z = float2_to_bf16x2(__uint_as_float(r[8 * qd + 4]) * inv,
-                                   __uint_as_float(r[8 * qd + 5]) * inv);
-            w.w = float2_to_bf16x2(__uint_as_float(r[8 * qd + 6]) * inv,
-                                   __uint_as_float(r[8 * qd + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + c * 32 + qd * 8) = w;
+          for (int qd = 0; qd < 2; ++qd) {
+            float f[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) f[x] = __uint_as_float(r[16 * qd + x]);
+            store_out<16>(a.out, dst + c * 32 + qd * 16, f, inv, a.out_dtype);
           }
         }
       }
@@ -358,12 +354,12 @@ prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CU
 
 int launch_prefill(const pka_prefill_plan& plan, const PrefillArgs& args, const CUtensorMap& qmap,
                    const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream) {
-  (void)plan;
   if (args.num_tiles == 0) return PKA_OK;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = plan.desc.dtype == PKA_DTYPE_F16 ? prefill_kernel<true> : prefill_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
-  prefill_kernel<<<args.num_tiles, kThreads, kSmemBytes, stream>>>(args, qmap, kmap, vmap);
+  kern<<<args.num_tiles, kThreads, kSmemBytes, stream>>>(args, qmap, kmap, vmap);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill_kernel launch");
   return PKA_OK;

@@ -42,6 +42,7 @@ struct PrefillArgs {
   int32_t heads_per_cta;
   float scale_log2;
   float output_scale;
+  int32_t out_dtype;       // PKA_DTYPE_BF16 / F16 / F32
 };
 
 }  // namespace pka

@@ -26,8 +26,11 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
   PKA_CHECK_ARG(d.num_qo_heads % d.num_kv_heads == 0,
                 "num_qo_heads (%d) must be a multiple of num_kv_heads (%d)", d.num_qo_heads,
                 d.num_kv_heads);
-  if (d.dtype != PKA_DTYPE_BF16)
-    return fail(PKA_ERR_UNSUPPORTED, "only bf16 q/K/V are supported (dtype %d)", d.dtype);
+  if (d.dtype != PKA_DTYPE_BF16 && d.dtype != PKA_DTYPE_F16)
+    return fail(PKA_ERR_UNSUPPORTED, "q/K/V must be bf16 or f16 (dtype %d)", d.dtype);
+  PKA_CHECK_ARG(d.out_dtype == PKA_DTYPE_BF16 || d.out_dtype == PKA_DTYPE_F16 ||
+                    d.out_dtype == PKA_DTYPE_F32,
+                "out_dtype must be bf16, f16 or f32 (got %d)", d.out_dtype);
   if (d.head_dim != 128)
     return fail(PKA_ERR_UNSUPPORTED, "prefill head_dim must be 128 (got %d; 256 not built)",
                 d.head_dim);

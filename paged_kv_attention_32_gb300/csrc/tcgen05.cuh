@@ -52,13 +52,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16)
-//   bit 15 A major (0 = K), bit 16 B major (0 = K, 1 = MN)
+// Instruction descriptor, kind::f16: bf16 (or, with f16 = true, IEEE half) A
+// and B -- both the same type -- and an fp32 accumulator.
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
+//   1 = bf16), bit 15 A major (0 = K), bit 16 B major (0 = K, 1 = MN),
 //   bits 17-22 N >> 3, bits 24-28 M >> 4
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, int a_mn_major,
-                                                      int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) |
+                                                      int b_mn_major, bool f16 = false) {
+  return (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) | ((uint32_t)a_mn_major << 15) |
          ((uint32_t)b_mn_major << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 

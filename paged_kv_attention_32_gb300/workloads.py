@@ -103,7 +103,7 @@ def _randint(gen, lo, hi, n):
     return torch.randint(lo, hi + 1, (n,), generator=gen, dtype=torch.int64)
 
 
-def make_decode_inputs(w: DecodeWorkload, seed: int = 0, device="cpu"):
+def make_decode_inputs(w: DecodeWorkload, seed: int = 0, device="cpu", dtype=torch.bfloat16):
     """Draw one batch of decode inputs for workload ``w``.
 
     Returns a dict of tensors (q, k_pages, v_pages, block_tables, seq_lens_kv,
@@ -146,10 +146,10 @@ def make_decode_inputs(w: DecodeWorkload, seed: int = 0, device="cpu"):
     gd = torch.Generator(device=device)
     gd.manual_seed(seed + 1)
     shape_pool = (pool, w.num_kv_heads, ps, w.head_dim)
-    k_pages = torch.randn(shape_pool, generator=gd, device=device, dtype=torch.bfloat16)
-    v_pages = torch.randn(shape_pool, generator=gd, device=device, dtype=torch.bfloat16)
+    k_pages = torch.randn(shape_pool, generator=gd, device=device, dtype=dtype)
+    v_pages = torch.randn(shape_pool, generator=gd, device=device, dtype=dtype)
     q = torch.randn((total_q, w.num_qo_heads, w.head_dim), generator=gd, device=device,
-                    dtype=torch.bfloat16)
+                    dtype=dtype)
     sinks = (torch.randn((w.num_qo_heads,), generator=gd, device=device, dtype=torch.float32)
              if w.sinks else None)
     return {
@@ -198,5 +198,5 @@ def make_prefill_inputs(w: PrefillWorkload, seed: int = 0, device="cpu"):
 
 
 def bf16_bits(t: torch.Tensor):
-    """The uint16 bit patterns of a bf16 tensor, as a numpy array (host copy)."""
+    """The uint16 bit patterns of a 16-bit (bf16 or f16) tensor, as a numpy array (host copy)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")

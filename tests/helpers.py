@@ -14,6 +14,7 @@ O_ATOL, O_RTOL, LSE_ATOL = 2e-2, 2e-2, 1e-3
 
 def decode_plan_for(inp, **kw):
     w_tables = inp["block_tables"]
+    kw.setdefault("dtype", inp["q"].dtype)
     seq = inp["seq_lens_kv"].cpu()
     args = dict(num_qo_heads=inp["q"].shape[1], num_kv_heads=inp["num_kv_heads"],
                 page_size=inp["page_size"], max_pages_per_seq=w_tables.shape[1],
@@ -39,6 +40,7 @@ def run_decode(inp, plan=None, **kw):
 
 
 def oracle_decode(inp, requests=None, window_left=None):
+    dtype = "f16" if inp["q"].dtype == torch.float16 else "bf16"
     q_len = inp["q_len"] if inp["q_len"] is not None else 1
     indptr = inp["qo_indptr"].cpu().numpy() if inp["qo_indptr"] is not None else None
     bt = inp["block_tables"].cpu().numpy()
@@ -64,7 +66,7 @@ def oracle_decode(inp, requests=None, window_left=None):
         wl.bf16_bits(inp["q"]), kbits, vbits, bt, inp["seq_lens_kv"].cpu().numpy(),
         inp["num_kv_heads"], inp["page_size"], qo_indptr=indptr, q_len=q_len,
         causal=inp["causal"], window_left=inp["window_left"] if window_left is None else window_left,
-        scale=None, bmm2_scale=inp["bmm2_scale"], sinks=sinks, requests=requests)
+        scale=None, bmm2_scale=inp["bmm2_scale"], sinks=sinks, requests=requests, dtype=dtype)
 
 
 def row_mask(inp, requests):

@@ -96,6 +96,24 @@ def test_decode_wide_groups(G, L, packed, split):
     assert_close(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("in_dtype,out_dtype", [
+    (torch.float16, None), (torch.float16, torch.float32), (torch.bfloat16, torch.float32),
+    (torch.bfloat16, torch.float16)])
+@pytest.mark.parametrize("name,mma", [("llama3_8b", 0), ("spec", 0), ("skewed", 16)])
+def test_decode_input_and_output_dtypes(in_dtype, out_dtype, name, mma):
+    """fp16 q/K/V (cudnn_batch_decode_with_kv_cache takes float16 or bfloat16) and
+    out_dtype bf16 / f16 / fp32 (batch_decode_with_paged_kv_cache, out_dtype), on the
+    CUDA-core kernel (4 and 8 rows), the mma kernel and the split + merge path."""
+    inp = wl.make_decode_inputs(SMALL[name], seed=14, device=DEV, dtype=in_dtype)
+    kw = dict(out_dtype=out_dtype, num_sms=32, split_waves=2, min_chunk_tokens=128)
+    if mma:
+        kw["mma_min_rows"] = mma
+    out, lse, plan = run_decode(inp, **kw)
+    assert out.dtype == (in_dtype if out_dtype is None else out_dtype)
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
 def test_decode_page_size_64_and_bmm2_scale():
     w = wl.DecodeWorkload(name="ps64", batch=4, num_qo_heads=8, num_kv_heads=2, head_dim=128,
                           page_size=64, kv_len_range=(1, 900), bmm2_scale=0.5)

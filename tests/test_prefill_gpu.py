@@ -13,9 +13,9 @@ from helpers import LSE_ATOL, O_ATOL, O_RTOL
 pytestmark = pytest.mark.gpu
 
 
-def _rand(shape, seed):
+def _rand(shape, seed, dtype=torch.bfloat16):
     g = torch.Generator(device="cuda").manual_seed(seed)
-    return torch.randn(shape, generator=g, device="cuda", dtype=torch.bfloat16)
+    return torch.randn(shape, generator=g, device="cuda", dtype=dtype)
 
 
 def _indptr(lens):
@@ -31,17 +31,20 @@ def _check(out, lse, ref_o, ref_l):
         assert (np.abs(l - ref_l) <= LSE_ATOL).all(), f"LSE err {np.abs(l - ref_l).max():.4g}"
 
 
-def _run(lq, lk, Hq, Hkv, causal=True, seed=0, **kw):
+def _run(lq, lk, Hq, Hkv, causal=True, seed=0, dtype=torch.bfloat16, out_dtype=None, **kw):
     qi, ki = _indptr(lq), _indptr(lk)
-    q = _rand((int(qi[-1]), Hq, 128), seed + 1)
-    k, v = _rand((int(ki[-1]), Hkv, 128), seed + 2), _rand((int(ki[-1]), Hkv, 128), seed + 3)
+    q = _rand((int(qi[-1]), Hq, 128), seed + 1, dtype)
+    k = _rand((int(ki[-1]), Hkv, 128), seed + 2, dtype)
+    v = _rand((int(ki[-1]), Hkv, 128), seed + 3, dtype)
     plan = api.batch_prefill_plan(qi, ki, num_qo_heads=Hq, num_kv_heads=Hkv, causal=causal,
-                                  return_lse=True, **kw)
+                                  return_lse=True, dtype=dtype, out_dtype=out_dtype, **kw)
     out, lse = api.batch_prefill_run(plan, q, k, v)
     torch.cuda.synchronize()
     plan.check()
+    assert out.dtype == (dtype if out_dtype is None else out_dtype)
     ref_o, ref_l = oracle.batch_prefill(wl.bf16_bits(q), wl.bf16_bits(k), wl.bf16_bits(v),
-                                        qi.numpy(), ki.numpy(), Hkv, causal=causal, **kw)
+                                        qi.numpy(), ki.numpy(), Hkv, causal=causal,
+                                        dtype="f16" if dtype == torch.float16 else "bf16", **kw)
     _check(out, lse, ref_o, ref_l)
 
 
@@ -112,6 +115,15 @@ def test_prefill_variable_window(Hq, Hkv, seed):
     en[:, ::7] = st[:, ::7]                      # single-key rows
     _fixed_case(B, Sq, Sk, Hq, Hkv, seed=seed, mask_type="variable_window",
                 variable_window_token_starts=st, variable_window_token_ends=en)
+
+
+@pytest.mark.parametrize("dtype,out_dtype", [(torch.float16, None), (torch.float16, torch.float32),
+                                             (torch.bfloat16, torch.float32),
+                                             (torch.bfloat16, torch.float16)])
+def test_prefill_input_and_output_dtypes(dtype, out_dtype):
+    """fp16 q/k/v (kind::f16 MMAs on half operands) and out_dtype (batch_prefill)."""
+    lens = [1, 127, 300, 513]
+    _run(lens, lens, 8, 2, seed=70, dtype=dtype, out_dtype=out_dtype, window_left=200)
 
 
 def test_prefill_full_size_sampled():
