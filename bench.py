@@ -353,24 +353,26 @@ def headline_traffic(head):
     return int(round(NCU_TRAFFIC["dram_bytes"] * head["kv_bytes"] / NCU_TRAFFIC["kv_bytes"]))
 
 
-def measure_workload(name, seed, steps, warmup, peak_gbs, dist=None):
+def measure_workload(name, seed, steps, warmup, peak_gbs, dist=None, dtype=None):
     """Inputs drawn on the GPU, plan, device timing; returns (result dict, inp, plan)."""
+    import torch
     from paged_kv_attention_32_gb300 import workloads as wl
     w = wl.DECODE_WORKLOADS[name]
-    inp = wl.make_decode_inputs(w, seed=seed, device="cuda")
-    plan = make_plan(inp)
+    inp = wl.make_decode_inputs(w, seed=seed, device="cuda", dtype=dtype or torch.bfloat16)
+    plan = make_plan(inp, dtype=inp["q"].dtype)
     ms = time_decode(inp, plan, steps, warmup, dist)
     nbytes, keys = kv_bytes(inp)
     info = plan.info
     gbs = nbytes / (ms * 1e-3) / 1e9
-    res = {"workload": w.name, "ms_per_call": round(ms, 5), "kv_bytes": nbytes,
+    res = {"workload": w.name + (f" {inp['q'].dtype}" if dtype is not None else ""),
+           "ms_per_call": round(ms, 5), "kv_bytes": nbytes,
            "kv_tokens": keys, "GB_per_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak_gbs, 4),
            "kernel": ["cuda_core", "mma"][info["kernel"]], "ctas": info["num_items"],
            "split_requests": info["num_split"], "launches_per_call": 1 + (info["num_split"] > 0)}
     return res, inp, plan
 
 
-def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1):
+def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1, dtype=None):
     """Ragged causal prefill; FLOPs = 4 * D per unmasked (query, key) pair per query head
     (with a window, row i of a request keeps min(i + 1, window_left + 1) keys)."""
     import torch
@@ -378,6 +380,9 @@ def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1):
     from paged_kv_attention_32_gb300 import workloads as wl
     w = wl.RAGGED_PREFILL
     inp = wl.make_prefill_inputs(w, seed=seed, device="cuda")
+    if dtype is not None:   # the same values drawn in bf16, held as fp16
+        for key in ("q", "k", "v"):
+            inp[key] = inp[key].to(dtype)
     lens = inp["lens"].tolist()
     if window_left >= 0:
         W1 = window_left + 1
@@ -385,11 +390,12 @@ def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1):
     else:
         pairs = sum(n * (n + 1) // 2 for n in lens)
     flops = 4 * 128 * pairs * w.num_qo_heads
-    name = w.name + (f" window_left={window_left}" if window_left >= 0 else "")
+    name = w.name + (f" window_left={window_left}" if window_left >= 0 else "") + (
+        f" {dtype}" if dtype is not None else "")
     try:
         plan = api.batch_prefill_plan(inp["qo_indptr"].cpu(), inp["kv_indptr"].cpu(),
                                       num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
-                                      window_left=window_left)
+                                      window_left=window_left, dtype=inp["q"].dtype)
         out = torch.empty_like(inp["q"])
         for _ in range(warmup):
             api.batch_prefill_run(plan, inp["q"], inp["k"], inp["v"], out=out)
@@ -642,6 +648,13 @@ def main():
                                                   window_left=PREFILL_WINDOW)
         extra["prefill_fixed"] = measure_prefill_fixed(args.seed, max(3, args.steps // 4), 3,
                                                        peak_tf)
+        r16, i16, p16 = measure_workload(HEADLINE, args.seed, max(5, args.steps // 2),
+                                         max(3, args.warmup), peak_gbs, dtype=torch.float16)
+        extra["llama3_8b_f16"] = r16
+        del i16, p16
+        torch.cuda.empty_cache()
+        extra["prefill_f16"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf,
+                                               dtype=torch.float16)
         extra["prefill_variable_window"] = measure_prefill_fixed(
             args.seed, max(3, args.steps // 4), 3, peak_tf, variable_window=True)
         line["decode_headline"] = head
