@@ -372,13 +372,16 @@ def measure_workload(name, seed, steps, warmup, peak_gbs, dist=None, dtype=None)
     return res, inp, plan
 
 
-def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1, dtype=None):
+def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1, dtype=None, head_dim=128):
     """Ragged causal prefill; FLOPs = 4 * D per unmasked (query, key) pair per query head
     (with a window, row i of a request keeps min(i + 1, window_left + 1) keys)."""
     import torch
     from paged_kv_attention_32_gb300 import api
     from paged_kv_attention_32_gb300 import workloads as wl
+    import dataclasses
     w = wl.RAGGED_PREFILL
+    if head_dim != w.head_dim:
+        w = dataclasses.replace(w, head_dim=head_dim, name=w.name.replace("D=128", f"D={head_dim}"))
     inp = wl.make_prefill_inputs(w, seed=seed, device="cuda")
     if dtype is not None:   # the same values drawn in bf16, held as fp16
         for key in ("q", "k", "v"):
@@ -389,13 +392,14 @@ def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1, dtype=None
         pairs = sum(min(n, W1) * (min(n, W1) + 1) // 2 + max(0, n - W1) * W1 for n in lens)
     else:
         pairs = sum(n * (n + 1) // 2 for n in lens)
-    flops = 4 * 128 * pairs * w.num_qo_heads
+    flops = 4 * head_dim * pairs * w.num_qo_heads
     name = w.name + (f" window_left={window_left}" if window_left >= 0 else "") + (
         f" {dtype}" if dtype is not None else "")
     try:
         plan = api.batch_prefill_plan(inp["qo_indptr"].cpu(), inp["kv_indptr"].cpu(),
                                       num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
-                                      window_left=window_left, dtype=inp["q"].dtype)
+                                      window_left=window_left, dtype=inp["q"].dtype,
+                                      head_dim=head_dim)
         out = torch.empty_like(inp["q"])
         for _ in range(warmup):
             api.batch_prefill_run(plan, inp["q"], inp["k"], inp["v"], out=out)
@@ -655,6 +659,8 @@ def main():
         torch.cuda.empty_cache()
         extra["prefill_f16"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf,
                                                dtype=torch.float16)
+        extra["prefill_d256"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf,
+                                                head_dim=256)
         extra["prefill_variable_window"] = measure_prefill_fixed(
             args.seed, max(3, args.steps // 4), 3, peak_tf, variable_window=True)
         line["decode_headline"] = head

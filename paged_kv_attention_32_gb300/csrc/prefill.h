@@ -17,7 +17,7 @@ struct PrefillTile {
   int32_t request;
   int32_t head;     // first query head of the tile
   int32_t q_tile;   // 128-row tile index inside the request
-  int32_t n_kv;     // KV tiles (128 keys) the tile visits
+  int32_t n_kv;     // KV tiles (128 keys; 64 with head_dim 256) the tile visits
   int32_t kv0;      // first of them (past 0 only with a window)
 };
 
@@ -74,8 +74,13 @@ int build_prefill_plan(pka_prefill_plan& plan, const pka_prefill_desc& desc, con
                        const int32_t* kv, const int32_t* win_lo = nullptr,
                        const int32_t* win_hi = nullptr);
 
-// Launches the prefill kernel over the plan's tiles.
+// Launches the prefill kernel over the plan's tiles (head_dim 128).
 int launch_prefill(const pka_prefill_plan& plan, const PrefillArgs& args, const CUtensorMap& qmap,
                    const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream);
+
+// Same for head_dim 256 (64-key tiles, one head per CTA).
+int launch_prefill_d256(const pka_prefill_plan& plan, const PrefillArgs& args,
+                        const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                        cudaStream_t stream);
 
 }  // namespace pka

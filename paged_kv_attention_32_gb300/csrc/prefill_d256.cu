@@ -1,0 +1,326 @@
+// Prefill with head_dim 256 on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// batch_prefill allows D = 128 or 256.  Same masks and outputs as the D = 128
+// kernel (bottom-right causal diagonal, dense, left window, variable_window;
+// O scaled by output_scale, base-2 LSE), with a tile shape that fits D = 256:
+// one CTA = one 128-row query tile of one request and one query head, keys in
+// tiles of 64 (Q 64 KB + two K and two V stages of 32 KB in shared memory).
+//   warp 4      TMA producer: Q once (four 64-column boxes), then K and V
+//               tiles (four 64-column boxes each, 128-byte swizzle);
+//   warp 5      allocates TMEM and issues every tcgen05.mma from one thread:
+//               S_b = Q K^T (M=128, N=64, 16 k-steps) into one of two S
+//               buffers -- two key tiles ahead of the softmax, so the tensor
+//               core works while the softmax runs -- and O += P V (M=128,
+//               N=256, 4 k-steps of 16 keys, P read from TMEM, V MN-major);
+//   warps 0-3   softmax, one thread per query row (TMEM lane): row max of the
+//               64 scores, lazy rescaling of O only when the max grew by more
+//               than 2^8, p = exp2(s * scale*log2e - m), bf16/f16 P over the
+//               first 32 columns of the S buffer, final O / l and LSE.
+// TMEM columns: S0 [0,64) S1 [64,128) O [128,384) (512 allocated).
+#include <cuda_bf16.h>
+
+#include "device_common.cuh"
+#include "host_common.h"
+#include "prefill.h"
+#include "tcgen05.cuh"
+
+namespace pka {
+
+using namespace dev;
+
+namespace {
+
+constexpr int kTileQ = 128, kTileK = 64;
+constexpr uint32_t kQBox = 16384;           // 128 rows x 128 bytes (64 columns)
+constexpr uint32_t kKBox = 8192;            // 64 rows x 128 bytes
+constexpr uint32_t kOffQ = 0;               // 4 column blocks x 16 KB
+constexpr uint32_t kOffK = 65536;           // 2 stages x 4 blocks x 8 KB
+constexpr uint32_t kOffV = 131072;          // 2 stages x 4 blocks x 8 KB
+constexpr uint32_t kOffBar = 196608;
+constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr uint32_t kColO = 128, kTmemCols = 512;
+
+enum {
+  B_Q = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 7, B_SFULL = 9, B_PFULL = 11,
+  B_ODONE = 13, B_MMADONE = 15, B_COUNT = 16
+};
+
+template <bool F16> constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, 0, 0, F16);
+template <bool F16> constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1, F16);
+
+// Q (128 rows) or K (64 rows) as the K-major operand: column block kk / 4,
+// 32-byte step kk % 4 inside the 128-byte rows, 8-row groups every 1024 bytes.
+__device__ __forceinline__ uint64_t kmajor(uint32_t base, uint32_t block_bytes, int kk) {
+  return smem_desc_sw128(base + (uint32_t)(kk >> 2) * block_bytes + (uint32_t)(kk & 3) * 32u, 16u,
+                         1024u);
+}
+// V tile (64 keys x 256 dims) as the MN-major B operand of k-step kk (keys
+// 16kk .. 16kk+15): 64-dim blocks every 8 KB, 8-key groups every 1024 bytes.
+__device__ __forceinline__ uint64_t vmn(uint32_t base, int kk) {
+  return smem_desc_sw128(base + (uint32_t)kk * 2048u, kKBox, 1024u);
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_d256_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
+                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + B_COUNT * 8);
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (uint32_t)i; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const PrefillTile tile = a.tiles[blockIdx.x];
+  const int b = tile.request, h = tile.head, mt = tile.q_tile, n_kv = tile.n_kv;
+  const int kv0 = tile.kv0;
+  const int q0 = a.qo_indptr[b], Lq = a.qo_indptr[b + 1] - q0;
+  const int k0 = a.kv_indptr[b], Lk = a.kv_indptr[b + 1] - k0;
+  const int hk = h / a.group;
+
+  if (tid == 0) {
+    mbar_init(bar(B_Q), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+      mbar_init(bar(B_VFULL + s), 1);
+      mbar_init(bar(B_VEMPTY + s), 1);
+      mbar_init(bar(B_SFULL + s), 1);
+      mbar_init(bar(B_PFULL + s), 128);
+      mbar_init(bar(B_ODONE + s), 1);
+    }
+    mbar_init(bar(B_MMADONE), 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      mbar_arrive_expect_tx(bar(B_Q), 4u * kQBox);
+      for (int blk = 0; blk < 4; ++blk)
+        tma_load_3d(sbase + kOffQ + (uint32_t)blk * kQBox, &tmq, bar(B_Q), blk * 64, h,
+                    q0 + mt * kTileQ);
+      auto load_kv = [&](int j, int which) -> bool {   // which: 0 = K, 1 = V
+        const int st = j & 1;
+        const int full = which ? B_VFULL : B_KFULL, empty = which ? B_VEMPTY : B_KEMPTY;
+        if (j >= 2 && !mbar_wait(bar(empty + st), (uint32_t)(((j >> 1) - 1) & 1), a.status))
+          return false;
+        const uint32_t dst = sbase + (which ? kOffV : kOffK) + (uint32_t)st * 4u * kKBox;
+        mbar_arrive_expect_tx(bar(full + st), 4u * kKBox);
+        for (int blk = 0; blk < 4; ++blk)
+          tma_load_3d(dst + (uint32_t)blk * kKBox, which ? &tmv : &tmk, bar(full + st), blk * 64,
+                      hk, k0 + (kv0 + j) * kTileK);
+        return true;
+      };
+      bool ok = true;
+      int kd = 0, vd = 0;   // K and V tiles issued
+      // order K0 K1 V0 K2 V1 K3 ...: S of tile j + 2 is issued after P V of tile j
+      while (ok && (kd < n_kv || vd < n_kv)) {
+        if (kd < n_kv && kd <= vd + 1) {
+          ok = load_kv(kd, 0);
+          kd += ok;
+        } else {
+          ok = load_kv(vd, 1);
+          vd += ok;
+        }
+      }
+      if (!ok) {   // give the copies already issued a bounded chance to land
+        mbar_wait(bar(B_Q), 0, nullptr);
+        if (kd > 0) mbar_wait(bar(B_KFULL + ((kd - 1) & 1)), (uint32_t)(((kd - 1) >> 1) & 1), nullptr);
+        if (vd > 0) mbar_wait(bar(B_VFULL + ((vd - 1) & 1)), (uint32_t)(((vd - 1) >> 1) & 1), nullptr);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer (one thread) ----------------
+    if (lane == 0) {
+      auto issue_qk = [&](int j) -> bool {   // S of tile j into buffer j & 1
+        const int st = j & 1;
+        if (!mbar_wait(bar(B_KFULL + st), (uint32_t)((j >> 1) & 1), a.status)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)st * 64u;
+        const uint32_t kb = sbase + kOffK + (uint32_t)st * 4u * kKBox;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk)
+          umma_bf16(d, kmajor(sbase + kOffQ, kQBox, kk), kmajor(kb, kKBox, kk), kIdescQK<F16>,
+                    kk > 0 ? 1u : 0u);
+        umma_commit(bar(B_SFULL + st));
+        umma_commit(bar(B_KEMPTY + st));
+        return true;
+      };
+      bool ok = mbar_wait(bar(B_Q), 0, a.status);
+      for (int j = 0; ok && j < n_kv && j < 2; ++j) ok = issue_qk(j);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j & 1;
+        ok = mbar_wait(bar(B_VFULL + st), (uint32_t)((j >> 1) & 1), a.status) &&
+             mbar_wait(bar(B_PFULL + st), (uint32_t)((j >> 1) & 1), a.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t p_tm = tmem + (uint32_t)st * 64u;   // P: 32 columns, lanes 0-127
+        const uint32_t vb = sbase + kOffV + (uint32_t)st * 4u * kKBox;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16_ts(tmem + kColO, p_tm + (uint32_t)kk * 8u, vmn(vb, kk), kIdescPV<F16>,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_ODONE + st));
+        umma_commit(bar(B_VEMPTY + st));
+        // S buffer st is free again once this P V has read P (issue order)
+        if (j + 2 < n_kv) ok = issue_qk(j + 2);
+      }
+      umma_commit(bar(B_MMADONE));
+      mbar_wait(bar(B_MMADONE), 0, a.status);   // nothing of ours still runs on the tensor core
+    }
+  } else {
+    // ---------------- softmax: one thread per query row ----------------
+    const int row = tid;                       // warps 0-3
+    const int t = mt * kTileQ + row;
+    const bool row_valid = t < Lq;
+    int hi = a.causal ? min(Lk, Lk - Lq + t + 1) : Lk;   // keys [lo, hi) visible
+    int lo = a.window_left >= 0 ? min(hi, max(0, Lk - Lq + t - a.window_left)) : 0;
+    if (a.window_lo != nullptr) {   // variable_window: the row's inclusive bounds
+      lo = row_valid ? __ldg(a.window_lo + q0 + t) : 0;
+      hi = row_valid ? __ldg(a.window_hi + q0 + t) + 1 : 0;
+    }
+    const unsigned span = (unsigned)(hi - lo);   // key visible <=> (unsigned)(key - lo) < span
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t o_tm = tmem + lane_off + kColO;
+    const float sl2 = a.scale_log2;   // >= 0 (checked by the planner)
+    float m_ref = neg_inf(), l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      if (!(ok = warp_wait(bar(B_SFULL + st), (uint32_t)((j >> 1) & 1), a.status))) break;
+      tc_fence_after();
+      const uint32_t s_tm = tmem + lane_off + (uint32_t)st * 64u;
+      const int key0 = (kv0 + j) * kTileK;
+      const bool masked = key0 < lo || key0 + kTileK > hi;
+      uint32_t ra[32], rb[32];
+      tmem_ld32(s_tm, ra);
+      tmem_ld32(s_tm + 32u, rb);
+      tmem_wait_ld();
+      reg_fence32(ra);
+      reg_fence32(rb);
+      if (masked) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if ((unsigned)(key0 + i - lo) >= span) ra[i] = __float_as_uint(neg_inf());
+          if ((unsigned)(key0 + 32 + i - lo) >= span) rb[i] = __float_as_uint(neg_inf());
+        }
+      }
+      float mraw = neg_inf();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mraw = fmax3(mraw, __uint_as_float(ra[i]), __uint_as_float(rb[i]));
+      // lazy rescale: move the reference max only when it grew by more than 2^8
+      const float mx = mraw == neg_inf() ? neg_inf() : mraw * sl2;
+      const bool grow = mx > m_ref + kRescaleThreshold;
+      const float m_new = grow ? mx : m_ref;
+      const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // O holds tiles before j: wait for P V of tile j - 1 before rescaling
+        if (!(ok = warp_wait(bar(B_ODONE + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1),
+                             a.status)))
+          break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32_sync(o_tm + (uint32_t)c * 32u, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(o_tm + (uint32_t)c * 32u, r);
+        }
+        tmem_wait_st();
+      }
+      m_ref = m_new;
+      const float neg_m = -m_ref;
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t* r = half ? rb : ra;
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), sl2, neg_m));
+          float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), sl2, neg_m));
+          if (masked) {
+            if ((unsigned)(key0 + 32 * half + 2 * i - lo) >= span) p0 = 0.f;
+            if ((unsigned)(key0 + 32 * half + 2 * i + 1 - lo) >= span) p1 = 0.f;
+          }
+          sum0 += p0;
+          sum1 += p1;
+          pk[i] = pack2<F16>(p0, p1);
+        }
+        tmem_st16(s_tm + 16u * (uint32_t)half, pk);   // P over S columns already read
+      }
+      tmem_wait_st();
+      l = l * alpha + (sum0 + sum1);
+      tc_fence_before();
+      mbar_arrive(bar(B_PFULL + st));
+    }
+    if (ok && n_kv > 0 &&
+        warp_wait(bar(B_ODONE + ((n_kv - 1) & 1)), (uint32_t)(((n_kv - 1) >> 1) & 1), a.status)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? a.output_scale / l : 0.f;
+      const int64_t dst = ((int64_t)(q0 + t) * a.num_qo_heads + h) * 256;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t r[32];
+        tmem_ld32_sync(o_tm + (uint32_t)c * 32u, r);
+        if (row_valid) {
+#pragma unroll
+          for (int qd = 0; qd < 2; ++qd) {
+            float f[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) f[x] = __uint_as_float(r[16 * qd + x]);
+            store_out<16>(a.out, dst + c * 32 + qd * 16, f, inv, a.out_dtype);
+          }
+        }
+      }
+      if (row_valid && a.lse != nullptr)
+        a.lse[(int64_t)(q0 + t) * a.num_qo_heads + h] = l > 0.f ? m_ref + log2f(l) : neg_inf();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int launch_prefill_d256(const pka_prefill_plan& plan, const PrefillArgs& args,
+                        const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                        cudaStream_t stream) {
+  if (args.num_tiles == 0) return PKA_OK;
+  auto kern = plan.desc.dtype == PKA_DTYPE_F16 ? prefill_d256_kernel<true>
+                                               : prefill_d256_kernel<false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_d256)");
+  kern<<<args.num_tiles, kThreads, kSmemBytes, stream>>>(args, qmap, kmap, vmap);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "prefill_d256_kernel launch");
+  return PKA_OK;
+}
+
+}  // namespace pka

@@ -14,7 +14,6 @@ namespace pka {
 
 namespace {
 constexpr int kTileQ = 128;
-constexpr int kTileK = 128;
 }  // namespace
 
 int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const int32_t* qo,
@@ -31,9 +30,8 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
   PKA_CHECK_ARG(d.out_dtype == PKA_DTYPE_BF16 || d.out_dtype == PKA_DTYPE_F16 ||
                     d.out_dtype == PKA_DTYPE_F32,
                 "out_dtype must be bf16, f16 or f32 (got %d)", d.out_dtype);
-  if (d.head_dim != 128)
-    return fail(PKA_ERR_UNSUPPORTED, "prefill head_dim must be 128 (got %d; 256 not built)",
-                d.head_dim);
+  if (d.head_dim != 128 && d.head_dim != 256)
+    return fail(PKA_ERR_UNSUPPORTED, "prefill head_dim must be 128 or 256 (got %d)", d.head_dim);
   PKA_CHECK_ARG(d.mask == PKA_MASK_DENSE || d.mask == PKA_MASK_CAUSAL ||
                     d.mask == PKA_MASK_VARIABLE_WINDOW,
                 "unknown mask %d", d.mask);
@@ -56,7 +54,10 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
   p.G = p.Hq / p.Hkv;
   p.D = d.head_dim;
   p.scale = d.sm_scale;
-  p.heads_per_cta = (p.G % 2 == 0) ? 2 : 1;
+  // D = 128: 128-key tiles, two heads of a GQA group per CTA when the group is
+  // even; D = 256: 64-key tiles, one head per CTA (shared memory and TMEM).
+  p.heads_per_cta = (p.D == 128 && p.G % 2 == 0) ? 2 : 1;
+  const int64_t kTileK = p.D == 128 ? 128 : 64;
   p.qo.assign(qo, qo + B + 1);
   p.kv.assign(kv, kv + B + 1);
   p.win_lo.clear();

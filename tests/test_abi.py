@@ -78,7 +78,7 @@ def test_run_rejects_host_only_plan_and_null_pointers():
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(head_dim=256), L.PKA_ERR_UNSUPPORTED),
+    (dict(head_dim=64), L.PKA_ERR_UNSUPPORTED),
     (dict(window_left=-2), L.PKA_ERR_INVALID_ARG),
     (dict(num_qo_heads=6, num_kv_heads=4), L.PKA_ERR_INVALID_ARG),
 ])

@@ -31,13 +31,15 @@ def _check(out, lse, ref_o, ref_l):
         assert (np.abs(l - ref_l) <= LSE_ATOL).all(), f"LSE err {np.abs(l - ref_l).max():.4g}"
 
 
-def _run(lq, lk, Hq, Hkv, causal=True, seed=0, dtype=torch.bfloat16, out_dtype=None, **kw):
+def _run(lq, lk, Hq, Hkv, causal=True, seed=0, dtype=torch.bfloat16, out_dtype=None, D=128,
+         **kw):
     qi, ki = _indptr(lq), _indptr(lk)
-    q = _rand((int(qi[-1]), Hq, 128), seed + 1, dtype)
-    k = _rand((int(ki[-1]), Hkv, 128), seed + 2, dtype)
-    v = _rand((int(ki[-1]), Hkv, 128), seed + 3, dtype)
+    q = _rand((int(qi[-1]), Hq, D), seed + 1, dtype)
+    k = _rand((int(ki[-1]), Hkv, D), seed + 2, dtype)
+    v = _rand((int(ki[-1]), Hkv, D), seed + 3, dtype)
     plan = api.batch_prefill_plan(qi, ki, num_qo_heads=Hq, num_kv_heads=Hkv, causal=causal,
-                                  return_lse=True, dtype=dtype, out_dtype=out_dtype, **kw)
+                                  return_lse=True, dtype=dtype, out_dtype=out_dtype, head_dim=D,
+                                  **kw)
     out, lse = api.batch_prefill_run(plan, q, k, v)
     torch.cuda.synchronize()
     plan.check()
@@ -124,6 +126,39 @@ def test_prefill_input_and_output_dtypes(dtype, out_dtype):
     """fp16 q/k/v (kind::f16 MMAs on half operands) and out_dtype (batch_prefill)."""
     lens = [1, 127, 300, 513]
     _run(lens, lens, 8, 2, seed=70, dtype=dtype, out_dtype=out_dtype, window_left=200)
+
+
+@pytest.mark.parametrize("causal,W", [(True, -1), (False, -1), (True, 100)])
+def test_prefill_head_dim_256(causal, W):
+    """head_dim 256 (batch_prefill allows D = 128 or 256): 64-key tiles, one head per CTA."""
+    lq = [1, 64, 65, 127, 300, 513]
+    lk = [1, 64, 100, 127, 400, 513] if causal else [9, 64, 65, 200, 300, 513]
+    _run(lq, lk, 4, 2, causal=causal, seed=80, D=256, window_left=W, output_scale=0.5)
+
+
+@pytest.mark.parametrize("dtype,out_dtype", [(torch.float16, torch.float32), (torch.bfloat16, None)])
+def test_prefill_head_dim_256_dtypes_and_odd_group(dtype, out_dtype):
+    _run([200, 37], [260, 37], 6, 2, seed=81, D=256, dtype=dtype, out_dtype=out_dtype)
+
+
+def test_prefill_head_dim_256_variable_window():
+    B, Sq, Sk = 2, 150, 230
+    g = np.random.default_rng(82)
+    a, b = g.integers(0, Sk, size=(B, Sq)), g.integers(0, Sk, size=(B, Sq))
+    st, en = np.minimum(a, b).astype(np.int32), np.maximum(a, b).astype(np.int32)
+    q = _rand((B, Sq, 4, 256), 83)
+    k, v = _rand((B, Sk, 2, 256), 84), _rand((B, Sk, 2, 256), 85)
+    plan = api.batch_prefill_plan_fixed(B, Sq, Sk, num_qo_heads=4, num_kv_heads=2,
+                                        mask_type="variable_window", head_dim=256,
+                                        variable_window_token_starts=st,
+                                        variable_window_token_ends=en, return_lse=True)
+    out, lse = api.batch_prefill_run(plan, q, k, v)
+    torch.cuda.synchronize()
+    plan.check()
+    ref_o, ref_l = oracle.batch_prefill(wl.bf16_bits(q.flatten(0, 1)), wl.bf16_bits(k.flatten(0, 1)),
+                                        wl.bf16_bits(v.flatten(0, 1)), np.arange(B + 1) * Sq,
+                                        np.arange(B + 1) * Sk, 2, window_starts=st, window_ends=en)
+    _check(out.flatten(0, 1), lse.flatten(0, 1), ref_o, ref_l)
 
 
 def test_prefill_full_size_sampled():
