@@ -300,7 +300,8 @@ def time_decode(inp, plan, steps, warmup, dist=None):
 def time_decode_e2e(inp, plan_kw, steps, warmup):
     """The user-facing call sequence with host buffers, wall clock per step:
     pinned host q / block_tables / seq_lens -> device, host planning on the
-    lengths, paged_decode_run, device -> pinned host read of O (and LSE).
+    lengths (paged_decode_plan_update of one plan, as a serving loop re-plans
+    each step), paged_decode_run, device -> pinned host read of O (and LSE).
     The KV pools are the cache: they stay resident on the device."""
     import torch
     from paged_kv_attention_32_gb300 import api
@@ -318,14 +319,16 @@ def time_decode_e2e(inp, plan_kw, steps, warmup):
     bytes_in = (h_q.numel() * 2 + h_bt.numel() * 4 + h_seq.numel() * 4)
     bytes_out = h_out.numel() * 2 + (h_lse.numel() * 4 if inp["return_lse"] else 0)
 
+    kw = dict(plan_kw)
+    if h_ind is not None:
+        kw["qo_indptr"] = h_ind
+    plan = api.paged_decode_plan(h_seq, stream=stream, **kw)   # made once, re-planned per step
+
     def step():
         d_q.copy_(h_q, non_blocking=True)
         d_bt.copy_(h_bt, non_blocking=True)
         d_seq.copy_(h_seq, non_blocking=True)
-        kw = dict(plan_kw)
-        if h_ind is not None:
-            kw["qo_indptr"] = h_ind
-        p = api.paged_decode_plan(h_seq, stream=stream, **kw)
+        p = plan.update(h_seq, qo_indptr=h_ind, stream=stream)
         r = api.paged_decode_run(p, d_q, inp["k_pages"], inp["v_pages"], d_bt,
                                  seq_lens_kv=d_seq, sinks=inp["sinks"], stream=stream)
         o = r[0] if isinstance(r, tuple) else r
@@ -632,7 +635,8 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
                     "h2d_bytes_per_step": bin_, "d2h_bytes_per_step": bout,
-                    "note": "host planning + pinned H2D of q/tables/lengths + run + D2H of O; "
+                    "note": "host re-planning of one plan (paged_decode_plan_update) + pinned "
+                            "H2D of q/tables/lengths + run + D2H of O; "
                             "the KV cache stays resident"},
             "gpu_launches": args.steps * head["launches_per_call"],
             "clocks": clocks,

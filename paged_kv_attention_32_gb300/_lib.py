@@ -26,7 +26,8 @@ PKA_KERNEL_CUDA_CORE, PKA_KERNEL_MMA = 0, 1
 # every symbol include/pka.h declares
 EXPORTED = (
     "pka_last_error", "pka_version",
-    "paged_decode_plan", "paged_decode_plan_destroy", "paged_decode_plan_info",
+    "paged_decode_plan", "paged_decode_plan_update", "paged_decode_plan_destroy",
+    "paged_decode_plan_info",
     "paged_decode_plan_export", "paged_decode_run", "paged_decode_plan_check",
     "paged_decode_run_noalloc",
     "attn_merge_lse",
@@ -81,6 +82,8 @@ _SIGS = {
     "pka_version": (ctypes.c_char_p, []),
     "paged_decode_plan": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.POINTER(DecodeDesc), _pi32,
                                          _pi32, ctypes.POINTER(_sz), _vp]),
+    "paged_decode_plan_update": (ctypes.c_int, [_vp, _i32, _pi32, _pi32, ctypes.POINTER(_sz),
+                                                _vp]),
     "paged_decode_plan_destroy": (None, [_vp]),
     "paged_decode_plan_info": (ctypes.c_int, [_vp, ctypes.POINTER(PlanInfo)]),
     "paged_decode_plan_export": (ctypes.c_int, [_vp, _pi32, _pi32, _pi32, _pi32, _pi32, _pi32]),

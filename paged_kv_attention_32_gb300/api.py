@@ -82,6 +82,21 @@ class DecodePlan:
         out["items"] = [tuple(r) for r in items[: n * 5].view(n, 5).tolist()]
         return out
 
+    def update(self, seq_lens_kv, qo_indptr=None, stream=None):
+        """Re-plan in place for a new batch (``paged_decode_plan_update``): new host
+        lengths (and packed offsets), same heads, masks and options."""
+        seq_t, seq_p = _host_i32(seq_lens_kv)
+        ind_t, ind_p = _host_i32(qo_indptr)
+        ws = ctypes.c_size_t()
+        host_only = bool(self.desc.flags & L.PKA_PLAN_HOST_ONLY)
+        rc = L.lib().paged_decode_plan_update(self.handle, seq_t.numel(), seq_p, ind_p,
+                                              ctypes.byref(ws),
+                                              None if host_only else _stream(stream))
+        L.check(rc, "paged_decode_plan_update")
+        self.desc.batch_size = seq_t.numel()
+        self.workspace_bytes = ws.value
+        return self
+
     def check(self, stream=None):
         """Synchronise and read the device status word (raises on a kernel timeout)."""
         L.check(L.lib().paged_decode_plan_check(self.handle, _stream(stream)), "plan_check")

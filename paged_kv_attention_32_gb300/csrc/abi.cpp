@@ -52,14 +52,26 @@ int upload_decode_plan(pka_plan& p, cudaStream_t stream) {
   const size_t off_merge = off_reqs + up256(n_reqs);
   const size_t off_status = off_merge + up256(n_merge);
   const size_t total = off_status + 256;
-  PKA_CUDA_TRY(cudaGetDevice(&p.device), "cudaGetDevice");
-  PKA_CUDA_TRY(cudaMalloc(&p.dev_buf, total), "cudaMalloc(decode plan)");
+  if (p.dev_buf == nullptr || total > p.dev_capacity) {
+    // a replan that outgrows the buffer reallocates it with headroom
+    if (p.dev_buf != nullptr) {
+      PKA_CUDA_TRY(cudaFree(p.dev_buf), "cudaFree(decode plan)");
+      p.dev_buf = nullptr;
+      p.dev_capacity = 0;
+    }
+    const size_t cap = p.dev_capacity == 0 && total < 4096 ? 4096 : total + total / 2;
+    PKA_CUDA_TRY(cudaGetDevice(&p.device), "cudaGetDevice");
+    PKA_CUDA_TRY(cudaMalloc(&p.dev_buf, cap), "cudaMalloc(decode plan)");
+    p.dev_capacity = cap;
+  }
   uint8_t* base = static_cast<uint8_t*>(p.dev_buf);
   p.d_items = reinterpret_cast<const WorkItem*>(base);
   p.d_reqs = reinterpret_cast<const ReqInfo*>(base + off_reqs);
   p.d_merge_rows = reinterpret_cast<const MergeRow*>(base + off_merge);
   p.d_status = reinterpret_cast<int32_t*>(base + off_status);
-  // The host vectors live as long as the plan, so asynchronous copies are safe.
+  // Copies from these pageable host vectors are staged before cudaMemcpyAsync
+  // returns, so a later replan may overwrite them; stream order keeps the
+  // upload behind runs already queued on the same stream.
   if (n_items)
     PKA_CUDA_TRY(cudaMemcpyAsync(base, p.items.data(), n_items, cudaMemcpyHostToDevice, stream),
                  "cudaMemcpyAsync(plan items)");
@@ -161,6 +173,35 @@ int paged_decode_plan(pka_plan** plan_out, const pka_decode_desc* desc,
   }
   if (workspace_bytes_out) *workspace_bytes_out = (size_t)p->workspace_bytes;
   *plan_out = p;
+  return PKA_OK;
+}
+
+int paged_decode_plan_update(pka_plan* p, int32_t batch_size, const int32_t* seq_lens_kv_host,
+                             const int32_t* qo_indptr_host, size_t* workspace_bytes_out,
+                             void* stream) {
+  clear_error();
+  PKA_CHECK_ARG(p != nullptr, "plan must not be NULL");
+  pka_decode_desc d = p->desc;
+  d.batch_size = batch_size;
+  pka_plan fresh;
+  int rc = build_decode_plan(fresh, d, seq_lens_kv_host, qo_indptr_host);
+  if (rc != PKA_OK) return rc;   // the old plan stays as it was
+  if (!(p->desc.flags & PKA_PLAN_HOST_ONLY)) {
+    int dev = -1;
+    PKA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+    PKA_CHECK_ARG(dev == p->device, "plan was made on device %d, current device is %d", p->device,
+                  dev);
+  }
+  fresh.dev_buf = p->dev_buf;
+  fresh.dev_capacity = p->dev_capacity;
+  fresh.device = p->device;
+  p->dev_buf = nullptr;
+  *p = std::move(fresh);
+  if (!(p->desc.flags & PKA_PLAN_HOST_ONLY)) {
+    rc = upload_decode_plan(*p, static_cast<cudaStream_t>(stream));
+    if (rc != PKA_OK) return rc;
+  }
+  if (workspace_bytes_out) *workspace_bytes_out = (size_t)p->workspace_bytes;
   return PKA_OK;
 }
 

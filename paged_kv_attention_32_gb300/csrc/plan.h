@@ -89,6 +89,7 @@ struct pka_plan {
   std::vector<pka::MergeRow> merge_rows;
   // one device allocation holding items | reqs | merge rows | status word
   void* dev_buf = nullptr;
+  size_t dev_capacity = 0;    // bytes of dev_buf (reused by paged_decode_plan_update)
   const pka::WorkItem* d_items = nullptr;
   const pka::ReqInfo* d_reqs = nullptr;
   const pka::MergeRow* d_merge_rows = nullptr;

@@ -160,6 +160,23 @@ def test_decode_strided_query_and_combined_kv():
     assert_close(out, lse, ref_o, ref_l)
 
 
+def test_decode_plan_update_reuses_and_grows():
+    """One plan re-planned for three batches: 2 requests, then 40 (outgrows the plan's
+    device buffer: reallocated), then 5 (fits: reused)."""
+    from helpers import decode_plan_for
+    plan = None
+    for seed, batch in [(15, 2), (16, 40), (17, 5)]:
+        w = wl.shrink(SMALL["llama3_8b"], batch=batch, pool_pages=7000)
+        inp = wl.make_decode_inputs(w, seed=seed, device=DEV)
+        if plan is None:
+            plan = decode_plan_for(inp, num_sms=16)
+        else:
+            plan.update(inp["seq_lens_kv"].cpu())
+        out, lse, _ = run_decode(inp, plan=plan)
+        ref_o, ref_l = oracle_decode(inp)
+        assert_close(out, lse, ref_o, ref_l)
+
+
 def test_decode_graph_capture_replays_eagerly_equal():
     inp = wl.make_decode_inputs(SMALL["skewed"], seed=9, device=DEV)
     from helpers import decode_plan_for

@@ -8,6 +8,7 @@ import random
 import pytest
 
 from oracle.plan_spec import plan_spec
+from paged_kv_attention_32_gb300 import _lib as L
 from paged_kv_attention_32_gb300 import api
 
 
@@ -77,3 +78,20 @@ def test_kernel_choice_follows_rows_per_kv_head():
     assert kernel(8, 2) == (1, 16)
     assert kernel(4, 3, mma_min_rows=16) == (1, 12)   # 9..15 rows exceed one CUDA-core warp
     assert kernel(4, 1, mma_min_rows=4) == (1, 4)
+
+
+def test_plan_update_equals_a_fresh_plan():
+    """paged_decode_plan_update rebuilds in place: the same arrays as a new plan for the
+    new batch (size, lengths, packed offsets), and a failed update leaves the plan as it was."""
+    kw = dict(num_qo_heads=16, num_kv_heads=2, page_size=16, max_pages_per_seq=600,
+              num_pages=10 ** 6, num_sms=16, causal=True, window_left=300, host_only=True)
+    p = api.paged_decode_plan([100, 3000, 50], qo_indptr=[0, 2, 5, 6], **kw)
+    for seq, ind in [([4000, 20, 20, 6000, 7], [0, 1, 4, 5, 8, 9]), ([9000], [0, 3])]:
+        p.update(seq, qo_indptr=ind)
+        fresh = api.paged_decode_plan(seq, qo_indptr=ind, **kw)
+        assert p.export() == fresh.export()
+        assert p.info == fresh.info and p.workspace_bytes == fresh.workspace_bytes
+    before = p.export()
+    with pytest.raises(L.PkaError):
+        p.update([5, 5], qo_indptr=[0, 6, 7])   # kv_len < q_len
+    assert p.export() == before
