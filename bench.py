@@ -348,6 +348,19 @@ def time_decode_e2e(inp, plan_kw, steps, warmup):
     return (time.perf_counter() - t0) * 1e3 / steps, bytes_in, bytes_out
 
 
+def reduce_over_ranks(ms, nbytes, dist=None, device="cpu"):
+    """Whole-job figure of N replicas: the slowest rank's time and every rank's bytes
+    (each rank decodes its own seeded batch, so the byte counts differ)."""
+    if dist is None:
+        return ms, nbytes
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    b = torch.tensor([float(nbytes)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(round(b.item()))
+
+
 def headline_traffic(head):
     """DRAM bytes per headline launch from the ncu capture, scaled to this call's K+V bytes
     (None when the plan runs another kernel than the one captured)."""
@@ -597,25 +610,25 @@ def main():
         head, inp, plan = measure_workload(HEADLINE, args.seed + rank, args.steps, args.warmup,
                                            peak_gbs, dist)
     clocks = clk.summary()
-    ms = head["ms_per_call"]
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    total_bytes = head["kv_bytes"] * world
+    ms, total_bytes = reduce_over_ranks(head["ms_per_call"], head["kv_bytes"], dist, "cuda")
     value = total_bytes / (ms * 1e-3) / 1e9
     gbs_kernel = head["kv_bytes"] / (head["ms_per_call"] * 1e-3) / 1e9
 
+    # end to end through the public API on every rank: slowest rank, all ranks' bytes
+    from paged_kv_attention_32_gb300 import workloads as wl
+    w = wl.DECODE_WORKLOADS[HEADLINE]
+    plan_kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
+                   page_size=w.page_size, max_pages_per_seq=inp["block_tables"].shape[1],
+                   num_pages=inp["k_pages"].shape[0], return_lse=w.return_lse, q_len=1)
+    if dist is not None:
+        dist.barrier()
+    e2e_ms, bin_, bout = time_decode_e2e(inp, plan_kw, min(args.steps, 50),
+                                         max(3, min(args.warmup, 3)))
+    e2e_ms, e2e_bytes = reduce_over_ranks(e2e_ms, head["kv_bytes"], dist, "cuda")
+
     line = None
     if rank == 0:
-        from paged_kv_attention_32_gb300 import workloads as wl
-        w = wl.DECODE_WORKLOADS[HEADLINE]
-        plan_kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
-                       page_size=w.page_size, max_pages_per_seq=inp["block_tables"].shape[1],
-                       num_pages=inp["k_pages"].shape[0], return_lse=w.return_lse, q_len=1)
-        e2e_ms, bin_, bout = time_decode_e2e(inp, plan_kw, min(args.steps, 50),
-                                             max(3, min(args.warmup, 3)))
-        e2e_val = head["kv_bytes"] * world / (e2e_ms * 1e-3) / 1e9
+        e2e_val = e2e_bytes / (e2e_ms * 1e-3) / 1e9
         cpu = cpu_baseline(inp) if (world == 1 and not args.no_cpu) else None
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
