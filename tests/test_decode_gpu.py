@@ -177,6 +177,37 @@ def test_decode_plan_update_reuses_and_grows():
         assert_close(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("G,ps", [(4, 256), (8, 256), (16, 128)])
+def test_decode_largest_page_sizes(G, ps):
+    """page_size up to 256 (16 TMA units per page), GQA group 4, 8 and 16 rows."""
+    w = wl.DecodeWorkload(name="bigpage", batch=3, num_qo_heads=2 * G, num_kv_heads=2,
+                          head_dim=128, page_size=ps, kv_len_range=(1, 2000), causal=True)
+    inp = wl.make_decode_inputs(w, seed=18, device=DEV)
+    out, lse, _ = run_decode(inp)
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+def test_decode_single_request_single_key():
+    """The degenerate decode: one request, one key -> O is that key's value row (bmm2 1)."""
+    w = wl.DecodeWorkload(name="one", batch=1, num_qo_heads=4, num_kv_heads=1, head_dim=128,
+                          page_size=16, kv_len_range=(1, 1))
+    inp = wl.make_decode_inputs(w, seed=19, device=DEV)
+    out, lse, _ = run_decode(inp)
+    page = int(inp["block_tables"][0, 0])
+    v0 = inp["v_pages"][page, 0, 0].float()
+    assert torch.equal(out[0].float(), v0.expand(4, 128))
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+def test_decode_sink_minus_infinity_is_no_sink():
+    inp = wl.make_decode_inputs(SMALL["spec"], seed=20, device=DEV)
+    out_a, lse_a, _ = run_decode(dict(inp, sinks=torch.full_like(inp["sinks"], -float("inf"))))
+    out_b, lse_b, _ = run_decode(dict(inp, sinks=None))
+    assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
+
+
 def test_decode_graph_capture_replays_eagerly_equal():
     inp = wl.make_decode_inputs(SMALL["skewed"], seed=9, device=DEV)
     from helpers import decode_plan_for

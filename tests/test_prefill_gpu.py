@@ -161,6 +161,12 @@ def test_prefill_head_dim_256_variable_window():
     _check(out.flatten(0, 1), lse.flatten(0, 1), ref_o, ref_l)
 
 
+@pytest.mark.parametrize("D", [128, 256])
+def test_prefill_empty_and_single_row_requests(D):
+    """Requests with no rows and no keys, and one-row one-key requests, among others."""
+    _run([0, 1, 0, 200, 1], [0, 1, 0, 230, 5], 4, 2, seed=90, D=D)
+
+
 def test_prefill_full_size_sampled():
     """The ragged prefill workload at full size (as bench.py times it), sampled rows."""
     w = wl.RAGGED_PREFILL
