@@ -447,7 +447,7 @@ int batch_prefill_run(const pka_prefill_plan* p, const void* q, int64_t q_stride
   {
     const uint64_t dims[3] = {(uint64_t)p->D, (uint64_t)p->Hkv, (uint64_t)p->total_kv};
     const uint64_t strides[2] = {(uint64_t)kv_stride_head * 2, (uint64_t)kv_stride_tok * 2};
-    const uint32_t box[3] = {64, 1, p->D == 128 ? 128u : 64u};   // one key tile per box row
+    const uint32_t box[3] = {64, 1, 64};   // one 64-key tile per 64-column block
     rc = encode_bf16_map(&kmap, k, 3, dims, strides, box);
     if (rc != PKA_OK) return rc;
     rc = encode_bf16_map(&vmap, v, 3, dims, strides, box);
@@ -471,13 +471,10 @@ int batch_prefill_run(const pka_prefill_plan* p, const void* q, int64_t q_stride
   a.window_left = p->desc.window_left;
   a.window_lo = p->d_win_lo;
   a.window_hi = p->d_win_hi;
-  a.heads_per_cta = p->heads_per_cta;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.output_scale = p->desc.output_scale;
   a.out_dtype = p->desc.out_dtype;
-  if (p->D == 256)
-    return launch_prefill_d256(*p, a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream));
-  return launch_prefill(*p, a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream));
+  return launch_prefill_1h(*p, a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream));
 }
 
 int batch_prefill_plan_check(const pka_prefill_plan* p, void* stream) {

@@ -11,13 +11,13 @@
 
 namespace pka {
 
-// One CTA of the prefill kernel: a 128-row query tile of one request for a
-// pair of query heads that share a KV head (or one head when the group is odd).
+// One CTA of the prefill kernel: a 128-row query tile of one request for one
+// query head.
 struct PrefillTile {
   int32_t request;
   int32_t head;     // first query head of the tile
   int32_t q_tile;   // 128-row tile index inside the request
-  int32_t n_kv;     // KV tiles (128 keys; 64 with head_dim 256) the tile visits
+  int32_t n_kv;     // KV tiles (64 keys) the tile visits
   int32_t kv0;      // first of them (past 0 only with a window)
 };
 
@@ -39,7 +39,6 @@ struct PrefillArgs {
   int32_t window_left;   // -1: no window
   const int32_t* window_lo;   // variable_window: first key of each query row, else nullptr
   const int32_t* window_hi;   // variable_window: last key (inclusive) of each query row
-  int32_t heads_per_cta;
   float scale_log2;
   float output_scale;
   int32_t out_dtype;       // PKA_DTYPE_BF16 / F16 / F32
@@ -50,7 +49,7 @@ struct PrefillArgs {
 struct pka_prefill_plan {
   pka_prefill_desc desc;
   int32_t B = 0, Hq = 0, Hkv = 0, G = 0, D = 0;
-  int32_t total_q = 0, total_kv = 0, heads_per_cta = 1;
+  int32_t total_q = 0, total_kv = 0;
   float scale = 0.f;
   std::vector<int32_t> qo, kv;
   std::vector<int32_t> win_lo, win_hi;   // variable_window bounds per query row (host)
@@ -74,13 +73,10 @@ int build_prefill_plan(pka_prefill_plan& plan, const pka_prefill_desc& desc, con
                        const int32_t* kv, const int32_t* win_lo = nullptr,
                        const int32_t* win_hi = nullptr);
 
-// Launches the prefill kernel over the plan's tiles (head_dim 128).
-int launch_prefill(const pka_prefill_plan& plan, const PrefillArgs& args, const CUtensorMap& qmap,
-                   const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream);
-
-// Same for head_dim 256 (64-key tiles, one head per CTA).
-int launch_prefill_d256(const pka_prefill_plan& plan, const PrefillArgs& args,
-                        const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                        cudaStream_t stream);
+// Launches the prefill kernel (one query head and 128 rows per CTA, 64-key
+// tiles; head_dim 128 or 256) over the plan's tiles.
+int launch_prefill_1h(const pka_prefill_plan& plan, const PrefillArgs& args,
+                      const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                      cudaStream_t stream);
 
 }  // namespace pka

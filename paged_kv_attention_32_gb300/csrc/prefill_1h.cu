@@ -1,22 +1,24 @@
-// Prefill with head_dim 256 on the 5th-generation tensor cores (tcgen05 + TMEM).
+// Prefill, one query head per CTA, on the 5th-generation tensor cores
+// (tcgen05 + TMEM); head_dim D = 256 (batch_prefill allows 128 or 256), or 128.
 //
-// batch_prefill allows D = 128 or 256.  Same masks and outputs as the D = 128
-// kernel (bottom-right causal diagonal, dense, left window, variable_window;
-// O scaled by output_scale, base-2 LSE), with a tile shape that fits D = 256:
-// one CTA = one 128-row query tile of one request and one query head, keys in
-// tiles of 64 (Q 64 KB + two K and two V stages of 32 KB in shared memory).
-//   warp 4      TMA producer: Q once (four 64-column boxes), then K and V
-//               tiles (four 64-column boxes each, 128-byte swizzle);
+// Same masks and outputs as the two-head D = 128 kernel (bottom-right causal
+// diagonal, dense, left window, variable_window; O scaled by output_scale,
+// base-2 LSE).  One CTA = one 128-row query tile of one request and one query
+// head, keys in tiles of 64: Q (D/64 boxes of 16 KB) + two K and two V stages
+// (D/64 boxes of 8 KB each) in shared memory.
+//   warp 4      TMA producer: Q once, then K and V tiles (64-column boxes,
+//               128-byte swizzle);
 //   warp 5      allocates TMEM and issues every tcgen05.mma from one thread:
-//               S_b = Q K^T (M=128, N=64, 16 k-steps) into one of two S
+//               S_b = Q K^T (M=128, N=64, D/16 k-steps) into one of two S
 //               buffers -- two key tiles ahead of the softmax, so the tensor
 //               core works while the softmax runs -- and O += P V (M=128,
-//               N=256, 4 k-steps of 16 keys, P read from TMEM, V MN-major);
+//               N=D, 4 k-steps of 16 keys, P read from TMEM, V MN-major);
 //   warps 0-3   softmax, one thread per query row (TMEM lane): row max of the
 //               64 scores, lazy rescaling of O only when the max grew by more
 //               than 2^8, p = exp2(s * scale*log2e - m), bf16/f16 P over the
 //               first 32 columns of the S buffer, final O / l and LSE.
-// TMEM columns: S0 [0,64) S1 [64,128) O [128,384) (512 allocated).
+// TMEM columns: S0 [0,64) S1 [64,128) O [128,128+D) (256 or 512 allocated;
+// with D = 128 two CTAs share an SM).
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
@@ -33,14 +35,23 @@ namespace {
 constexpr int kTileQ = 128, kTileK = 64;
 constexpr uint32_t kQBox = 16384;           // 128 rows x 128 bytes (64 columns)
 constexpr uint32_t kKBox = 8192;            // 64 rows x 128 bytes
-constexpr uint32_t kOffQ = 0;               // 4 column blocks x 16 KB
-constexpr uint32_t kOffK = 65536;           // 2 stages x 4 blocks x 8 KB
-constexpr uint32_t kOffV = 131072;          // 2 stages x 4 blocks x 8 KB
-constexpr uint32_t kOffBar = 196608;
-constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
 constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr uint32_t kColO = 128, kTmemCols = 512;
+constexpr uint32_t kColO = 128;
+
+// Shared memory and TMEM of head_dim D (NB = D / 64 column blocks): Q NB x 16 KB,
+// then two K and two V stages of NB x 8 KB; S0 S1 (64 columns each) then O (D).
+template <int D>
+struct Geo {
+  static constexpr int NB = D / 64;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = NB * kQBox;
+  static constexpr uint32_t kOffV = kOffK + 2 * NB * kKBox;
+  static constexpr uint32_t kOffBar = kOffV + 2 * NB * kKBox;
+  static constexpr size_t kSmemBytes = 1024 + kOffBar + 256;
+  static constexpr uint32_t kTmemCols = kColO + D <= 256 ? 256 : 512;
+  static constexpr int kMinBlocks = D == 128 ? 2 : 1;   // 2 x 97 KB, 2 x 256 TMEM columns
+};
 
 enum {
   B_Q = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 7, B_SFULL = 9, B_PFULL = 11,
@@ -48,7 +59,7 @@ enum {
 };
 
 template <bool F16> constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, 0, 0, F16);
-template <bool F16> constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1, F16);
+template <int D, bool F16> constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1, F16);
 
 // Q (128 rows) or K (64 rows) as the K-major operand: column block kk / 4,
 // 32-byte step kk % 4 inside the 128-byte rows, 8-row groups every 1024 bytes.
@@ -66,10 +77,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
 }
 
-template <bool F16>
-__global__ void __launch_bounds__(kThreads, 1)
-prefill_d256_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
+template <int D, bool F16>
+__global__ void __launch_bounds__(kThreads, Geo<D>::kMinBlocks)
+prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  using Gm = Geo<D>;
+  constexpr int NB = Gm::NB;
+  constexpr uint32_t kOffQ = Gm::kOffQ, kOffK = Gm::kOffK, kOffV = Gm::kOffV, kOffBar = Gm::kOffBar;
+  constexpr uint32_t kTmemCols = Gm::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -114,8 +129,8 @@ prefill_d256_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant
       tma_prefetch_desc(&tmq);
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
-      mbar_arrive_expect_tx(bar(B_Q), 4u * kQBox);
-      for (int blk = 0; blk < 4; ++blk)
+      mbar_arrive_expect_tx(bar(B_Q), NB * kQBox);
+      for (int blk = 0; blk < NB; ++blk)
         tma_load_3d(sbase + kOffQ + (uint32_t)blk * kQBox, &tmq, bar(B_Q), blk * 64, h,
                     q0 + mt * kTileQ);
       auto load_kv = [&](int j, int which) -> bool {   // which: 0 = K, 1 = V
@@ -123,9 +138,9 @@ prefill_d256_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant
         const int full = which ? B_VFULL : B_KFULL, empty = which ? B_VEMPTY : B_KEMPTY;
         if (j >= 2 && !mbar_wait(bar(empty + st), (uint32_t)(((j >> 1) - 1) & 1), a.status))
           return false;
-        const uint32_t dst = sbase + (which ? kOffV : kOffK) + (uint32_t)st * 4u * kKBox;
-        mbar_arrive_expect_tx(bar(full + st), 4u * kKBox);
-        for (int blk = 0; blk < 4; ++blk)
+        const uint32_t dst = sbase + (which ? kOffV : kOffK) + (uint32_t)st * NB * kKBox;
+        mbar_arrive_expect_tx(bar(full + st), NB * kKBox);
+        for (int blk = 0; blk < NB; ++blk)
           tma_load_3d(dst + (uint32_t)blk * kKBox, which ? &tmv : &tmk, bar(full + st), blk * 64,
                       hk, k0 + (kv0 + j) * kTileK);
         return true;
@@ -156,9 +171,9 @@ prefill_d256_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant
         if (!mbar_wait(bar(B_KFULL + st), (uint32_t)((j >> 1) & 1), a.status)) return false;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)st * 64u;
-        const uint32_t kb = sbase + kOffK + (uint32_t)st * 4u * kKBox;
+        const uint32_t kb = sbase + kOffK + (uint32_t)st * NB * kKBox;
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
+        for (int kk = 0; kk < D / 16; ++kk)
           umma_bf16(d, kmajor(sbase + kOffQ, kQBox, kk), kmajor(kb, kKBox, kk), kIdescQK<F16>,
                     kk > 0 ? 1u : 0u);
         umma_commit(bar(B_SFULL + st));
@@ -174,10 +189,10 @@ prefill_d256_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant
         if (!ok) break;
         tc_fence_after();
         const uint32_t p_tm = tmem + (uint32_t)st * 64u;   // P: 32 columns, lanes 0-127
-        const uint32_t vb = sbase + kOffV + (uint32_t)st * 4u * kKBox;
+        const uint32_t vb = sbase + kOffV + (uint32_t)st * NB * kKBox;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ts(tmem + kColO, p_tm + (uint32_t)kk * 8u, vmn(vb, kk), kIdescPV<F16>,
+          umma_bf16_ts(tmem + kColO, p_tm + (uint32_t)kk * 8u, vmn(vb, kk), kIdescPV<D, F16>,
                        (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar(B_ODONE + st));
         umma_commit(bar(B_VEMPTY + st));
@@ -239,7 +254,7 @@ prefill_d256_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant
           break;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld32_sync(o_tm + (uint32_t)c * 32u, r);
 #pragma unroll
@@ -278,9 +293,9 @@ prefill_d256_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant
         warp_wait(bar(B_ODONE + ((n_kv - 1) & 1)), (uint32_t)(((n_kv - 1) >> 1) & 1), a.status)) {
       tc_fence_after();
       const float inv = l > 0.f ? a.output_scale / l : 0.f;
-      const int64_t dst = ((int64_t)(q0 + t) * a.num_qo_heads + h) * 256;
+      const int64_t dst = ((int64_t)(q0 + t) * a.num_qo_heads + h) * D;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32_sync(o_tm + (uint32_t)c * 32u, r);
         if (row_valid) {
@@ -306,21 +321,28 @@ prefill_d256_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant
   }
 }
 
+template <int D>
+int launch_1h(const pka_prefill_plan& plan, const PrefillArgs& args, const CUtensorMap& qmap,
+              const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t stream) {
+  if (args.num_tiles == 0) return PKA_OK;
+  auto kern = plan.desc.dtype == PKA_DTYPE_F16 ? prefill_1h_kernel<D, true>
+                                               : prefill_1h_kernel<D, false>;
+  const int smem = (int)Geo<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_1h)");
+  kern<<<args.num_tiles, kThreads, smem, stream>>>(args, qmap, kmap, vmap);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "prefill_1h_kernel launch");
+  return PKA_OK;
+}
+
 }  // namespace
 
-int launch_prefill_d256(const pka_prefill_plan& plan, const PrefillArgs& args,
-                        const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                        cudaStream_t stream) {
-  if (args.num_tiles == 0) return PKA_OK;
-  auto kern = plan.desc.dtype == PKA_DTYPE_F16 ? prefill_d256_kernel<true>
-                                               : prefill_d256_kernel<false>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_d256)");
-  kern<<<args.num_tiles, kThreads, kSmemBytes, stream>>>(args, qmap, kmap, vmap);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "prefill_d256_kernel launch");
-  return PKA_OK;
+int launch_prefill_1h(const pka_prefill_plan& plan, const PrefillArgs& args,
+                      const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                      cudaStream_t stream) {
+  if (plan.D == 256) return launch_1h<256>(plan, args, qmap, kmap, vmap, stream);
+  return launch_1h<128>(plan, args, qmap, kmap, vmap, stream);
 }
 
 }  // namespace pka

@@ -1,6 +1,6 @@
 // Host tile schedule of the ragged causal prefill (batch_prefill with packed
-// qo_indptr / kv_indptr).  One tile = 128 query rows of one request for the
-// query heads one CTA serves, with the run of 128-key tiles its rows can see
+// qo_indptr / kv_indptr).  One tile = 128 query rows of one request for one
+// query head, with the run of 64-key tiles its rows can see
 // (causal diagonal, optional left window); tiles are ordered heaviest first
 // (most KV tiles to visit), so that the hardware block scheduler hands the
 // long causal rows out before the short ones (longest-processing-time order).
@@ -13,7 +13,8 @@
 namespace pka {
 
 namespace {
-constexpr int kTileQ = 128;
+constexpr int kTileQ = 128;   // query rows per CTA
+constexpr int kTileK = 64;    // keys per K/V tile
 }  // namespace
 
 int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const int32_t* qo,
@@ -54,10 +55,6 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
   p.G = p.Hq / p.Hkv;
   p.D = d.head_dim;
   p.scale = d.sm_scale;
-  // D = 128: 128-key tiles, two heads of a GQA group per CTA when the group is
-  // even; D = 256: 64-key tiles, one head per CTA (shared memory and TMEM).
-  p.heads_per_cta = (p.D == 128 && p.G % 2 == 0) ? 2 : 1;
-  const int64_t kTileK = p.D == 128 ? 128 : 64;
   p.qo.assign(qo, qo + B + 1);
   p.kv.assign(kv, kv + B + 1);
   p.win_lo.clear();
@@ -96,7 +93,7 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
       }
       const int32_t kv0 = (int32_t)(lo / kTileK);
       const int32_t n_kv = (int32_t)(ceil_div(hi, kTileK) - kv0);
-      for (int32_t h = 0; h < p.Hq; h += p.heads_per_cta)
+      for (int32_t h = 0; h < p.Hq; ++h)
         p.tiles.push_back(PrefillTile{b, h, (int32_t)m, n_kv, kv0});
     }
   }

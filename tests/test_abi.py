@@ -98,8 +98,8 @@ def test_prefill_plan_rejects_causal_kv_shorter_than_q():
 def test_prefill_tiles_heaviest_first():
     p = api.batch_prefill_plan([0, 300, 310], [0, 300, 310], num_qo_heads=4, num_kv_heads=1,
                                host_only=True)
-    # 3 q-tiles for request 0 + 1 for request 1, two head pairs each
-    assert p.num_tiles == (3 + 1) * 2
+    # 3 q-tiles for request 0 + 1 for request 1, one CTA per query head each
+    assert p.num_tiles == (3 + 1) * 4
 
 
 def test_merge_rejects_bad_head_dim():
@@ -108,10 +108,10 @@ def test_merge_rejects_bad_head_dim():
 
 
 def test_prefill_fixed_plan_tiles_and_bound_checks():
-    """Fixed-shape prefill: B * ceil(Sq / 128) q-tiles per head pair; variable_window
+    """Fixed-shape prefill: B * ceil(Sq / 128) q-tiles per query head; variable_window
     bounds must satisfy 0 <= start <= end < Sk and come only with that mask."""
     p = api.batch_prefill_plan_fixed(2, 200, 300, num_qo_heads=8, num_kv_heads=2, host_only=True)
-    assert p.num_tiles == 2 * 2 * 4
+    assert p.num_tiles == 2 * 2 * 8
     st = np.zeros((2, 200), np.int32)
     en = np.full((2, 200), 299, np.int32)
     api.batch_prefill_plan_fixed(2, 200, 300, num_qo_heads=8, num_kv_heads=2,
