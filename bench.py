@@ -34,7 +34,7 @@ PREFILL_WINDOW = 2047   # sliding-window variant of the ragged prefill (2048 key
 # command and numbers are in profiles/decode_cc_kernel_llama3_8b_full_traffic.md.
 # Other seeds or ranks scale it by their algorithmic K+V bytes.
 NCU_TRAFFIC = {"kernel": "decode_cuda_core_kernel", "kv_bytes": 1128361984,
-               "dram_bytes": 1134495232}
+               "dram_bytes": 1130908672 + 3318528}
 METRIC = "paged decode effective KV HBM GB/s"
 UNIT = "GB/s"
 
