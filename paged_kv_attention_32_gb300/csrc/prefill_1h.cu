@@ -8,7 +8,8 @@
 // (D/64 boxes of 8 KB each) in shared memory.
 //   warp 4      TMA producer: Q once, then K and V tiles (64-column boxes,
 //               128-byte swizzle);
-//   warp 5      allocates TMEM and issues every tcgen05.mma from one thread:
+//   warp 5      allocates TMEM and issues every tcgen05.mma (one elected lane,
+//               four chained k-steps per asm block):
 //               S_b = Q K^T (M=128, N=64, D/16 k-steps) into one of two S
 //               buffers -- two key tiles ahead of the softmax, so the tensor
 //               core works while the softmax runs -- and O += P V (M=128,
@@ -164,44 +165,40 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       }
     }
   } else if (warp == 5) {
-    // ---------------- MMA issuer (one thread) ----------------
-    if (lane == 0) {
-      auto issue_qk = [&](int j) -> bool {   // S of tile j into buffer j & 1
-        const int st = j & 1;
-        if (!mbar_wait(bar(B_KFULL + st), (uint32_t)((j >> 1) & 1), a.status)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)st * 64u;
-        const uint32_t kb = sbase + kOffK + (uint32_t)st * NB * kKBox;
+    // ---------------- MMA issuer: the warp waits, one elected lane issues ----------------
+    auto issue_qk = [&](int j) -> bool {   // S of tile j into buffer j & 1
+      const int st = j & 1;
+      if (!warp_wait(bar(B_KFULL + st), (uint32_t)((j >> 1) & 1), a.status)) return false;
+      tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)st * 64u;
+      const uint32_t kb = sbase + kOffK + (uint32_t)st * NB * kKBox;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_bf16(d, kmajor(sbase + kOffQ, kQBox, kk), kmajor(kb, kKBox, kk), kIdescQK<F16>,
-                    kk > 0 ? 1u : 0u);
-        umma_commit(bar(B_SFULL + st));
-        umma_commit(bar(B_KEMPTY + st));
-        return true;
-      };
-      bool ok = mbar_wait(bar(B_Q), 0, a.status);
-      for (int j = 0; ok && j < n_kv && j < 2; ++j) ok = issue_qk(j);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j & 1;
-        ok = mbar_wait(bar(B_VFULL + st), (uint32_t)((j >> 1) & 1), a.status) &&
-             mbar_wait(bar(B_PFULL + st), (uint32_t)((j >> 1) & 1), a.status);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t p_tm = tmem + (uint32_t)st * 64u;   // P: 32 columns, lanes 0-127
-        const uint32_t vb = sbase + kOffV + (uint32_t)st * NB * kKBox;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ts(tmem + kColO, p_tm + (uint32_t)kk * 8u, vmn(vb, kk), kIdescPV<D, F16>,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_ODONE + st));
-        umma_commit(bar(B_VEMPTY + st));
-        // S buffer st is free again once this P V has read P (issue order)
-        if (j + 2 < n_kv) ok = issue_qk(j + 2);
-      }
-      umma_commit(bar(B_MMADONE));
-      mbar_wait(bar(B_MMADONE), 0, a.status);   // nothing of ours still runs on the tensor core
+      for (int blk = 0; blk < NB; ++blk)   // 4 k-steps of 16 per 64-column block
+        umma_ss_k4(d, kmajor(sbase + kOffQ, kQBox, 4 * blk), kmajor(kb, kKBox, 4 * blk),
+                   kIdescQK<F16>, blk > 0 ? 1u : 0u);
+      umma_commit_elect(bar(B_SFULL + st));
+      umma_commit_elect(bar(B_KEMPTY + st));
+      return true;
+    };
+    bool ok = warp_wait(bar(B_Q), 0, a.status);
+    for (int j = 0; ok && j < n_kv && j < 2; ++j) ok = issue_qk(j);
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int st = j & 1;
+      ok = warp_wait(bar(B_VFULL + st), (uint32_t)((j >> 1) & 1), a.status) &&
+           warp_wait(bar(B_PFULL + st), (uint32_t)((j >> 1) & 1), a.status);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t p_tm = tmem + (uint32_t)st * 64u;   // P: 32 columns, lanes 0-127
+      const uint32_t vb = sbase + kOffV + (uint32_t)st * NB * kKBox;
+      // 4 k-steps of 16 keys: P columns +8, V rows +16 (2048 bytes)
+      umma_ts_k4<2048 / 16>(tmem + kColO, p_tm, vmn(vb, 0), kIdescPV<D, F16>, j > 0 ? 1u : 0u);
+      umma_commit_elect(bar(B_ODONE + st));
+      umma_commit_elect(bar(B_VEMPTY + st));
+      // S buffer st is free again once this P V has read P (issue order)
+      if (j + 2 < n_kv) ok = issue_qk(j + 2);
     }
+    umma_commit_elect(bar(B_MMADONE));
+    warp_wait(bar(B_MMADONE), 0, a.status);   // nothing of ours still runs on the tensor core
   } else {
     // ---------------- softmax: one thread per query row ----------------
     const int row = tid;                       // warps 0-3
