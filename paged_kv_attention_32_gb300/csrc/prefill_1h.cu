@@ -78,6 +78,39 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
 }
 
+// p = exp2(s * sl2 - m) for the 64 scores of one row (ra: keys 0-31, rb: 32-63),
+// packed to 16-bit P over the first 32 columns of the row's S buffer; returns the
+// (even-key, odd-key) partial sums of p.  MASKED: keys outside [lo, lo + span)
+// give p = 0 (the scores there were already set to -inf for the row max; p is
+// zeroed again because -inf * 0 or -inf + inf would give NaN).
+template <bool MASKED, bool F16>
+__device__ __forceinline__ float2 exp_tile(const uint32_t* ra, const uint32_t* rb, float sl2,
+                                           float neg_m, int key0, int lo, unsigned span,
+                                           uint32_t s_tm) {
+  const float2 sc = make_float2(sl2, sl2), nm = make_float2(neg_m, neg_m);
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint32_t* r = half ? rb : ra;
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                  sc, nm);
+      float2 p = make_float2(ex2(x.x), ex2(x.y));
+      if constexpr (MASKED) {
+        if ((unsigned)(key0 + 32 * half + 2 * i - lo) >= span) p.x = 0.f;
+        if ((unsigned)(key0 + 32 * half + 2 * i + 1 - lo) >= span) p.y = 0.f;
+      }
+      if (i & 1) acc1 = __fadd2_rn(acc1, p);
+      else acc0 = __fadd2_rn(acc0, p);
+      pk[i] = pack2<F16>(p.x, p.y);
+    }
+    tmem_st16(s_tm + 16u * (uint32_t)half, pk);   // P over S columns already read
+  }
+  return __fadd2_rn(acc0, acc1);
+}
+
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, Geo<D>::kMinBlocks)
 prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
@@ -222,7 +255,8 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       tc_fence_after();
       const uint32_t s_tm = tmem + lane_off + (uint32_t)st * 64u;
       const int key0 = (kv0 + j) * kTileK;
-      const bool masked = key0 < lo || key0 + kTileK > hi;
+      // warp-uniform: a tile that needs the mask in any row takes the masked path
+      const bool masked = __any_sync(0xffffffffu, key0 < lo || key0 + kTileK > hi);
       uint32_t ra[32], rb[32];
       tmem_ld32(s_tm, ra);
       tmem_ld32(s_tm + 32u, rb);
@@ -236,9 +270,12 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           if ((unsigned)(key0 + 32 + i - lo) >= span) rb[i] = __float_as_uint(neg_inf());
         }
       }
-      float mraw = neg_inf();
+      // row max as four independent chains (short dependency chains for the scheduler)
+      float mq[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) mraw = fmax3(mraw, __uint_as_float(ra[i]), __uint_as_float(rb[i]));
+      for (int i = 0; i < 32; ++i)
+        mq[i & 3] = fmax3(mq[i & 3], __uint_as_float(ra[i]), __uint_as_float(rb[i]));
+      const float mraw = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
       // lazy rescale: move the reference max only when it grew by more than 2^8
       const float mx = mraw == neg_inf() ? neg_inf() : mraw * sl2;
       const bool grow = mx > m_ref + kRescaleThreshold;
@@ -262,27 +299,10 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       }
       m_ref = m_new;
       const float neg_m = -m_ref;
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t* r = half ? rb : ra;
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), sl2, neg_m));
-          float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), sl2, neg_m));
-          if (masked) {
-            if ((unsigned)(key0 + 32 * half + 2 * i - lo) >= span) p0 = 0.f;
-            if ((unsigned)(key0 + 32 * half + 2 * i + 1 - lo) >= span) p1 = 0.f;
-          }
-          sum0 += p0;
-          sum1 += p1;
-          pk[i] = pack2<F16>(p0, p1);
-        }
-        tmem_st16(s_tm + 16u * (uint32_t)half, pk);   // P over S columns already read
-      }
+      const float2 sum = masked ? exp_tile<true, F16>(ra, rb, sl2, neg_m, key0, lo, span, s_tm)
+                                : exp_tile<false, F16>(ra, rb, sl2, neg_m, key0, lo, span, s_tm);
       tmem_wait_st();
-      l = l * alpha + (sum0 + sum1);
+      l = l * alpha + (sum.x + sum.y);
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + st));
     }
