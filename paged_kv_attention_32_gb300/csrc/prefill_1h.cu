@@ -1,11 +1,11 @@
 // Prefill, one query head per CTA, on the 5th-generation tensor cores
-// (tcgen05 + TMEM); head_dim D = 256 (batch_prefill allows 128 or 256), or 128.
+// (tcgen05 + TMEM); head_dim D = 128 or 256.
 //
-// Same masks and outputs as the two-head D = 128 kernel (bottom-right causal
-// diagonal, dense, left window, variable_window; O scaled by output_scale,
-// base-2 LSE).  One CTA = one 128-row query tile of one request and one query
-// head, keys in tiles of 64: Q (D/64 boxes of 16 KB) + two K and two V stages
-// (D/64 boxes of 8 KB each) in shared memory.
+// Masks and outputs: bottom-right causal diagonal, dense, left window,
+// variable_window; O scaled by output_scale, base-2 LSE.  One CTA = one
+// 128-row query tile of one request and one query head, keys in tiles of 64:
+// Q (D/64 boxes of 16 KB) + two K and two V stages (D/64 boxes of 8 KB each)
+// in shared memory.
 //   warp 4      TMA producer: Q once, then K and V tiles (64-column boxes,
 //               128-byte swizzle);
 //   warp 5      allocates TMEM and issues every tcgen05.mma (one elected lane,
@@ -25,6 +25,7 @@
 #include "device_common.cuh"
 #include "host_common.h"
 #include "prefill.h"
+#include "prefill_softmax.cuh"
 #include "tcgen05.cuh"
 
 namespace pka {
@@ -72,43 +73,6 @@ __device__ __forceinline__ uint64_t kmajor(uint32_t base, uint32_t block_bytes, 
 // 16kk .. 16kk+15): 64-dim blocks every 8 KB, 8-key groups every 1024 bytes.
 __device__ __forceinline__ uint64_t vmn(uint32_t base, int kk) {
   return smem_desc_sw128(base + (uint32_t)kk * 2048u, kKBox, 1024u);
-}
-
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t* status) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
-}
-
-// p = exp2(s * sl2 - m) for the 64 scores of one row (ra: keys 0-31, rb: 32-63),
-// packed to 16-bit P over the first 32 columns of the row's S buffer; returns the
-// (even-key, odd-key) partial sums of p.  MASKED: keys outside [lo, lo + span)
-// give p = 0 (the scores there were already set to -inf for the row max; p is
-// zeroed again because -inf * 0 or -inf + inf would give NaN).
-template <bool MASKED, bool F16>
-__device__ __forceinline__ float2 exp_tile(const uint32_t* ra, const uint32_t* rb, float sl2,
-                                           float neg_m, int key0, int lo, unsigned span,
-                                           uint32_t s_tm) {
-  const float2 sc = make_float2(sl2, sl2), nm = make_float2(neg_m, neg_m);
-  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const uint32_t* r = half ? rb : ra;
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
-                                  sc, nm);
-      float2 p = make_float2(ex2(x.x), ex2(x.y));
-      if constexpr (MASKED) {
-        if ((unsigned)(key0 + 32 * half + 2 * i - lo) >= span) p.x = 0.f;
-        if ((unsigned)(key0 + 32 * half + 2 * i + 1 - lo) >= span) p.y = 0.f;
-      }
-      if (i & 1) acc1 = __fadd2_rn(acc1, p);
-      else acc0 = __fadd2_rn(acc0, p);
-      pk[i] = pack2<F16>(p.x, p.y);
-    }
-    tmem_st16(s_tm + 16u * (uint32_t)half, pk);   // P over S columns already read
-  }
-  return __fadd2_rn(acc0, acc1);
 }
 
 template <int D, bool F16>
@@ -263,19 +227,8 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       tmem_wait_ld();
       reg_fence32(ra);
       reg_fence32(rb);
-      if (masked) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if ((unsigned)(key0 + i - lo) >= span) ra[i] = __float_as_uint(neg_inf());
-          if ((unsigned)(key0 + 32 + i - lo) >= span) rb[i] = __float_as_uint(neg_inf());
-        }
-      }
-      // row max as four independent chains (short dependency chains for the scheduler)
-      float mq[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        mq[i & 3] = fmax3(mq[i & 3], __uint_as_float(ra[i]), __uint_as_float(rb[i]));
-      const float mraw = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+      if (masked) mask_scores64(ra, rb, key0, lo, span);
+      const float mraw = row_max64(ra, rb);
       // lazy rescale: move the reference max only when it grew by more than 2^8
       const float mx = mraw == neg_inf() ? neg_inf() : mraw * sl2;
       const bool grow = mx > m_ref + kRescaleThreshold;
