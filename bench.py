@@ -56,6 +56,8 @@ def parse():
                     help="decode plan: rows per KV head from which the mma kernel is used")
     ap.add_argument("--split-waves", type=int, default=0,
                     help="decode plan: target CTAs = split_waves x SMs (0 = library default)")
+    ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
+                    help="profiling: q/K/V type of the one decode workload timed")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -79,11 +81,24 @@ def profile_case(args):
         if args.batch:
             pool = None if w.pool_pages is None else max(1000, w.pool_pages * args.batch // w.batch)
             wl.DECODE_WORKLOADS[args.workload] = wl.shrink(w, batch=args.batch, pool_pages=pool)
-        r, _, _ = measure_workload(args.workload, args.seed, args.steps, args.warmup, peak_gbs)
+        dtype = torch.float16 if args.dtype == "f16" else torch.bfloat16
+        r, _, _ = measure_workload(args.workload, args.seed, args.steps, args.warmup, peak_gbs,
+                                   dtype=dtype)
         wl.DECODE_WORKLOADS[args.workload] = w
     torch.cuda.synchronize()
     emit({"profile_case": args.workload, "batch": args.batch, "plan": PLAN_OVERRIDES,
           "result": r})
+
+
+def measured_peaks_all():
+    """(HBM GB/s, bf16 TFLOP/s burst, source, bf16 TFLOP/s sustained or None)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return (d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured",
+                d.get("bf16_tflops_sustained"))
+    return 6800.0, 1900.0, "fallback", 1700.0
 
 
 def measured_peaks():
@@ -388,6 +403,38 @@ def measure_workload(name, seed, steps, warmup, peak_gbs, dist=None, dtype=None)
     return res, inp, plan
 
 
+def time_prefill_calls(run, steps, warmup):
+    """Device time per call of `run` (CUDA events over `steps` back-to-back calls
+    after `warmup`), with the SM clocks sampled during the timed calls."""
+    import torch
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0.record()
+        for _ in range(steps):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, clk.summary()
+
+
+def prefill_result(name, ms, flops, peak_tflops, tiles, clocks):
+    """A prefill line: achieved TFLOP/s against the measured bf16 peak taken as a
+    burst (the main fraction) and as sustained under the power cap, with the
+    clocks seen while timing (long runs of dense MMAs drive the part to its power
+    cap, where the SM clock drops below its maximum)."""
+    tf = flops / (ms * 1e-3) / 1e12
+    _, _, _, sustained = measured_peaks_all()
+    res = {"workload": name, "ms_per_call": round(ms, 4), "flops": flops,
+           "TFLOP_per_s": round(tf, 1), "frac_of_measured_bf16": round(tf / peak_tflops, 4),
+           "tiles": tiles, "clocks": clocks}
+    if sustained:
+        res["frac_of_measured_bf16_sustained"] = round(tf / sustained, 4)
+    return res
+
+
 def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1, dtype=None, head_dim=128):
     """Ragged causal prefill; FLOPs = 4 * D per unmasked (query, key) pair per query head
     (with a window, row i of a request keeps min(i + 1, window_left + 1) keys)."""
@@ -417,23 +464,13 @@ def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1, dtype=None
                                       window_left=window_left, dtype=inp["q"].dtype,
                                       head_dim=head_dim)
         out = torch.empty_like(inp["q"])
-        for _ in range(warmup):
-            api.batch_prefill_run(plan, inp["q"], inp["k"], inp["v"], out=out)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(steps):
-            api.batch_prefill_run(plan, inp["q"], inp["k"], inp["v"], out=out)
-        e1.record()
-        torch.cuda.synchronize()
+        ms, clocks = time_prefill_calls(
+            lambda: api.batch_prefill_run(plan, inp["q"], inp["k"], inp["v"], out=out), steps,
+            warmup)
         plan.check()
-        ms = e0.elapsed_time(e1) / steps
     except Exception as exc:   # reported, not hidden: the line says why there is no number
         return {"workload": name, "status": f"not measured: {exc}", "flops": flops}
-    tf = flops / (ms * 1e-3) / 1e12
-    return {"workload": name, "ms_per_call": round(ms, 4), "flops": flops,
-            "TFLOP_per_s": round(tf, 1), "frac_of_measured_bf16": round(tf / peak_tflops, 4),
-            "tiles": plan.num_tiles}
+    return prefill_result(name, ms, flops, peak_tflops, plan.num_tiles, clocks)
 
 
 def measure_prefill_fixed(seed, steps, warmup, peak_tflops, variable_window=False):
@@ -463,21 +500,10 @@ def measure_prefill_fixed(seed, steps, warmup, peak_tflops, variable_window=Fals
     flops = 4 * 128 * pairs * Hq
     plan = api.batch_prefill_plan_fixed(B, S, S, num_qo_heads=Hq, num_kv_heads=Hkv, **kw)
     out = torch.empty_like(q)
-    for _ in range(warmup):
-        api.batch_prefill_run(plan, q, k, v, out=out)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        api.batch_prefill_run(plan, q, k, v, out=out)
-    e1.record()
-    torch.cuda.synchronize()
+    ms, clocks = time_prefill_calls(lambda: api.batch_prefill_run(plan, q, k, v, out=out), steps,
+                                    warmup)
     plan.check()
-    ms = e0.elapsed_time(e1) / steps
-    tf = flops / (ms * 1e-3) / 1e12
-    return {"workload": name, "ms_per_call": round(ms, 4), "flops": flops,
-            "TFLOP_per_s": round(tf, 1), "frac_of_measured_bf16": round(tf / peak_tflops, 4),
-            "tiles": plan.num_tiles}
+    return prefill_result(name, ms, flops, peak_tflops, plan.num_tiles, clocks)
 
 
 def _oracle_worker(conn, task):
