@@ -33,7 +33,9 @@ PREFILL_WINDOW = 2047   # sliding-window variant of the ragged prefill (2048 key
 # seed 0, one GB300) from an ncu capture of this same command; the full
 # command and numbers are in profiles/decode_cc_kernel_llama3_8b_full_traffic.md.
 # Other seeds or ranks scale it by their algorithmic K+V bytes.
-NCU_TRAFFIC = {"kernel": "decode_cuda_core_kernel", "kv_bytes": 1128361984,
+# the kernel symbol each decode plan launches
+KERNEL_SYMBOL = {"cuda_core": "decode_cc_kernel", "mma": "decode_mma_kernel"}
+NCU_TRAFFIC = {"kernel": "decode_cc_kernel", "kv_bytes": 1128361984,
                "dram_bytes": 1130908672 + 3318528}
 METRIC = "paged decode effective KV HBM GB/s"
 UNIT = "GB/s"
@@ -379,7 +381,7 @@ def reduce_over_ranks(ms, nbytes, dist=None, device="cpu"):
 def headline_traffic(head):
     """DRAM bytes per headline launch from the ncu capture, scaled to this call's K+V bytes
     (None when the plan runs another kernel than the one captured)."""
-    if f"decode_{head['kernel']}_kernel" != NCU_TRAFFIC["kernel"]:
+    if KERNEL_SYMBOL[head["kernel"]] != NCU_TRAFFIC["kernel"]:
         return None
     return int(round(NCU_TRAFFIC["dram_bytes"] * head["kv_bytes"] / NCU_TRAFFIC["kv_bytes"]))
 
@@ -667,7 +669,7 @@ def main():
                        "kv_bytes_per_call": head["kv_bytes"],
                        "l2": "inputs larger than L2 (each call reads >1 GB of K/V; no flush)",
                        "parallelism": f"replicas x{world} (one batch per GPU)"},
-            "roofline": {"bound": "hbm", "kernel": f"decode_{head['kernel']}_kernel",
+            "roofline": {"bound": "hbm", "kernel": KERNEL_SYMBOL[head["kernel"]],
                          "achieved": round(gbs_kernel, 1), "peak": peak_gbs, "unit": "GB/s",
                          "frac": round(gbs_kernel / peak_gbs, 4), "peak_source": peak_kind,
                          "traffic": headline_traffic(head)},

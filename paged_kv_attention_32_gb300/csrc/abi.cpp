@@ -69,9 +69,40 @@ int upload_decode_plan(pka_plan& p, cudaStream_t stream) {
   p.d_reqs = reinterpret_cast<const ReqInfo*>(base + off_reqs);
   p.d_merge_rows = reinterpret_cast<const MergeRow*>(base + off_merge);
   p.d_status = reinterpret_cast<int32_t*>(base + off_status);
-  // Copies from these pageable host vectors are staged before cudaMemcpyAsync
-  // returns, so a later replan may overwrite them; stream order keeps the
-  // upload behind runs already queued on the same stream.
+  // One asynchronous copy from a pinned image of the buffer.  The image is
+  // rewritten only after the copy that last read it has completed (stage_done);
+  // stream order keeps the upload behind runs already queued on the same stream.
+  if (p.host_stage != nullptr && p.stage_done != nullptr)
+    PKA_CUDA_TRY(cudaEventSynchronize(p.stage_done), "cudaEventSynchronize(plan upload)");
+  if (p.host_stage == nullptr || total > p.host_capacity) {
+    if (p.host_stage != nullptr) {
+      PKA_CUDA_TRY(cudaFreeHost(p.host_stage), "cudaFreeHost(plan image)");
+      p.host_stage = nullptr;
+      p.host_capacity = 0;
+    }
+    if (cudaMallocHost(&p.host_stage, p.dev_capacity) == cudaSuccess) {
+      p.host_capacity = p.dev_capacity;
+    } else {
+      (void)cudaGetLastError();   // no pinned memory: copy from the pageable vectors
+      p.host_stage = nullptr;
+    }
+  }
+  if (p.host_stage != nullptr) {
+    uint8_t* img = static_cast<uint8_t*>(p.host_stage);
+    if (n_items) std::memcpy(img, p.items.data(), n_items);
+    std::memcpy(img + off_reqs, p.reqs.data(), n_reqs);
+    if (n_merge) std::memcpy(img + off_merge, p.merge_rows.data(), n_merge);
+    std::memset(img + off_status, 0, 256);
+    PKA_CUDA_TRY(cudaMemcpyAsync(base, img, total, cudaMemcpyHostToDevice, stream),
+                 "cudaMemcpyAsync(plan)");
+    if (p.stage_done == nullptr)
+      PKA_CUDA_TRY(cudaEventCreateWithFlags(&p.stage_done, cudaEventDisableTiming),
+                   "cudaEventCreate(plan upload)");
+    PKA_CUDA_TRY(cudaEventRecord(p.stage_done, stream), "cudaEventRecord(plan upload)");
+    return PKA_OK;
+  }
+  // Copies from pageable host vectors are staged before cudaMemcpyAsync returns,
+  // so a later replan may overwrite them.
   if (n_items)
     PKA_CUDA_TRY(cudaMemcpyAsync(base, p.items.data(), n_items, cudaMemcpyHostToDevice, stream),
                  "cudaMemcpyAsync(plan items)");
@@ -195,7 +226,12 @@ int paged_decode_plan_update(pka_plan* p, int32_t batch_size, const int32_t* seq
   fresh.dev_buf = p->dev_buf;
   fresh.dev_capacity = p->dev_capacity;
   fresh.device = p->device;
+  fresh.host_stage = p->host_stage;
+  fresh.host_capacity = p->host_capacity;
+  fresh.stage_done = p->stage_done;
   p->dev_buf = nullptr;
+  p->host_stage = nullptr;
+  p->stage_done = nullptr;
   *p = std::move(fresh);
   if (!(p->desc.flags & PKA_PLAN_HOST_ONLY)) {
     rc = upload_decode_plan(*p, static_cast<cudaStream_t>(stream));
@@ -207,6 +243,11 @@ int paged_decode_plan_update(pka_plan* p, int32_t batch_size, const int32_t* seq
 
 void paged_decode_plan_destroy(pka_plan* plan) {
   if (plan == nullptr) return;
+  if (plan->stage_done != nullptr) {
+    cudaEventSynchronize(plan->stage_done);   // the image is not freed under a pending copy
+    cudaEventDestroy(plan->stage_done);
+  }
+  if (plan->host_stage != nullptr) cudaFreeHost(plan->host_stage);
   if (plan->dev_buf != nullptr) cudaFree(plan->dev_buf);
   delete plan;
 }

@@ -412,7 +412,8 @@ int launch_cc(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMap
                       (size_t)kWarps * kUnit * R * sizeof(float) + kWarps * NSTAGE * 8;
   static_assert(kWarps * R * 130 * 4 <= kWarps * NSTAGE * kStageBytes, "combine area too small");
   auto kern = decode_cc_kernel<R, NSTAGE, F16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<uint64_t> smem_set{0};   // devices whose limit this launcher raised
+  cudaError_t e = set_smem_once(kern, (int)smem, smem_set);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_cc)");
   kern<<<args.num_items, 128, smem, stream>>>(args, kmap, vmap);
   e = cudaGetLastError();

@@ -152,7 +152,8 @@ int launch_mma(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMa
   static_assert(kWarps * 16 * (kMmaCombStride + 2) * 4 <= kWarps * NSTAGE * kStageBytes,
                 "merge buffer does not fit in the stage area");
   auto kern = decode_mma_kernel<NSTAGE, F16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<uint64_t> smem_set{0};   // devices whose limit this launcher raised
+  cudaError_t e = set_smem_once(kern, (int)smem, smem_set);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_mma)");
   const int mt = (args.rows_per_cta + 15) / 16;
   const int64_t grid = (int64_t)args.num_items * mt;

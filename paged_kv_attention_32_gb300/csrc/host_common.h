@@ -2,6 +2,7 @@
 // the thread-local last-error message and CUDA error mapping.
 #pragma once
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -20,6 +21,21 @@ int fail(int code, const char* fmt, ...);
 void clear_error();
 
 // Maps a CUDA runtime error to PKA_ERR_CUDA with a message naming `what`.
+// Raises a kernel's dynamic shared memory limit once per device: `done` is the
+// calling launcher's own bit set (devices 0-63; a higher device sets it on
+// every launch).  The attribute stays set for the life of the process.
+template <typename Kernel>
+inline cudaError_t set_smem_once(Kernel kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 inline int cuda_fail(cudaError_t e, const char* what) {
   return fail(PKA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }

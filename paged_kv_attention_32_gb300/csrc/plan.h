@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <vector>
 
+#include <cuda_runtime.h>
+
 #include "pka.h"
 
 namespace pka {
@@ -95,6 +97,11 @@ struct pka_plan {
   const pka::MergeRow* d_merge_rows = nullptr;
   int32_t* d_status = nullptr;
   int device = -1;
+  // pinned host image of dev_buf: a replan writes it and uploads it with one
+  // asynchronous copy; stage_done marks when that copy has read it
+  void* host_stage = nullptr;
+  size_t host_capacity = 0;
+  cudaEvent_t stage_done = nullptr;
 };
 
 namespace pka {

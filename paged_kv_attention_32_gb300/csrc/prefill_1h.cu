@@ -298,7 +298,8 @@ int launch_1h(const pka_prefill_plan& plan, const PrefillArgs& args, const CUten
   auto kern = plan.desc.dtype == PKA_DTYPE_F16 ? prefill_1h_kernel<D, true>
                                                : prefill_1h_kernel<D, false>;
   const int smem = (int)Geo<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<uint64_t> smem_set[2];   // per input type: devices whose limit was raised
+  cudaError_t e = set_smem_once(kern, smem, smem_set[plan.desc.dtype == PKA_DTYPE_F16]);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_1h)");
   kern<<<args.num_tiles, kThreads, smem, stream>>>(args, qmap, kmap, vmap);
   e = cudaGetLastError();
