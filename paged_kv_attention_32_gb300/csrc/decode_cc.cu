@@ -171,11 +171,16 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
       ++tbatch;
     }
     const int pid = __shfl_sync(FULL, tcur, k & 31);
-    if (lane == 0) {
-      const int u = unit0 + warp + k * kWarps;
-      const int slot = (u % upp) * kUnit;
-      const int st = k % NSTAGE;
-      const uint32_t dst = stage_u32 + st * kStageBytes, bar = bar_u32 + st * 8;
+    const int u = unit0 + warp + k * kWarps;
+    const int slot = (u % upp) * kUnit;
+    const int st = k % NSTAGE;
+    const uint32_t dst = stage_u32 + st * kStageBytes, bar = bar_u32 + st * 8;
+    if constexpr (!F16) {
+      tma_load_kv_pair_elect(dst, dst + 2 * kBoxBytes, &tmk, &tmv, bar, kStageBytes, slot, hk,
+                             pid);
+    } else if (lane == 0) {
+      // measured: the fp16 instantiation runs ~1 % faster with the copies issued
+      // as separate statements from lane 0 (the bf16 one ~0.7 % slower)
       mbar_arrive_expect_tx(bar, kStageBytes);
       tma_load_kv_unit(dst, &tmk, bar, slot, hk, pid);
       tma_load_kv_unit(dst + 2 * kBoxBytes, &tmv, bar, slot, hk, pid);

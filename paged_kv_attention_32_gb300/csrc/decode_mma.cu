@@ -107,15 +107,11 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
       ++tbatch;
     }
     const int pid = __shfl_sync(FULL, tcur, k & 31);
-    if (lane == 0) {
-      const int u = unit0 + warp + k * kWarps;
-      const int slot = (u % upp) * kUnit;
-      const int st = k % NSTAGE;
-      const uint32_t dst = stage_u32 + st * kStageBytes, bar = bar_u32 + st * 8;
-      mbar_arrive_expect_tx(bar, kStageBytes);
-      tma_load_kv_unit(dst, &tmk, bar, slot, hk, pid);
-      tma_load_kv_unit(dst + 2 * kBoxBytes, &tmv, bar, slot, hk, pid);
-    }
+    const int u = unit0 + warp + k * kWarps;
+    const int slot = (u % upp) * kUnit;
+    const int st = k % NSTAGE;
+    const uint32_t dst = stage_u32 + st * kStageBytes, bar = bar_u32 + st * 8;
+    tma_load_kv_pair_elect(dst, dst + 2 * kBoxBytes, &tmk, &tmv, bar, kStageBytes, slot, hk, pid);
   };
   const int pre = my_units < NSTAGE ? my_units : NSTAGE;
   for (int k = 0; k < pre; ++k) issue(k);
