@@ -192,13 +192,14 @@ int paged_decode_plan(pka_plan** plan_out, const pka_decode_desc* desc,
                       const int32_t* seq_lens_kv_host, const int32_t* qo_indptr_host,
                       size_t* workspace_bytes_out, void* stream);
 
-/* Free a plan (NULL is ignored).  Must not be called while a run that uses
- * the plan may still execute on the device. */
 /*
  * Re-plan an existing plan for a new batch (new lengths, query offsets and
  * batch size; every other descriptor field stays), as a serving loop does
  * each step.  The plan's device buffer is reused when the new work list fits
  * (no allocation, no device synchronisation), else reallocated with headroom.
+ * The new work list goes up in one asynchronous copy from a pinned host image
+ * that the plan keeps; the call first waits (on the host) until the previous
+ * upload of this plan has read that image, which it normally has long since.
  * The upload is ordered on `stream` after earlier runs queued there; a run
  * on another stream must be ordered by the caller.  On error the plan is
  * unchanged.  workspace_bytes_out as for paged_decode_plan.
@@ -207,6 +208,8 @@ int paged_decode_plan_update(pka_plan* plan, int32_t batch_size, const int32_t* 
                              const int32_t* qo_indptr_host, size_t* workspace_bytes_out,
                              void* stream);
 
+/* Free a plan (NULL is ignored).  Must not be called while a run that uses
+ * the plan may still execute on the device; waits for the plan's last upload. */
 void paged_decode_plan_destroy(pka_plan* plan);
 
 /* Fill `info` with the plan's summary. */
