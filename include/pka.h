@@ -19,6 +19,9 @@
  *   paged_kv_gather
  *       test hook: copies paged K or V rows to a dense buffer through the same
  *       page addressing the decode kernels use.
+ *   pka_wait_timeout_probe
+ *       test hook: runs the kernels' bounded wait until it gives up, so that
+ *       the timeout report can be checked without faulting or hanging.
  *
  * Conventions shared by every entry point
  *   - Return value: PKA_OK (0) or a negative PKA_ERR_* code.  The message of
@@ -432,6 +435,18 @@ int paged_kv_gather(const void* pages, int64_t num_pages, int64_t stride_page,
                     int32_t head_dim, const int32_t* block_tables, int64_t bt_row_stride,
                     int32_t request, int32_t kv_head, int32_t tok_begin, int32_t tok_end,
                     void* out, void* stream);
+
+/*
+ * Exercise the bounded wait every kernel uses: one warp waits on a barrier
+ * phase that nothing completes, gives up after limit_ns nanoseconds (1e6 to
+ * 2e9), ORs the timeout bit (1) into a status word and returns; the context
+ * stays usable.  The status word is the decode plan's own when `plan` is not
+ * NULL (paged_decode_plan_check then returns PKA_ERR_DEVICE_TIMEOUT, and
+ * clears it), else *status_dev (device int32, caller-owned).  Does not
+ * synchronise.
+ */
+int pka_wait_timeout_probe(const pka_plan* plan, int32_t* status_dev, int64_t limit_ns,
+                           void* stream);
 
 #ifdef __cplusplus
 }

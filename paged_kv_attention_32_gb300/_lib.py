@@ -33,7 +33,7 @@ EXPORTED = (
     "attn_merge_lse",
     "batch_prefill_plan", "batch_prefill_plan_fixed", "batch_prefill_plan_destroy", "batch_prefill_plan_check",
     "batch_prefill_run",
-    "paged_kv_gather",
+    "paged_kv_gather", "pka_wait_timeout_probe",
 )
 
 
@@ -104,6 +104,7 @@ _SIGS = {
                                          _vp, _sz, _vp]),
     "paged_kv_gather": (ctypes.c_int, [_vp, _i64, _i64, _i64, _i32, _i32, _i32, _vp, _i64, _i32,
                                        _i32, _i32, _i32, _vp, _vp]),
+    "pka_wait_timeout_probe": (ctypes.c_int, [_vp, _vp, _i64, _vp]),
 }
 
 _lib = None

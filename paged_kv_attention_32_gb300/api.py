@@ -294,3 +294,16 @@ def paged_kv_gather(pages, block_tables, request, kv_head, tok_begin, tok_end, o
 
 def default_scale(head_dim=128):
     return 1.0 / math.sqrt(head_dim)
+
+
+def wait_timeout_probe(limit_ns=10_000_000, plan=None, status=None, stream=None):
+    """Run the kernels' bounded wait on a barrier nothing completes until it gives
+    up after ``limit_ns``.  The timeout bit (1) goes into ``plan``'s status word
+    (its ``check()`` then raises) or, without a plan, into ``status`` (a device
+    int32 tensor, made when not given), which is returned."""
+    if plan is None and status is None:
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = L.lib().pka_wait_timeout_probe(plan.handle if plan is not None else None,
+                                        _ptr(status), int(limit_ns), _stream(stream))
+    L.check(rc, "pka_wait_timeout_probe")
+    return status

@@ -549,4 +549,18 @@ int paged_kv_gather(const void* pages, int64_t num_pages, int64_t stride_page,
                              tok_begin, tok_end, out, static_cast<cudaStream_t>(stream));
 }
 
+int pka_wait_timeout_probe(const pka_plan* plan, int32_t* status_dev, int64_t limit_ns,
+                           void* stream) {
+  clear_error();
+  if (plan != nullptr) {
+    PKA_CHECK_ARG(plan->d_status != nullptr, "plan has no device state");
+    status_dev = plan->d_status;
+  }
+  PKA_CHECK_ARG(status_dev != nullptr && aligned(status_dev, 4),
+                "status_dev must be a 4-byte aligned device pointer");
+  PKA_CHECK_ARG(limit_ns >= 1000000 && limit_ns <= 2000000000,
+                "limit_ns must be in [1e6, 2e9] (got %lld)", (long long)limit_ns);
+  return launch_wait_probe((uint64_t)limit_ns, status_dev, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

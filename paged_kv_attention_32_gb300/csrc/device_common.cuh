@@ -65,17 +65,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of the barrier to complete.  Gives up after
-// kWaitLimitNs, OR-ing STATUS_WAIT_TIMEOUT into *status; returns false then.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status) {
+// limit_ns, OR-ing STATUS_WAIT_TIMEOUT into *status; returns false then.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, int32_t* status,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       if (status) atomicOr(status, STATUS_WAIT_TIMEOUT);
       return false;
     }
   }
+}
+
+// Every kernel's wait: mbar_wait_for with the kWaitLimitNs bound.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status) {
+  return mbar_wait_for(bar, parity, status, kWaitLimitNs);
 }
 
 // ---- TMA -------------------------------------------------------------------

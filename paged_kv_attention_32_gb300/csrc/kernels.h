@@ -21,6 +21,10 @@ int launch_merge_states(const float* v_states, const float* s_states, int32_t n,
                         cudaStream_t stream);
 
 // Test hook: paged rows -> dense rows through the decode kernels' addressing.
+// One warp waiting on a barrier nothing completes, bounded by limit_ns: the
+// timeout bit ends up in *status (device int32).
+int launch_wait_probe(uint64_t limit_ns, int32_t* status, cudaStream_t stream);
+
 int launch_paged_gather(const CUtensorMap& map, const int32_t* block_tables,
                         int64_t bt_row_stride, int32_t page_size, int32_t request,
                         int32_t kv_head, int32_t tok_begin, int32_t tok_end, void* out,

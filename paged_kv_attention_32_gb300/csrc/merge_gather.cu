@@ -98,7 +98,27 @@ paged_gather_kernel(const __grid_constant__ CUtensorMap map, const int32_t* __re
   }
 }
 
+// One warp waits on phase 0 of an mbarrier that nothing arrives on, through
+// the same bounded wait every kernel uses, with a bound of limit_ns.
+__global__ void __launch_bounds__(32) wait_probe_kernel(uint64_t limit_ns, int32_t* status) {
+  __shared__ uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  (void)__all_sync(0xffffffffu, mbar_wait_for(b, 0, status, limit_ns));
+}
+
 }  // namespace
+
+int launch_wait_probe(uint64_t limit_ns, int32_t* status, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "wait_probe_kernel launch");
+  return PKA_OK;
+}
 
 int launch_merge_states(const float* v_states, const float* s_states, int32_t n, int32_t s,
                         int32_t h, int32_t d, void* v_out, int32_t out_dtype, float* s_out,
