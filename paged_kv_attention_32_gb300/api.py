@@ -47,6 +47,22 @@ def _check_inputs(plan, *tensors):
             raise ValueError(f"the plan was made for {want} inputs, got {t.dtype}")
 
 
+def _check_layout(q, k, v, out=None, lse=None, paged=False):
+    """What the C ABI assumes but cannot see: the head dim dense (stride 1), V
+    laid out like K (the ABI takes one set of K/V strides), a paged pool's slots
+    dense rows of D, and contiguous outputs."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.stride(-1) != 1:
+            raise ValueError(f"{name} must have a dense last (head) dimension")
+    if tuple(v.stride()) != tuple(k.stride()) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("v must have the shape and strides of k")
+    if paged and k.stride(2) != k.shape[3]:
+        raise ValueError("each page's slots must be dense rows of head_dim elements")
+    for name, t in (("out", out), ("lse", lse)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
 def _host_i32(x):
     """Contiguous host int32 array (kept alive by the caller) and its pointer."""
     if x is None:
@@ -140,6 +156,9 @@ def paged_decode_run(plan, q, k_pages, v_pages, block_tables, seq_lens_kv=None, 
                      out=None, lse=None, workspace=None, stream=None):
     """Run a planned decode; returns ``out`` (and ``lse`` when the plan returns it)."""
     _check_inputs(plan, q, k_pages, v_pages)
+    _check_layout(q, k_pages, v_pages, out, lse, paged=True)
+    if block_tables.stride(-1) != 1:
+        raise ValueError("block_tables rows must be dense")
     if out is not None and out.dtype != _TORCH[plan.desc.out_dtype]:
         raise ValueError(f"out must be {_TORCH[plan.desc.out_dtype]} (the plan's out_dtype)")
     total_q, Hq, D = q.shape
@@ -265,6 +284,7 @@ def batch_prefill_run(plan, q, k, v, out=None, lse=None, stream=None):
             return res[0].view(B, Sq, *res[0].shape[1:]), res[1].view(B, Sq, res[1].shape[1])
         return res.view(B, Sq, *res.shape[1:])
     _check_inputs(plan, q, k, v)
+    _check_layout(q, k, v, out, lse)
     if out is not None and out.dtype != _TORCH[plan.desc.out_dtype]:
         raise ValueError(f"out must be {_TORCH[plan.desc.out_dtype]} (the plan's out_dtype)")
     total_q, Hq, D = q.shape

@@ -50,6 +50,24 @@ def _run(lq, lk, Hq, Hkv, causal=True, seed=0, dtype=torch.bfloat16, out_dtype=N
     _check(out, lse, ref_o, ref_l)
 
 
+def test_prefill_fused_qkv_views():
+    """q, k and v as head slices of one fused [total, Hq + 2 Hkv, D] projection output
+    (strided tokens, K and V at other base pointers with the same strides)."""
+    lens = [70, 129, 3]
+    qi = _indptr(lens)
+    Hq, Hkv, D = 4, 2, 128
+    qkv = _rand((int(qi[-1]), Hq + 2 * Hkv, D), 91)
+    q, k, v = qkv[:, :Hq], qkv[:, Hq:Hq + Hkv], qkv[:, Hq + Hkv:]
+    plan = api.batch_prefill_plan(qi, qi, num_qo_heads=Hq, num_kv_heads=Hkv, return_lse=True)
+    out, lse = api.batch_prefill_run(plan, q, k, v)
+    torch.cuda.synchronize()
+    plan.check()
+    ref_o, ref_l = oracle.batch_prefill(wl.bf16_bits(q.contiguous()), wl.bf16_bits(k.contiguous()),
+                                        wl.bf16_bits(v.contiguous()), qi.numpy(), qi.numpy(), Hkv,
+                                        causal=True)
+    _check(out, lse, ref_o, ref_l)
+
+
 def test_prefill_smallest():
     _run([1, 5, 130], [1, 5, 130], 4, 2)
 
