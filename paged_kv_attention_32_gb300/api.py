@@ -14,15 +14,16 @@ from . import _lib as L
 
 
 def _stream(stream):
+    """cudaStream_t as an int (ctypes passes ints to void* parameters as is)."""
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
-        return ctypes.c_void_p(stream.cuda_stream)
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
 
 
 def _ptr(t):
-    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 _DTYPES = {torch.bfloat16: L.PKA_DTYPE_BF16, torch.float16: L.PKA_DTYPE_F16,
@@ -67,7 +68,11 @@ def _host_i32(x):
     """Contiguous host int32 array (kept alive by the caller) and its pointer."""
     if x is None:
         return None, None
-    t = torch.as_tensor(x).to(device="cpu", dtype=torch.int32).contiguous()
+    if (isinstance(x, torch.Tensor) and x.dtype == torch.int32 and x.device.type == "cpu"
+            and x.is_contiguous()):
+        t = x
+    else:
+        t = torch.as_tensor(x).to(device="cpu", dtype=torch.int32).contiguous()
     return t, ctypes.cast(t.data_ptr(), L._pi32)
 
 
