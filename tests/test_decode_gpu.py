@@ -249,3 +249,15 @@ def test_decode_full_size_sampled(name):
     rows = row_mask(inp, reqs)
     assert_close(out, lse, ref_o, ref_l, rows=rows)
     assert torch.isfinite(out.float()).all()
+
+
+def test_decode_many_short_requests():
+    """2048 requests of 1-64 keys (4096 CTAs, ragged single pages), sampled requests."""
+    w = wl.shrink(wl.TINY_DECODE, batch=2048, kv_len_range=(1, 64), pool_pages=2048 * 4 + 64,
+                  table_width=4)
+    inp = wl.make_decode_inputs(w, seed=31, device=DEV)
+    out, lse, plan = run_decode(inp, return_lse=True)
+    reqs = [0, 1, 777, 1500, 2047]
+    ref_o, ref_l = oracle_decode(inp, requests=reqs)
+    assert_close(out, lse, ref_o, ref_l, rows=row_mask(inp, reqs))
+    assert torch.isfinite(out.float()).all()

@@ -185,13 +185,18 @@ def test_prefill_empty_and_single_row_requests(D):
     _run([0, 1, 0, 200, 1], [0, 1, 0, 230, 5], 4, 2, seed=90, D=D)
 
 
-def test_prefill_full_size_sampled():
-    """The ragged prefill workload at full size (as bench.py times it), sampled rows."""
+@pytest.mark.parametrize("D", [128, 256])
+def test_prefill_full_size_sampled(D):
+    """The ragged prefill workload at full size (as bench.py times it, head_dim 128 and
+    the 256 line), sampled rows."""
+    import dataclasses
     w = wl.RAGGED_PREFILL
+    if D != w.head_dim:
+        w = dataclasses.replace(w, head_dim=D)
     inp = wl.make_prefill_inputs(w, seed=0, device="cuda")
     ind = inp["qo_indptr"].cpu()
     plan = api.batch_prefill_plan(ind, ind, num_qo_heads=w.num_qo_heads,
-                                  num_kv_heads=w.num_kv_heads, return_lse=True)
+                                  num_kv_heads=w.num_kv_heads, return_lse=True, head_dim=D)
     out, lse = api.batch_prefill_run(plan, inp["q"], inp["k"], inp["v"])
     torch.cuda.synchronize()
     plan.check()
