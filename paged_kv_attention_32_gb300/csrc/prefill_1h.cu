@@ -55,6 +55,12 @@ struct Geo {
   static constexpr int kMinBlocks = D == 128 ? 2 : 1;   // 2 x 97 KB, 2 x 256 TMEM columns
 };
 
+// mbarriers, two of each per stage or S buffer (tile j uses j & 1).  A parity
+// wait is only correct when the barrier has completed the phase before the
+// awaited one, and every wait here keeps to that: K/V full/empty and S/P are
+// waited in order by one consumer each; the O-done wait for P V of tile j - 1
+// (lazy rescale) or n_kv - 1 (epilogue) comes after S of tile j, whose QK was
+// issued after P V of tile j - 2, which therefore completed.
 enum {
   B_Q = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 7, B_SFULL = 9, B_PFULL = 11,
   B_ODONE = 13, B_MMADONE = 15, B_COUNT = 16
