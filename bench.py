@@ -475,10 +475,11 @@ def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1, dtype=None
     return prefill_result(name, ms, flops, peak_tflops, plan.num_tiles, clocks)
 
 
-def measure_prefill_fixed(seed, steps, warmup, peak_tflops, variable_window=False):
-    """Fixed-shape [B, S, H, D] prefill, B=4, S=4096, Hq=32, Hkv=8: causal, or
-    variable_window with row i of each request seeing keys [s_i, i], s_i uniform in
-    [max(0, i - 2047), i] (seeded).  FLOPs = 4 * D per visible (query, key) pair per head."""
+def measure_prefill_fixed(seed, steps, warmup, peak_tflops, variable_window=False, dense=False):
+    """Fixed-shape [B, S, H, D] prefill, B=4, S=4096, Hq=32, Hkv=8: causal, dense (every
+    row sees every key), or variable_window with row i of each request seeing keys
+    [s_i, i], s_i uniform in [max(0, i - 2047), i] (seeded).  FLOPs = 4 * D per visible
+    (query, key) pair per head."""
     import numpy as np
     import torch
     from paged_kv_attention_32_gb300 import api
@@ -489,6 +490,10 @@ def measure_prefill_fixed(seed, steps, warmup, peak_tflops, variable_window=Fals
     v = torch.randn((B, S, Hkv, 128), generator=g, device="cuda", dtype=torch.bfloat16)
     kw, name = {}, f"fixed-shape causal prefill B={B} S={S} Hq={Hq} Hkv={Hkv} D=128"
     pairs = B * S * (S + 1) // 2
+    if dense:
+        kw = dict(mask_type="dense")
+        pairs = B * S * S
+        name = f"fixed-shape dense prefill B={B} S={S} Hq={Hq} Hkv={Hkv} D=128"
     if variable_window:
         rng = np.random.default_rng(seed + 8)
         i = np.arange(S)
@@ -506,6 +511,36 @@ def measure_prefill_fixed(seed, steps, warmup, peak_tflops, variable_window=Fals
                                     warmup)
     plan.check()
     return prefill_result(name, ms, flops, peak_tflops, plan.num_tiles, clocks)
+
+
+def measure_merge(seed, steps, warmup, peak_gbs):
+    """Standalone attn_merge_lse: N=8 partial states of S=8192 rows, H=32 heads, D=128
+    (fp32 V [N, S, H, D] and base-2 LSE [N, S, H]) merged into bf16 O and an fp32 LSE.
+    Algorithmic bytes = every partial read once + the outputs written once."""
+    import torch
+    from paged_kv_attention_32_gb300 import api
+    N, S, H, D = 8, 8192, 32, 128
+    g = torch.Generator(device="cuda").manual_seed(seed + 9)
+    vs = torch.randn((N, S, H, D), generator=g, device="cuda", dtype=torch.float32)
+    ss = torch.randn((N, S, H), generator=g, device="cuda", dtype=torch.float32)
+    v_out = torch.empty((S, H, D), dtype=torch.bfloat16, device="cuda")
+    s_out = torch.empty((S, H), dtype=torch.float32, device="cuda")
+    for _ in range(warmup):
+        api.attn_merge_lse(vs, ss, v_out=v_out, s_out=s_out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        api.attn_merge_lse(vs, ss, v_out=v_out, s_out=s_out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = vs.numel() * 4 + ss.numel() * 4 + v_out.numel() * 2 + s_out.numel() * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"attn_merge_lse N={N} S={S} H={H} D={D} fp32 states -> bf16",
+            "ms_per_call": round(ms, 5), "bytes": nbytes, "GB_per_s": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak_gbs, 4),
+            "l2": "inputs (1.07 GB) larger than L2"}
 
 
 def _oracle_worker(conn, task):
@@ -708,6 +743,10 @@ def main():
                                                 head_dim=256)
         extra["prefill_variable_window"] = measure_prefill_fixed(
             args.seed, max(3, args.steps // 4), 3, peak_tf, variable_window=True)
+        extra["prefill_fixed_dense"] = measure_prefill_fixed(
+            args.seed, max(3, args.steps // 4), 3, peak_tf, dense=True)
+        extra["merge_lse"] = measure_merge(args.seed, max(5, args.steps // 2), max(3, args.warmup),
+                                           peak_gbs)
         line["decode_headline"] = head
         line["other_workloads"] = extra
     if rank == 0:
