@@ -8,6 +8,8 @@
 #include <new>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "host_common.h"
 #include "kernels.h"
 #include "plan.h"
@@ -41,6 +43,15 @@ using namespace pka;
 namespace {
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+// An NVTX range over an entry point, so that the plan and run calls show up by
+// name on a profiler's timeline (a no-op call when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -190,6 +201,7 @@ const char* pka_version(void) { return "pka 0.1.0 (sm_103a)"; }
 int paged_decode_plan(pka_plan** plan_out, const pka_decode_desc* desc,
                       const int32_t* seq_lens_kv_host, const int32_t* qo_indptr_host,
                       size_t* workspace_bytes_out, void* stream) {
+  NvtxRange nvtx_range("pka::paged_decode_plan");
   clear_error();
   PKA_CHECK_ARG(plan_out != nullptr && desc != nullptr, "plan_out and desc must not be NULL");
   *plan_out = nullptr;
@@ -210,6 +222,7 @@ int paged_decode_plan(pka_plan** plan_out, const pka_decode_desc* desc,
 int paged_decode_plan_update(pka_plan* p, int32_t batch_size, const int32_t* seq_lens_kv_host,
                              const int32_t* qo_indptr_host, size_t* workspace_bytes_out,
                              void* stream) {
+  NvtxRange nvtx_range("pka::paged_decode_plan_update");
   clear_error();
   PKA_CHECK_ARG(p != nullptr, "plan must not be NULL");
   pka_decode_desc d = p->desc;
@@ -300,6 +313,7 @@ int paged_decode_run(const pka_plan* p, const void* q, int64_t q_stride_tok,
                      const int32_t* block_tables, int64_t bt_row_stride,
                      const int32_t* seq_lens_kv_dev, const float* sinks, void* out, float* lse,
                      void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("pka::paged_decode_run");
   clear_error();
   PKA_CHECK_ARG(p != nullptr, "plan must not be NULL");
   PKA_CHECK_ARG(p->dev_buf != nullptr, "plan was built with PKA_PLAN_HOST_ONLY and cannot run");
@@ -381,6 +395,7 @@ int paged_decode_plan_check(const pka_plan* p, void* stream) {
 int attn_merge_lse(const float* v_states, const float* s_states, int32_t num_states,
                    int32_t num_rows, int32_t num_heads, int32_t head_dim, void* v_out,
                    int32_t out_dtype, float* s_out, void* stream) {
+  NvtxRange nvtx_range("pka::attn_merge_lse");
   clear_error();
   PKA_CHECK_ARG(v_states && s_states && v_out, "v_states, s_states and v_out must not be NULL");
   PKA_CHECK_ARG(num_states >= 1, "num_states must be >= 1");
@@ -402,6 +417,7 @@ int attn_merge_lse(const float* v_states, const float* s_states, int32_t num_sta
 int batch_prefill_plan(pka_prefill_plan** plan_out, const pka_prefill_desc* desc,
                        const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
                        size_t* workspace_bytes_out, int32_t* num_tiles_out, void* stream) {
+  NvtxRange nvtx_range("pka::batch_prefill_plan");
   clear_error();
   PKA_CHECK_ARG(plan_out != nullptr && desc != nullptr, "plan_out and desc must not be NULL");
   *plan_out = nullptr;
@@ -424,6 +440,7 @@ int batch_prefill_plan_fixed(pka_prefill_plan** plan_out, const pka_prefill_desc
                              int32_t seq_len_q, int32_t seq_len_kv,
                              const int32_t* window_starts_host, const int32_t* window_ends_host,
                              size_t* workspace_bytes_out, int32_t* num_tiles_out, void* stream) {
+  NvtxRange nvtx_range("pka::batch_prefill_plan_fixed");
   clear_error();
   PKA_CHECK_ARG(plan_out != nullptr && desc != nullptr, "plan_out and desc must not be NULL");
   *plan_out = nullptr;
@@ -462,6 +479,7 @@ int batch_prefill_run(const pka_prefill_plan* p, const void* q, int64_t q_stride
                       int64_t q_stride_head, const void* k, const void* v, int64_t kv_stride_tok,
                       int64_t kv_stride_head, void* out, float* lse, void* workspace,
                       size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("pka::batch_prefill_run");
   clear_error();
   (void)workspace;
   (void)workspace_bytes;

@@ -7,6 +7,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "host_common.h"
 #include "kernels.h"
 #include "plan.h"
@@ -54,6 +56,8 @@ extern "C" int paged_decode_run_noalloc(const pka_plan* p, const void* q, int64_
                                         int64_t kv_stride_head, const int32_t* block_tables,
                                         int64_t bt_row_stride, const int32_t* seq_lens_kv_dev,
                                         const float* sinks, void* out, float* lse, void* stream) {
+  nvtxRangePushA("pka::paged_decode_run_noalloc");
+  struct PopOnExit { ~PopOnExit() { nvtxRangePop(); } } nvtx_pop;
   clear_error();
   PKA_CHECK_ARG(p != nullptr, "plan must not be NULL");
   PKA_CHECK_ARG(q && k_pages && v_pages && block_tables && out,
