@@ -16,6 +16,8 @@
  *   batch_prefill_plan / batch_prefill_run
  *       packed ragged causal context attention:
  *       "flashinfer.attention.prims_ts.batch_prefill".
+ *   paged_decode_check_tables
+ *       validation of the block-table entries a decode run reads.
  *   paged_kv_gather
  *       test hook: copies paged K or V rows to a dense buffer through the same
  *       page addressing the decode kernels use.
@@ -57,7 +59,7 @@ extern "C" {
 #define PKA_ERR_UNSUPPORTED (-2)          /* valid on the pages, not built here        */
 #define PKA_ERR_WORKSPACE_TOO_SMALL (-3)  /* workspace_bytes below the plan's need     */
 #define PKA_ERR_CUDA (-4)                 /* a CUDA runtime/driver call failed         */
-#define PKA_ERR_DEVICE_BOUNDS (-5)        /* reserved: device-side bounds report       */
+#define PKA_ERR_DEVICE_BOUNDS (-5)        /* a block-table entry outside the pool      */
 #define PKA_ERR_DEVICE_TIMEOUT (-6)       /* a kernel gave up on a bounded wait        */
 
 /* ---- enums ------------------------------------------------------------- */
@@ -271,11 +273,28 @@ int paged_decode_run(const pka_plan* plan, const void* q, int64_t q_stride_tok,
 
 /*
  * Wait for `stream`, then read and clear the plan's device status word, which
- * kernels set instead of trapping: returns PKA_OK, or PKA_ERR_DEVICE_TIMEOUT
- * when some kernel of an earlier run gave up on a bounded (2 s) wait -- the
- * outputs of that run are then not valid.  Synchronises; not for capture.
+ * kernels set instead of trapping: returns PKA_OK; PKA_ERR_DEVICE_TIMEOUT when
+ * some kernel of an earlier run gave up on a bounded (2 s) wait (the outputs
+ * of that run are then not valid); or PKA_ERR_DEVICE_BOUNDS when
+ * paged_decode_check_tables found a block-table entry outside [0, num_pages).
+ * Synchronises; not for capture.
  */
 int paged_decode_plan_check(const pka_plan* plan, void* stream);
+
+/*
+ * Validate, on the device, the block-table entries that paged_decode_run with
+ * this plan would read: for every request, the pages its visited keys lie in
+ * (the window's start on; up to the live length from seq_lens_kv_dev when the
+ * plan does not freeze the lengths, which may then be NULL only if frozen).
+ * An entry outside [0, num_pages) sets the plan's status word, which the next
+ * paged_decode_plan_check reports as PKA_ERR_DEVICE_BOUNDS.  A run never reads
+ * outside the pools: an out-of-range entry's copy reads zeros (TMA bounds), so
+ * this check is what makes such a table visible.  One small launch, reading
+ * only the entries; allocates nothing; does not synchronise.
+ */
+int paged_decode_check_tables(const pka_plan* plan, const int32_t* block_tables,
+                              int64_t bt_row_stride, const int32_t* seq_lens_kv_dev,
+                              void* stream);
 
 /*
  * paged_decode_run without any device allocation.  The pages have no

@@ -29,6 +29,7 @@ EXPORTED = (
     "paged_decode_plan", "paged_decode_plan_update", "paged_decode_plan_destroy",
     "paged_decode_plan_info",
     "paged_decode_plan_export", "paged_decode_run", "paged_decode_plan_check",
+    "paged_decode_check_tables",
     "paged_decode_run_noalloc",
     "attn_merge_lse",
     "batch_prefill_plan", "batch_prefill_plan_fixed", "batch_prefill_plan_destroy", "batch_prefill_plan_check",
@@ -90,6 +91,7 @@ _SIGS = {
     "paged_decode_run": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _i64,
                                         _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "paged_decode_plan_check": (ctypes.c_int, [_vp, _vp]),
+    "paged_decode_check_tables": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp]),
     "paged_decode_run_noalloc": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _vp,
                                                 _i64, _vp, _vp, _vp, _vp, _vp]),
     "attn_merge_lse": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]),

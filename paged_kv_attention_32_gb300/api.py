@@ -119,8 +119,19 @@ class DecodePlan:
         return self
 
     def check(self, stream=None):
-        """Synchronise and read the device status word (raises on a kernel timeout)."""
+        """Synchronise and read the device status word (raises on a kernel timeout, or
+        on a bad block-table entry found by ``check_tables``)."""
         L.check(L.lib().paged_decode_plan_check(self.handle, _stream(stream)), "plan_check")
+
+    def check_tables(self, block_tables, seq_lens_kv=None, stream=None):
+        """Validate on the device the block-table entries a run of this plan reads
+        (``paged_decode_check_tables``); ``check()`` then raises on a bad one."""
+        if block_tables.stride(-1) != 1:
+            raise ValueError("block_tables rows must be dense")
+        rc = L.lib().paged_decode_check_tables(self.handle, _ptr(block_tables),
+                                               block_tables.stride(0), _ptr(seq_lens_kv),
+                                               _stream(stream))
+        L.check(rc, "paged_decode_check_tables")
 
     def __del__(self):
         h, self.handle = getattr(self, "handle", None), None

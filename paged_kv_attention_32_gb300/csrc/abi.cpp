@@ -183,6 +183,10 @@ int read_status(int32_t* d_status, cudaStream_t stream) {
   PKA_CUDA_TRY(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
   if (st & STATUS_WAIT_TIMEOUT)
     return fail(PKA_ERR_DEVICE_TIMEOUT, "a kernel gave up on a bounded wait (status 0x%x)", st);
+  if (st & STATUS_PAGE_BOUNDS)
+    return fail(PKA_ERR_DEVICE_BOUNDS,
+                "a block-table entry a run would read is outside [0, num_pages) (status 0x%x)",
+                st);
   return PKA_OK;
 }
 
@@ -565,6 +569,23 @@ int paged_kv_gather(const void* pages, int64_t num_pages, int64_t stride_page,
   if (rc != PKA_OK) return rc;
   return launch_paged_gather(map, block_tables, bt_row_stride, page_size, request, kv_head,
                              tok_begin, tok_end, out, static_cast<cudaStream_t>(stream));
+}
+
+int paged_decode_check_tables(const pka_plan* p, const int32_t* block_tables,
+                              int64_t bt_row_stride, const int32_t* seq_lens_kv_dev,
+                              void* stream) {
+  NvtxRange nvtx_range("pka::paged_decode_check_tables");
+  clear_error();
+  PKA_CHECK_ARG(p != nullptr && p->d_status != nullptr, "plan has no device state");
+  PKA_CHECK_ARG(block_tables != nullptr, "block_tables must not be NULL");
+  PKA_CHECK_ARG(bt_row_stride >= p->C, "bt_row_stride (%lld) is smaller than the table width %d",
+                (long long)bt_row_stride, p->C);
+  int rc = check_device(p->device);
+  if (rc != PKA_OK) return rc;
+  return launch_check_tables(p->d_items, (int32_t)p->items.size(), p->d_reqs, block_tables,
+                             bt_row_stride, p->desc.freeze_seq_lens ? nullptr : seq_lens_kv_dev,
+                             p->ps, p->desc.num_pages, p->d_status,
+                             static_cast<cudaStream_t>(stream));
 }
 
 int pka_wait_timeout_probe(const pka_plan* plan, int32_t* status_dev, int64_t limit_ns,

@@ -21,6 +21,13 @@ int launch_merge_states(const float* v_states, const float* s_states, int32_t n,
                         cudaStream_t stream);
 
 // Test hook: paged rows -> dense rows through the decode kernels' addressing.
+// Checks the block-table entries a run of the plan reads (see pka.h,
+// paged_decode_check_tables); a bad one sets STATUS_PAGE_BOUNDS in *status.
+int launch_check_tables(const WorkItem* items, int32_t num_items, const ReqInfo* reqs,
+                        const int32_t* tables, int64_t row_stride, const int32_t* seq_lens_live,
+                        int32_t page_size, int64_t num_pages, int32_t* status,
+                        cudaStream_t stream);
+
 // One warp waiting on a barrier nothing completes, bounded by limit_ns: the
 // timeout bit ends up in *status (device int32).
 int launch_wait_probe(uint64_t limit_ns, int32_t* status, cudaStream_t stream);

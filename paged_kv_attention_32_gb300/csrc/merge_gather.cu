@@ -111,7 +111,43 @@ __global__ void __launch_bounds__(32) wait_probe_kernel(uint64_t limit_ns, int32
   (void)__all_sync(0xffffffffu, mbar_wait_for(b, 0, status, limit_ns));
 }
 
+// The block-table entries a run of the plan reads: for every work item of KV
+// head 0, pages [page_lo, page_hi) of its request, cut at the live length when
+// the plan reads lengths at run time.  An entry outside [0, num_pages) sets
+// STATUS_PAGE_BOUNDS.
+__global__ void __launch_bounds__(128)
+check_tables_kernel(const WorkItem* __restrict__ items, const ReqInfo* __restrict__ reqs,
+                    const int32_t* __restrict__ tables, int64_t row_stride,
+                    const int32_t* __restrict__ seq_lens_live, int32_t page_size,
+                    int32_t num_pages, int32_t* status) {
+  const WorkItem it = items[blockIdx.x];
+  if ((it.head_chunk & 0xffff) != 0) return;
+  int hi = it.page_hi;
+  if (seq_lens_live != nullptr) {
+    const int live = min(__ldg(seq_lens_live + it.request), reqs[it.request].kv_len);
+    hi = min(hi, (max(live, 0) + page_size - 1) / page_size);
+  }
+  const int32_t* row = tables + (int64_t)it.request * row_stride;
+  bool bad = false;
+  for (int pg = it.page_lo + (int)threadIdx.x; pg < hi; pg += blockDim.x)
+    bad |= (unsigned)__ldg(row + pg) >= (unsigned)num_pages;
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, STATUS_PAGE_BOUNDS);
+}
+
 }  // namespace
+
+int launch_check_tables(const WorkItem* items, int32_t num_items, const ReqInfo* reqs,
+                        const int32_t* tables, int64_t row_stride, const int32_t* seq_lens_live,
+                        int32_t page_size, int64_t num_pages, int32_t* status,
+                        cudaStream_t stream) {
+  if (num_items == 0) return PKA_OK;
+  const int32_t np = num_pages > INT32_MAX ? INT32_MAX : (int32_t)num_pages;
+  check_tables_kernel<<<num_items, 128, 0, stream>>>(items, reqs, tables, row_stride,
+                                                     seq_lens_live, page_size, np, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "check_tables_kernel launch");
+  return PKA_OK;
+}
 
 int launch_wait_probe(uint64_t limit_ns, int32_t* status, cudaStream_t stream) {
   wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, status);

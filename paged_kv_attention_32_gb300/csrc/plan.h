@@ -72,6 +72,7 @@ struct DecodeArgs {
 // Device error word bits (OR-ed by kernels, read by paged_decode_status).
 enum : int32_t {
   STATUS_WAIT_TIMEOUT = 1,  // an mbarrier wait hit its iteration limit
+  STATUS_PAGE_BOUNDS = 2,   // paged_decode_check_tables found an entry outside [0, num_pages)
 };
 
 }  // namespace pka
