@@ -125,10 +125,13 @@ const char* pka_version(void);
  *                    "bind a stable runtime seq_lens tensor or let the plan
  *                    retain fixed sequence lengths").
  * num_sms            SM count the planner balances for; 0 = the device's.
- * split_waves        target CTAs = split_waves * num_sms; 0 = default (2).
- * min_chunk_tokens   smallest split chunk in tokens; 0 = default (256).
+ * split_waves        target CTAs = split_waves * num_sms; 0 = the environment
+ *                    variable PKA_SPLIT_WAVES if set to a positive integer, else 2.
+ * min_chunk_tokens   smallest split chunk in tokens; 0 = PKA_MIN_CHUNK_TOKENS,
+ *                    else 256.
  * mma_min_rows       the tensor-core kernel is used when
- *                    (Hq/Hkv) * max_q_len >= mma_min_rows; 0 = default (8).
+ *                    (Hq/Hkv) * max_q_len >= mma_min_rows; 0 = PKA_MMA_MIN_ROWS,
+ *                    else 8.  paged_decode_plan_info reports the values used.
  * flags              PKA_PLAN_HOST_ONLY or 0.
  * out_dtype          PKA_DTYPE_BF16, PKA_DTYPE_F16 or PKA_DTYPE_F32: O of
  *                    paged_decode_run (batch_decode_with_paged_kv_cache,

@@ -18,6 +18,7 @@
 //   - items run longest request first, then chunk, then KV head.
 #include <algorithm>
 #include <climits>
+#include <cstdlib>
 #include <cmath>
 #include <numeric>
 
@@ -32,6 +33,15 @@ constexpr int32_t kDefaultMinChunkTokens = 256;
 constexpr int32_t kDefaultMmaMinRows = 8;
 constexpr int32_t kMaxCudaCoreRows = 8;   // rows one warp of the CUDA-core kernel holds
 constexpr int32_t kMaxMmaRows = 64;       // four m16 tiles
+
+// A positive integer from the environment variable `name`, else `fallback`.
+int32_t env_int(const char* name, int32_t fallback) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || *v == '\0') return fallback;
+  char* end = nullptr;
+  const long x = std::strtol(v, &end, 10);
+  return (end != nullptr && *end == '\0' && x > 0 && x <= INT32_MAX) ? (int32_t)x : fallback;
+}
 }  // namespace
 
 int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* seq,
@@ -61,9 +71,12 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
   if (std::isnan(d.scale)) d.scale = 1.0f / std::sqrt((float)d.head_dim);
   PKA_CHECK_ARG(std::isfinite(d.scale), "scale must be finite");
   PKA_CHECK_ARG(std::isfinite(d.bmm2_scale), "bmm2_scale must be finite");
-  if (d.split_waves <= 0) d.split_waves = kDefaultWaves;
-  if (d.min_chunk_tokens <= 0) d.min_chunk_tokens = kDefaultMinChunkTokens;
-  if (d.mma_min_rows <= 0) d.mma_min_rows = kDefaultMmaMinRows;
+  // a field left 0 takes the environment's value (PKA_SPLIT_WAVES, PKA_MIN_CHUNK_TOKENS,
+  // PKA_MMA_MIN_ROWS), else the default; the plan records what it used
+  if (d.split_waves <= 0) d.split_waves = env_int("PKA_SPLIT_WAVES", kDefaultWaves);
+  if (d.min_chunk_tokens <= 0)
+    d.min_chunk_tokens = env_int("PKA_MIN_CHUNK_TOKENS", kDefaultMinChunkTokens);
+  if (d.mma_min_rows <= 0) d.mma_min_rows = env_int("PKA_MMA_MIN_ROWS", kDefaultMmaMinRows);
   if (d.num_sms <= 0) {
     int dev = 0, sms = 0;
     PKA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");

@@ -95,3 +95,27 @@ def test_plan_update_equals_a_fresh_plan():
     with pytest.raises(L.PkaError):
         p.update([5, 5], qo_indptr=[0, 6, 7])   # kv_len < q_len
     assert p.export() == before
+
+
+def test_planner_tunables_from_the_environment(monkeypatch):
+    """A descriptor field left 0 takes PKA_SPLIT_WAVES / PKA_MIN_CHUNK_TOKENS /
+    PKA_MMA_MIN_ROWS when set to a positive integer; an explicit field wins; a bad
+    value falls back to the default; the plan reports what it used."""
+    import torch
+    from paged_kv_attention_32_gb300 import api
+    seq = torch.tensor([4000, 300, 50], dtype=torch.int32)
+    kw = dict(num_qo_heads=8, num_kv_heads=2, page_size=16, max_pages_per_seq=256,
+              num_pages=1000, q_len=1, num_sms=8, host_only=True)
+    monkeypatch.setenv("PKA_SPLIT_WAVES", "5")
+    monkeypatch.setenv("PKA_MIN_CHUNK_TOKENS", "512")
+    monkeypatch.setenv("PKA_MMA_MIN_ROWS", "4")
+    info = api.paged_decode_plan(seq, **kw).info
+    assert (info["split_waves"], info["min_chunk_tokens"]) == (5, 512)
+    assert info["kernel"] == 1                      # group of 4 rows >= 4: tensor-core kernel
+    info = api.paged_decode_plan(seq, split_waves=3, **kw).info
+    assert info["split_waves"] == 3
+    monkeypatch.setenv("PKA_SPLIT_WAVES", "abc")
+    monkeypatch.setenv("PKA_MIN_CHUNK_TOKENS", "0")
+    monkeypatch.delenv("PKA_MMA_MIN_ROWS")
+    info = api.paged_decode_plan(seq, **kw).info
+    assert (info["split_waves"], info["min_chunk_tokens"], info["kernel"]) == (2, 256, 0)
