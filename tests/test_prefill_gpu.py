@@ -127,7 +127,7 @@ def test_prefill_fixed_shape(mask, W):
 @pytest.mark.parametrize("Hq,Hkv,seed", [(8, 2, 60), (6, 2, 61)])
 def test_prefill_variable_window(Hq, Hkv, seed):
     """Per-query inclusive key bounds: random spans, some of a single key, some far
-    left of the diagonal, over several 128-key tiles."""
+    left of the diagonal, over several 64-key tiles."""
     B, Sq, Sk = 3, 260, 400
     g = np.random.default_rng(seed)
     a, b = g.integers(0, Sk, size=(B, Sq)), g.integers(0, Sk, size=(B, Sq))
