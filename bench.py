@@ -60,6 +60,8 @@ def parse():
                     help="decode plan: target CTAs = split_waves x SMs (0 = library default)")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="profiling: q/K/V type of the one decode workload timed")
+    ap.add_argument("--head-dim", type=int, default=128, choices=[128, 256],
+                    help="profiling: head_dim of the 'prefill' workload")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -76,7 +78,7 @@ def profile_case(args):
         w = wl.RAGGED_PREFILL
         if args.batch:
             wl.RAGGED_PREFILL = wl.shrink(w, batch=args.batch)
-        r = measure_prefill(args.seed, args.steps, args.warmup, peak_tf)
+        r = measure_prefill(args.seed, args.steps, args.warmup, peak_tf, head_dim=args.head_dim)
         wl.RAGGED_PREFILL = w
     else:
         w = wl.DECODE_WORKLOADS[args.workload]
