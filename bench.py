@@ -317,45 +317,37 @@ def time_decode(inp, plan, steps, warmup, dist=None):
 
 
 def time_decode_e2e(inp, plan_kw, steps, warmup):
-    """The user-facing call sequence with host buffers, wall clock per step:
-    pinned host q / block_tables / seq_lens -> device, host planning on the
-    lengths (paged_decode_plan_update of one plan, as a serving loop re-plans
-    each step), paged_decode_run, device -> pinned host read of O (and LSE).
-    The KV pools are the cache: they stay resident on the device."""
+    """One serving step through the C ABI with host buffers, wall clock per step:
+    ``paged_decode_step_host`` re-plans one plan on the step's host lengths,
+    copies q / block tables (pinned host) to the device, runs the decode and
+    copies O and the LSE back to pinned host memory, then synchronises.  The KV
+    pools are the cache: they stay resident on the device."""
     import torch
     from paged_kv_attention_32_gb300 import api
-    dev = inp["q"].device
-    h_q = inp["q"].cpu().pin_memory()
-    h_bt = inp["block_tables"].cpu().pin_memory()
-    h_seq = inp["seq_lens_kv"].cpu().pin_memory()
-    h_ind = inp["qo_indptr"].cpu().pin_memory() if inp["qo_indptr"] is not None else None
-    d_q = torch.empty_like(inp["q"])
-    d_bt = torch.empty_like(inp["block_tables"])
-    d_seq = torch.empty_like(inp["seq_lens_kv"])
-    h_out = torch.empty(inp["q"].shape, dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty(inp["q"].shape[:2], dtype=torch.float32).pin_memory()
+    q, bt, seq = inp["q"], inp["block_tables"], inp["seq_lens_kv"]
+    rows = q.shape[:2]
+    io = api.DecodeHostIO(
+        q_host=q.cpu().pin_memory(), block_tables_host=bt.cpu().pin_memory(),
+        seq_lens_kv_host=seq.cpu().pin_memory(),
+        qo_indptr_host=None if inp["qo_indptr"] is None else inp["qo_indptr"].cpu().pin_memory(),
+        out_host=torch.empty(q.shape, dtype=q.dtype).pin_memory(),
+        lse_host=torch.empty(rows, dtype=torch.float32).pin_memory(),
+        q_dev=torch.empty_like(q), block_tables_dev=torch.empty_like(bt),
+        seq_lens_kv_dev=torch.empty_like(seq), out_dev=torch.empty_like(q),
+        lse_dev=torch.empty(rows, dtype=torch.float32, device=q.device))
+    t = io.tensors
     stream = torch.cuda.current_stream()
-    bytes_in = (h_q.numel() * 2 + h_bt.numel() * 4 + h_seq.numel() * 4)
-    bytes_out = h_out.numel() * 2 + (h_lse.numel() * 4 if inp["return_lse"] else 0)
-
+    bytes_in = q.numel() * q.element_size() + bt.numel() * 4 + seq.numel() * 4
+    bytes_out = q.numel() * q.element_size() + (t["lse_host"].numel() * 4
+                                                if inp["return_lse"] else 0)
     kw = dict(plan_kw)
-    if h_ind is not None:
-        kw["qo_indptr"] = h_ind
-    plan = api.paged_decode_plan(h_seq, stream=stream, **kw)   # made once, re-planned per step
+    if t["qo_indptr_host"] is not None:
+        kw["qo_indptr"] = t["qo_indptr_host"]
+    plan = api.paged_decode_plan(t["seq_lens_kv_host"], stream=stream, **kw)   # re-planned per step
 
     def step():
-        d_q.copy_(h_q, non_blocking=True)
-        d_bt.copy_(h_bt, non_blocking=True)
-        d_seq.copy_(h_seq, non_blocking=True)
-        p = plan.update(h_seq, qo_indptr=h_ind, stream=stream)
-        r = api.paged_decode_run(p, d_q, inp["k_pages"], inp["v_pages"], d_bt,
-                                 seq_lens_kv=d_seq, sinks=inp["sinks"], stream=stream)
-        o = r[0] if isinstance(r, tuple) else r
-        h_out.copy_(o, non_blocking=True)
-        if inp["return_lse"]:
-            h_lse.copy_(r[1], non_blocking=True)
-        stream.synchronize()
-        return p
+        api.paged_decode_step_host(plan, io, inp["k_pages"], inp["v_pages"], sinks=inp["sinks"],
+                                   stream=stream)
 
     for _ in range(warmup):
         step()
@@ -364,7 +356,9 @@ def time_decode_e2e(inp, plan_kw, steps, warmup):
     for _ in range(steps):
         step()
     torch.cuda.synchronize()
-    return (time.perf_counter() - t0) * 1e3 / steps, bytes_in, bytes_out
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    plan.check()
+    return ms, bytes_in, bytes_out
 
 
 def reduce_over_ranks(ms, nbytes, dist=None, device="cpu"):
@@ -713,9 +707,9 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
                     "h2d_bytes_per_step": bin_, "d2h_bytes_per_step": bout,
-                    "note": "host re-planning of one plan (paged_decode_plan_update) + pinned "
-                            "H2D of q/tables/lengths + run + D2H of O; "
-                            "the KV cache stays resident"},
+                    "note": "paged_decode_step_host per step: host re-planning of one plan "
+                            "on the step's lengths + pinned H2D of q/tables + run + D2H of "
+                            "O and LSE + synchronise; the KV cache stays resident"},
             "gpu_launches": args.steps * head["launches_per_call"],
             "clocks": clocks,
         }

@@ -16,6 +16,9 @@
  *   batch_prefill_plan / batch_prefill_run
  *       packed ragged causal context attention:
  *       "flashinfer.attention.prims_ts.batch_prefill".
+ *   paged_decode_step_host
+ *       one decode step from host buffers: re-plan, copies in, run, copies
+ *       out, queued in order on one stream.
  *   paged_decode_check_tables
  *       validation of the block-table entries a decode run reads.
  *   paged_kv_gather
@@ -131,7 +134,8 @@ const char* pka_version(void);
  *                    else 256.
  * mma_min_rows       the tensor-core kernel is used when
  *                    (Hq/Hkv) * max_q_len >= mma_min_rows; 0 = PKA_MMA_MIN_ROWS,
- *                    else 8.  paged_decode_plan_info reports the values used.
+ *                    else 8 (4 for PKA_DTYPE_F16 inputs).
+ *                    paged_decode_plan_info reports the values used.
  * flags              PKA_PLAN_HOST_ONLY or 0.
  * out_dtype          PKA_DTYPE_BF16, PKA_DTYPE_F16 or PKA_DTYPE_F32: O of
  *                    paged_decode_run (batch_decode_with_paged_kv_cache,
@@ -273,6 +277,59 @@ int paged_decode_run(const pka_plan* plan, const void* q, int64_t q_stride_tok,
                      const int32_t* block_tables, int64_t bt_row_stride,
                      const int32_t* seq_lens_kv_dev, const float* sinks, void* out, float* lse,
                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Host-buffer I/O of one decode step (paged_decode_step_host).  Host arrays
+ * should be pinned (page-locked) for the copies to be asynchronous; device
+ * staging arrays are the caller's and hold at least the sizes below.
+ *
+ * q_host, q_dev            [total_q, Hq, D] dense, the plan's input type.
+ * block_tables_host, _dev  [batch_size, bt_row_stride] int32 (as for
+ *                          paged_decode_run); the whole rows are copied.
+ * seq_lens_kv_host         [batch_size] int32: the step's key lengths, which
+ *                          the step re-plans on.
+ * seq_lens_kv_dev          [batch_size] int32 device, or NULL when the plan
+ *                          freezes the lengths (they then travel in the plan).
+ * qo_indptr_host           [batch_size + 1] int32, or NULL for the plan's
+ *                          fixed q_len.
+ * out_dev, out_host        [total_q, Hq, D] dense, the plan's output type.
+ * lse_dev, lse_host        [total_q, Hq] fp32; required when the plan returns
+ *                          the LSE, else ignored.
+ */
+typedef struct pka_decode_host_io {
+  const void* q_host;
+  const int32_t* block_tables_host;
+  const int32_t* seq_lens_kv_host;
+  const int32_t* qo_indptr_host;
+  void* out_host;
+  float* lse_host;
+  void* q_dev;
+  int32_t* block_tables_dev;
+  int32_t* seq_lens_kv_dev;
+  void* out_dev;
+  float* lse_dev;
+  int64_t bt_row_stride;
+} pka_decode_host_io;
+
+/*
+ * One decode step from host buffers, as a serving loop runs it: re-plan
+ * `plan` on the step's lengths (paged_decode_plan_update), copy q, the block
+ * table rows (and the live lengths) host -> device, run the decode over the
+ * device-resident K/V pools (arguments as for paged_decode_run, with dense q),
+ * and copy O (and the LSE) device -> host, all queued on `stream` in that
+ * order.  With `synchronize` nonzero the call returns once O is in host
+ * memory; otherwise the caller synchronises `stream` before reading it.
+ * workspace_bytes_out (may be NULL) receives the re-planned workspace size.
+ * Arguments are checked before anything is queued, and a failed re-plan
+ * leaves the plan unchanged.  PKA_ERR_WORKSPACE_TOO_SMALL means the plan was
+ * re-planned (its upload queued) but needs more workspace than given, and
+ * nothing else was queued.
+ */
+int paged_decode_step_host(pka_plan* plan, int32_t batch_size, const pka_decode_host_io* io,
+                           const void* k_pages, const void* v_pages, int64_t kv_stride_page,
+                           int64_t kv_stride_head, const float* sinks, void* workspace,
+                           size_t workspace_bytes, size_t* workspace_bytes_out,
+                           int32_t synchronize, void* stream);
 
 /*
  * Wait for `stream`, then read and clear the plan's device status word, which

@@ -29,7 +29,7 @@ EXPORTED = (
     "paged_decode_plan", "paged_decode_plan_update", "paged_decode_plan_destroy",
     "paged_decode_plan_info",
     "paged_decode_plan_export", "paged_decode_run", "paged_decode_plan_check",
-    "paged_decode_check_tables",
+    "paged_decode_check_tables", "paged_decode_step_host",
     "paged_decode_run_noalloc",
     "attn_merge_lse",
     "batch_prefill_plan", "batch_prefill_plan_fixed", "batch_prefill_plan_destroy", "batch_prefill_plan_check",
@@ -64,6 +64,17 @@ class PlanInfo(ctypes.Structure):
     ]
 
 
+class DecodeHostIO(ctypes.Structure):
+    _fields_ = [
+        ("q_host", ctypes.c_void_p), ("block_tables_host", ctypes.c_void_p),
+        ("seq_lens_kv_host", ctypes.c_void_p), ("qo_indptr_host", ctypes.c_void_p),
+        ("out_host", ctypes.c_void_p), ("lse_host", ctypes.c_void_p),
+        ("q_dev", ctypes.c_void_p), ("block_tables_dev", ctypes.c_void_p),
+        ("seq_lens_kv_dev", ctypes.c_void_p), ("out_dev", ctypes.c_void_p),
+        ("lse_dev", ctypes.c_void_p), ("bt_row_stride", ctypes.c_int64),
+    ]
+
+
 class PrefillDesc(ctypes.Structure):
     _fields_ = [
         ("batch_size", ctypes.c_int32), ("num_qo_heads", ctypes.c_int32),
@@ -92,6 +103,9 @@ _SIGS = {
                                         _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "paged_decode_plan_check": (ctypes.c_int, [_vp, _vp]),
     "paged_decode_check_tables": (ctypes.c_int, [_vp, _vp, _i64, _vp, _vp]),
+    "paged_decode_step_host": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(DecodeHostIO), _vp, _vp,
+                                              _i64, _i64, _vp, _vp, _sz, ctypes.POINTER(_sz),
+                                              _i32, _vp]),
     "paged_decode_run_noalloc": (ctypes.c_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _vp,
                                                 _i64, _vp, _vp, _vp, _vp, _vp]),
     "attn_merge_lse": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]),

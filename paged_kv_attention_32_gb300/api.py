@@ -194,6 +194,84 @@ def paged_decode_run(plan, q, k_pages, v_pages, block_tables, seq_lens_kv=None, 
     return (out, lse) if plan.desc.return_lse else out
 
 
+class DecodeHostIO:
+    """Host and device buffers of ``paged_decode_step_host`` (``pka_decode_host_io``).
+
+    Host tensors (CPU, pinned for asynchronous copies) hold each step's q, block
+    table rows and key lengths and receive O (and the LSE); device tensors of the
+    same shapes are the staging copies the run reads and writes.  The buffers are
+    sized for the largest batch; a step uses their leading rows.  The object keeps
+    every tensor alive and a workspace that grows when a re-plan needs more."""
+
+    def __init__(self, q_host, block_tables_host, seq_lens_kv_host, out_host, q_dev,
+                 block_tables_dev, out_dev, lse_host=None, lse_dev=None, seq_lens_kv_dev=None,
+                 qo_indptr_host=None):
+        host = dict(q_host=q_host, block_tables_host=block_tables_host,
+                    seq_lens_kv_host=seq_lens_kv_host, out_host=out_host, lse_host=lse_host,
+                    qo_indptr_host=qo_indptr_host)
+        dev = dict(q_dev=q_dev, block_tables_dev=block_tables_dev, out_dev=out_dev,
+                   lse_dev=lse_dev, seq_lens_kv_dev=seq_lens_kv_dev)
+        for name, t in host.items():
+            if t is not None and (t.device.type != "cpu" or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous CPU tensor")
+        for name in ("block_tables_host", "seq_lens_kv_host", "qo_indptr_host",
+                     "block_tables_dev", "seq_lens_kv_dev"):
+            t = host.get(name, dev.get(name))
+            if t is not None and t.dtype != torch.int32:
+                raise ValueError(f"{name} must be int32")
+        for name, t in dev.items():
+            if t is not None and (t.device.type != "cuda" or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        pairs = (("q", q_host, q_dev), ("block_tables", block_tables_host, block_tables_dev),
+                 ("out", out_host, out_dev), ("lse", lse_host, lse_dev))
+        for name, h, d in pairs:
+            if h is not None and d is not None and (h.shape != d.shape or h.dtype != d.dtype):
+                raise ValueError(f"{name}_host and {name}_dev must have one shape and dtype")
+        if q_host.shape != out_host.shape:
+            raise ValueError("out must have the shape of q")
+        self.tensors = dict(host, **dev)
+        self.workspace = None
+        self.c = L.DecodeHostIO(bt_row_stride=block_tables_host.stride(0),
+                                **{k: _ptr(v) for k, v in self.tensors.items()})
+
+
+def paged_decode_step_host(plan, io, k_pages, v_pages, sinks=None, batch_size=None,
+                           synchronize=True, stream=None):
+    """One decode step from host buffers (``paged_decode_step_host``): re-plan on the
+    lengths in ``io``, copy q / tables (/ lengths) in, run, copy O (/ LSE) out.
+    With ``synchronize`` the host outputs are ready on return."""
+    t = io.tensors
+    _check_inputs(plan, t["q_host"], k_pages, v_pages)
+    _check_layout(t["q_dev"], k_pages, v_pages, t["out_dev"], t["lse_dev"], paged=True)
+    if t["out_dev"].dtype != _TORCH[plan.desc.out_dtype]:
+        raise ValueError(f"out must be {_TORCH[plan.desc.out_dtype]} (the plan's out_dtype)")
+    B = t["seq_lens_kv_host"].numel() if batch_size is None else int(batch_size)
+    if B > t["block_tables_host"].shape[0] or B > t["seq_lens_kv_host"].numel():
+        raise ValueError("batch_size exceeds the io's table rows or lengths")
+    ind = t["qo_indptr_host"]
+    total_q = int(ind[B]) if ind is not None else B * plan.desc.q_len
+    if total_q > t["q_host"].shape[0]:
+        raise ValueError(f"the batch has {total_q} query rows, the io holds {t['q_host'].shape[0]}")
+    lib = L.lib()
+    ws_need = ctypes.c_size_t()
+    for attempt in range(2):
+        ws = io.workspace
+        ws_bytes = 0 if ws is None else ws.numel()
+        rc = lib.paged_decode_step_host(
+            plan.handle, B, ctypes.byref(io.c), _ptr(k_pages), _ptr(v_pages), k_pages.stride(0),
+            k_pages.stride(1), _ptr(sinks), _ptr(ws), ws_bytes, ctypes.byref(ws_need),
+            int(bool(synchronize)), _stream(stream))
+        if rc in (L.PKA_OK, L.PKA_ERR_WORKSPACE_TOO_SMALL):   # the plan was re-planned
+            plan.desc.batch_size = B
+            plan.workspace_bytes = ws_need.value
+        if rc != L.PKA_ERR_WORKSPACE_TOO_SMALL or attempt == 1:
+            break
+        io.workspace = torch.empty(ws_need.value + ws_need.value // 4 + 256, dtype=torch.uint8,
+                                   device=t["q_dev"].device)
+    L.check(rc, "paged_decode_step_host")
+    return (t["out_host"], t["lse_host"]) if plan.desc.return_lse else t["out_host"]
+
+
 def attn_merge_lse(v_states, s_states, out_dtype=torch.bfloat16, v_out=None, s_out=None,
                    stream=None):
     """Merge ``[N, S, H, D]`` fp32 states by their ``[N, S, H]`` base-2 LSEs."""

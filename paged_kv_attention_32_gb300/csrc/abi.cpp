@@ -386,6 +386,74 @@ int paged_decode_run(const pka_plan* p, const void* q, int64_t q_stride_tok,
   return launch_decode(*p, a, kmap, vmap, static_cast<cudaStream_t>(stream));
 }
 
+int paged_decode_step_host(pka_plan* p, int32_t batch_size, const pka_decode_host_io* io,
+                           const void* k_pages, const void* v_pages, int64_t kv_stride_page,
+                           int64_t kv_stride_head, const float* sinks, void* workspace,
+                           size_t workspace_bytes, size_t* workspace_bytes_out,
+                           int32_t synchronize, void* stream) {
+  NvtxRange nvtx_range("pka::paged_decode_step_host");
+  clear_error();
+  PKA_CHECK_ARG(p != nullptr && io != nullptr, "plan and io must not be NULL");
+  PKA_CHECK_ARG(p->dev_buf != nullptr, "plan was built with PKA_PLAN_HOST_ONLY and cannot run");
+  PKA_CHECK_ARG(io->q_host && io->block_tables_host && io->seq_lens_kv_host && io->out_host &&
+                    io->q_dev && io->block_tables_dev && io->out_dev,
+                "the q, block-table, length and output buffers must not be NULL");
+  PKA_CHECK_ARG(k_pages && v_pages, "k_pages and v_pages must not be NULL");
+  PKA_CHECK_ARG(p->desc.freeze_seq_lens || io->seq_lens_kv_dev != nullptr,
+                "seq_lens_kv_dev is required when the plan does not freeze the lengths");
+  PKA_CHECK_ARG(!p->desc.return_lse || (io->lse_host != nullptr && io->lse_dev != nullptr),
+                "the plan returns the LSE: lse_host and lse_dev are required");
+  PKA_CHECK_ARG(io->bt_row_stride >= p->C,
+                "bt_row_stride (%lld) is smaller than the table width %d",
+                (long long)io->bt_row_stride, p->C);
+  PKA_CHECK_ARG(aligned(io->q_dev, 16) && aligned(io->out_dev, 16) &&
+                    (io->lse_dev == nullptr || aligned(io->lse_dev, 4)),
+                "q_dev and out_dev must be 16-byte aligned, lse_dev 4-byte aligned");
+  PKA_CHECK_ARG(aligned(k_pages, 16) && aligned(v_pages, 16) && kv_stride_page % 8 == 0 &&
+                    kv_stride_head % 8 == 0,
+                "K/V pools must be 16-byte aligned with strides that are multiples of 8");
+  PKA_CHECK_ARG(workspace == nullptr || aligned(workspace, 256),
+                "workspace must be 256-byte aligned");
+  int rc = check_device(p->device);
+  if (rc != PKA_OK) return rc;
+
+  rc = paged_decode_plan_update(p, batch_size, io->seq_lens_kv_host, io->qo_indptr_host,
+                                workspace_bytes_out, stream);
+  if (rc != PKA_OK) return rc;
+  if (p->workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < (size_t)p->workspace_bytes))
+    return fail(PKA_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, the plan needs %lld",
+                workspace_bytes, (long long)p->workspace_bytes);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = (size_t)p->total_q * (size_t)p->Hq;
+  const size_t out_elem = p->desc.out_dtype == PKA_DTYPE_F32 ? 4 : 2;
+  PKA_CUDA_TRY(cudaMemcpyAsync(io->q_dev, io->q_host, rows * p->D * 2, cudaMemcpyHostToDevice, s),
+               "cudaMemcpyAsync (q)");
+  PKA_CUDA_TRY(cudaMemcpyAsync(io->block_tables_dev, io->block_tables_host,
+                               (size_t)batch_size * (size_t)io->bt_row_stride * sizeof(int32_t),
+                               cudaMemcpyHostToDevice, s),
+               "cudaMemcpyAsync (block tables)");
+  if (!p->desc.freeze_seq_lens)
+    PKA_CUDA_TRY(cudaMemcpyAsync(io->seq_lens_kv_dev, io->seq_lens_kv_host,
+                                 (size_t)batch_size * sizeof(int32_t), cudaMemcpyHostToDevice, s),
+                 "cudaMemcpyAsync (lengths)");
+  rc = paged_decode_run(p, io->q_dev, (int64_t)p->Hq * p->D, p->D, k_pages, v_pages,
+                        kv_stride_page, kv_stride_head, io->block_tables_dev, io->bt_row_stride,
+                        io->seq_lens_kv_dev, sinks, io->out_dev,
+                        p->desc.return_lse ? io->lse_dev : nullptr, workspace, workspace_bytes,
+                        stream);
+  if (rc != PKA_OK) return rc;
+  PKA_CUDA_TRY(cudaMemcpyAsync(io->out_host, io->out_dev, rows * p->D * out_elem,
+                               cudaMemcpyDeviceToHost, s),
+               "cudaMemcpyAsync (out)");
+  if (p->desc.return_lse)
+    PKA_CUDA_TRY(cudaMemcpyAsync(io->lse_host, io->lse_dev, rows * sizeof(float),
+                                 cudaMemcpyDeviceToHost, s),
+                 "cudaMemcpyAsync (lse)");
+  if (synchronize) PKA_CUDA_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  return PKA_OK;
+}
+
 int paged_decode_plan_check(const pka_plan* p, void* stream) {
   clear_error();
   PKA_CHECK_ARG(p != nullptr && p->d_status != nullptr, "plan has no device state");

@@ -30,7 +30,11 @@ namespace pka {
 namespace {
 constexpr int32_t kDefaultWaves = 2;
 constexpr int32_t kDefaultMinChunkTokens = 256;
+// rows per KV head from which the mma.sync kernel runs: measured on GB300, it
+// overtakes the CUDA-core kernel at 8 rows for bf16 and already at 4 for half,
+// whose conversions to fp32 the CUDA-core kernel pays and the tensor cores do not
 constexpr int32_t kDefaultMmaMinRows = 8;
+constexpr int32_t kDefaultMmaMinRowsF16 = 4;
 constexpr int32_t kMaxCudaCoreRows = 8;   // rows one warp of the CUDA-core kernel holds
 constexpr int32_t kMaxMmaRows = 64;       // four m16 tiles
 
@@ -76,7 +80,9 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
   if (d.split_waves <= 0) d.split_waves = env_int("PKA_SPLIT_WAVES", kDefaultWaves);
   if (d.min_chunk_tokens <= 0)
     d.min_chunk_tokens = env_int("PKA_MIN_CHUNK_TOKENS", kDefaultMinChunkTokens);
-  if (d.mma_min_rows <= 0) d.mma_min_rows = env_int("PKA_MMA_MIN_ROWS", kDefaultMmaMinRows);
+  if (d.mma_min_rows <= 0)
+    d.mma_min_rows = env_int("PKA_MMA_MIN_ROWS", d.dtype == PKA_DTYPE_F16 ? kDefaultMmaMinRowsF16
+                                                                          : kDefaultMmaMinRows);
   if (d.num_sms <= 0) {
     int dev = 0, sms = 0;
     PKA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");

@@ -74,3 +74,18 @@ def test_prefill_rejects_bad_layouts():
         api.batch_prefill_run(plan, q, k, torch.zeros((9, 3, 128), dtype=BF)[:, :2])
     with pytest.raises(ValueError, match="lse must be contiguous"):
         api.batch_prefill_run(plan, q, k, k, lse=torch.zeros((4, 9)).t())
+
+
+def test_host_io_wants_host_and_device_tensors_where_stated():
+    """DecodeHostIO: host buffers on the CPU, staging buffers on the device, int32
+    tables and lengths, matching host/device shapes (checked before any CUDA use)."""
+    q = torch.zeros((2, 4, 128), dtype=BF)
+    bt = torch.zeros((2, 4), dtype=torch.int32)
+    seq = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        api.DecodeHostIO(q_host=q, block_tables_host=bt, seq_lens_kv_host=seq, out_host=q.clone(),
+                         q_dev=q.clone(), block_tables_dev=bt.clone(), out_dev=q.clone())
+    with pytest.raises(ValueError, match="int32"):
+        api.DecodeHostIO(q_host=q, block_tables_host=bt.long(), seq_lens_kv_host=seq,
+                         out_host=q.clone(), q_dev=q.clone(), block_tables_dev=bt.clone(),
+                         out_dev=q.clone())

@@ -67,10 +67,12 @@ def test_native_plan_matches_spec(c):
 
 
 def test_kernel_choice_follows_rows_per_kv_head():
-    def kernel(G, L, mma_min_rows=0):
+    import torch
+
+    def kernel(G, L, mma_min_rows=0, dtype=torch.bfloat16):
         p = api.paged_decode_plan([100] * 2, num_qo_heads=G, num_kv_heads=1, page_size=16,
                                   max_pages_per_seq=8, num_pages=100, q_len=L, num_sms=8,
-                                  mma_min_rows=mma_min_rows, host_only=True)
+                                  mma_min_rows=mma_min_rows, host_only=True, dtype=dtype)
         return p.info["kernel"], p.info["rows_per_cta"]
     assert kernel(4, 1) == (0, 4)
     assert kernel(8, 1) == (1, 8)       # default threshold: 8 rows per KV head
@@ -78,6 +80,9 @@ def test_kernel_choice_follows_rows_per_kv_head():
     assert kernel(8, 2) == (1, 16)
     assert kernel(4, 3, mma_min_rows=16) == (1, 12)   # 9..15 rows exceed one CUDA-core warp
     assert kernel(4, 1, mma_min_rows=4) == (1, 4)
+    assert kernel(4, 1, dtype=torch.float16) == (1, 4)   # half: default threshold 4 rows
+    assert kernel(2, 1, dtype=torch.float16) == (0, 2)
+    assert kernel(4, 1, mma_min_rows=8, dtype=torch.float16) == (0, 4)
 
 
 def test_plan_update_equals_a_fresh_plan():
