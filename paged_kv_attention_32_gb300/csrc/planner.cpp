@@ -51,8 +51,8 @@ int32_t env_int(const char* name, int32_t fallback) {
 int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* seq,
                       const int32_t* indptr) {
   pka_decode_desc d = d_in;
-  PKA_CHECK_ARG(seq != nullptr, "seq_lens_kv_host is NULL");
   PKA_CHECK_ARG(d.batch_size >= 1, "batch_size must be >= 1 (got %d)", d.batch_size);
+  PKA_CHECK_ARG(seq != nullptr, "seq_lens_kv_host is NULL");
   PKA_CHECK_ARG(d.num_qo_heads >= 1 && d.num_kv_heads >= 1, "head counts must be >= 1");
   PKA_CHECK_ARG(d.num_qo_heads % d.num_kv_heads == 0,
                 "num_qo_heads (%d) must be a multiple of num_kv_heads (%d)", d.num_qo_heads,

@@ -124,3 +124,11 @@ def test_planner_tunables_from_the_environment(monkeypatch):
     monkeypatch.delenv("PKA_MMA_MIN_ROWS")
     info = api.paged_decode_plan(seq, **kw).info
     assert (info["split_waves"], info["min_chunk_tokens"], info["kernel"]) == (2, 256, 0)
+
+
+def test_an_empty_batch_is_rejected_by_name():
+    """A decode plan needs at least one request; an empty length array is reported as
+    such (not as a NULL pointer), and nothing is built."""
+    with pytest.raises(L.PkaError, match="batch_size"):
+        api.paged_decode_plan([], num_qo_heads=8, num_kv_heads=2, page_size=16,
+                              max_pages_per_seq=4, num_pages=100, num_sms=8, host_only=True)
