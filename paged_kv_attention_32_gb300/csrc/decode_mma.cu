@@ -1,6 +1,6 @@
 // Paged decode attention, tensor-core variant for wide query groups
-// ((Hq/Hkv) * max_q_len >= 8 rows per KV head by default: e.g. 8 query heads
-// per KV head, or speculative packed-Q verification with
+// ((Hq/Hkv) * max_q_len >= 8 rows per KV head by default, 4 with half inputs:
+// e.g. 8 query heads per KV head, or speculative packed-Q verification with
 // cudnn_batch_decode_with_kv_cache's q_len_per_req rows).
 //
 // Same work items, masks, softmax and outputs as the CUDA-core kernel; the
