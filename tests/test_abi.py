@@ -77,6 +77,24 @@ def test_run_rejects_host_only_plan_and_null_pointers():
     assert rc == L.PKA_ERR_INVALID_ARG
 
 
+def test_step_host_checks_its_arguments_before_any_device_work():
+    """paged_decode_step_host: a NULL io, a host-only plan and NULL buffers are
+    rejected on the host, and the plan is left as it was (not re-planned)."""
+    p = _plan()
+    before = p.export()
+    seq = (ctypes.c_int32 * 2)(300, 20)
+    io = L.DecodeHostIO(seq_lens_kv_host=ctypes.cast(seq, ctypes.c_void_p).value,
+                        bt_row_stride=20)
+    ws = ctypes.c_size_t(0)
+    lib = L.lib()
+    assert lib.paged_decode_step_host(p.handle, 2, None, None, None, 0, 0, None, None, 0,
+                                      ctypes.byref(ws), 1, None) == L.PKA_ERR_INVALID_ARG
+    assert lib.paged_decode_step_host(p.handle, 2, ctypes.byref(io), None, None, 0, 0, None,
+                                      None, 0, ctypes.byref(ws), 1, None) == L.PKA_ERR_INVALID_ARG
+    assert b"HOST_ONLY" in lib.pka_last_error()
+    assert p.export() == before
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(head_dim=64), L.PKA_ERR_UNSUPPORTED),
     (dict(window_left=-2), L.PKA_ERR_INVALID_ARG),
