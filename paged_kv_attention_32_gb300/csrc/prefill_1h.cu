@@ -258,8 +258,13 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       }
       m_ref = m_new;
       const float neg_m = -m_ref;
-      const float2 sum = masked ? exp_tile<true, F16>(ra, rb, sl2, neg_m, key0, lo, span, s_tm)
-                                : exp_tile<false, F16>(ra, rb, sl2, neg_m, key0, lo, span, s_tm);
+      // the masked scores are -inf now, so exp2(s * sl2 - m) is already 0 for them
+      // unless sl2 is 0 or the row has no finite reference yet (-inf + inf = NaN)
+      const bool zero_again =
+          masked && __any_sync(0xffffffffu, !(sl2 > 0.f) || m_ref == neg_inf());
+      const float2 sum = zero_again
+                             ? exp_tile<true, F16>(ra, rb, sl2, neg_m, key0, lo, span, s_tm)
+                             : exp_tile<false, F16>(ra, rb, sl2, neg_m, key0, lo, span, s_tm);
       tmem_wait_st();
       l = l * alpha + (sum.x + sum.y);
       tc_fence_before();

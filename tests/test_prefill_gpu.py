@@ -93,6 +93,14 @@ def test_prefill_window_left(W, causal):
     _run(lq, lk, 8, 2, causal=causal, seed=30 + W, window_left=W)
 
 
+@pytest.mark.parametrize("W", [-1, 40])
+def test_prefill_zero_scale_is_a_mean_over_visible_keys(W):
+    """sm_scale = 0: every visible key gets the same weight, so O is the mean of the
+    visible V rows; masked keys must still get none (their -inf score times 0 would
+    otherwise give NaN)."""
+    _run([1, 130, 257], [1, 200, 300], 4, 2, seed=45, sm_scale=0.0, window_left=W)
+
+
 def test_prefill_window_odd_group():
     _run([257, 64], [400, 64], 6, 2, seed=40, window_left=60)
 
