@@ -274,19 +274,62 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         warp_wait(bar(B_ODONE + ((n_kv - 1) & 1)), (uint32_t)(((n_kv - 1) >> 1) & 1), a.status)) {
       tc_fence_after();
       const float inv = l > 0.f ? a.output_scale / l : 0.f;
-      const int64_t dst = ((int64_t)(q0 + t) * a.num_qo_heads + h) * D;
+      // head_dim 256 (one CTA per SM) measured faster with direct stores
+      if (D != 128 || a.out_dtype == PKA_DTYPE_F32) {
+        const int64_t dst = ((int64_t)(q0 + t) * a.num_qo_heads + h) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32_sync(o_tm + (uint32_t)c * 32u, r);
-        if (row_valid) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32_sync(o_tm + (uint32_t)c * 32u, r);
+          if (row_valid) {
 #pragma unroll
-          for (int qd = 0; qd < 2; ++qd) {
-            float f[16];
+            for (int qd = 0; qd < 2; ++qd) {
+              float f[16];
 #pragma unroll
-            for (int x = 0; x < 16; ++x) f[x] = __uint_as_float(r[16 * qd + x]);
-            store_out<16>(a.out, dst + c * 32 + qd * 16, f, inv, a.out_dtype);
+              for (int x = 0; x < 16; ++x) f[x] = __uint_as_float(r[16 * qd + x]);
+              store_out<16>(a.out, dst + c * 32 + qd * 16, f, inv, a.out_dtype);
+            }
           }
+        }
+      } else {
+        // 16-bit O: each warp stages its 32 rows in the Q buffer (every QK has
+        // completed) with 16-byte chunks XOR-swizzled by row, then writes whole
+        // rows back, two per store instruction (coalesced 256-byte rows instead
+        // of 32 rows touched by every store).
+        constexpr int kRowBytes = D * 2, kChunks = kRowBytes / 16;
+        constexpr int kLanesPerRow = kChunks < 32 ? kChunks : 32;
+        uint8_t* wbuf = smem + kOffQ + (uint32_t)warp * 32u * kRowBytes;
+        const bool f16o = a.out_dtype == PKA_DTYPE_F16;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32_sync(o_tm + (uint32_t)c * 32u, r);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {   // 8 values = one 16-byte chunk
+            uint32_t w[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const float lo = __uint_as_float(r[8 * k + 2 * x]) * inv;
+              const float hi = __uint_as_float(r[8 * k + 2 * x + 1]) * inv;
+              w[x] = f16o ? pack2<true>(lo, hi) : pack2<false>(lo, hi);
+            }
+            const int q = c * 4 + k;
+            *reinterpret_cast<uint4*>(wbuf + lane * kRowBytes + ((q ^ (lane & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        __syncwarp();
+        const int q = lane % kLanesPerRow;
+#pragma unroll 4
+        for (int r0 = 0; r0 < 32; r0 += 32 / kLanesPerRow) {
+          const int rr = r0 + lane / kLanesPerRow;
+          const int tr = mt * kTileQ + warp * 32 + rr;
+          const uint4 val =
+              *reinterpret_cast<const uint4*>(wbuf + rr * kRowBytes + ((q ^ (rr & 7)) << 4));
+          if (tr < Lq)
+            *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
+                                      ((int64_t)(q0 + tr) * a.num_qo_heads + h) * kRowBytes +
+                                      q * 16) = val;
         }
       }
       if (row_valid && a.lse != nullptr)
