@@ -16,6 +16,7 @@ ranks over the slowest rank's time.
 """
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -132,18 +133,33 @@ def kv_bytes(inp):
     return keys * inp["num_kv_heads"] * D * 2 * 2, keys
 
 
-class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+_ACTIVE_SAMPLER = None
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+
+def clock_mark(which):
+    """Mark the start ("start") or end ("stop") of a timed region for the active
+    ClockSampler, whose summary then keeps only the samples taken inside it."""
+    if _ACTIVE_SAMPLER is not None:
+        setattr(_ACTIVE_SAMPLER, "t_" + which, time.time())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms; the summary keeps
+    the samples stamped inside the timed region (clock_mark), or all of them if
+    the region was too short to hold one."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.t_start = self.t_stop = None
 
     def __enter__(self):
+        global _ACTIVE_SAMPLER
+        _ACTIVE_SAMPLER = self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -155,6 +171,9 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
+        global _ACTIVE_SAMPLER
+        if _ACTIVE_SAMPLER is self:
+            _ACTIVE_SAMPLER = None
         self.lines = []
         if self.proc is not None:
             self.proc.terminate()
@@ -165,25 +184,39 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [l for l in out.splitlines() if l.strip()]
 
+    @staticmethod
+    def _stamp(text):
+        try:
+            return datetime.datetime.strptime(text, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
         if not getattr(self, "lines", None):
             return None
-        sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         for l in self.lines:
             parts = [p.strip() for p in l.split(",")]
             try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
+                samples.append((self._stamp(parts[0]), float(parts[1]), float(parts[2]),
+                                {n for n, v in zip(names, parts[4:])
+                                 if v.lower().startswith("active")}))
             except (ValueError, IndexError):
                 continue
-            for n, v in zip(names, parts[3:]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        window = "whole measurement"
+        inside = samples
+        if self.t_start is not None and self.t_stop is not None:
+            inside = [x for x in samples
+                      if x[0] is not None and self.t_start <= x[0] <= self.t_stop + 0.05]
+            window = "timed region"
+            if not inside:
+                inside, window = samples, "whole measurement (timed region shorter than a sample)"
+        if not inside:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": inside[-1][2],
+                "reasons": sorted(set().union(*(x[3] for x in inside))),
+                "samples": len(inside), "window": window}
 
 
 # ---------------------------------------------------------------------------
@@ -305,11 +338,13 @@ def time_decode(inp, plan, steps, warmup, dist=None):
         dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clock_mark("start")
     e0.record(stream)
     for _ in range(steps):
         api.paged_decode_run(*args, **kw)
     e1.record(stream)
     torch.cuda.synchronize()
+    clock_mark("stop")
     if dist is not None:
         dist.barrier()
     plan.check()
@@ -410,11 +445,13 @@ def time_prefill_calls(run, steps, warmup):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
+        clock_mark("start")
         e0.record()
         for _ in range(steps):
             run()
         e1.record()
         torch.cuda.synchronize()
+        clock_mark("stop")
     return e0.elapsed_time(e1) / steps, clk.summary()
 
 
