@@ -45,6 +45,27 @@ def test_decode_split_kv_path(name):
     assert_close(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("name,sms,wide", [("spec", 148, False), ("skewed", 148, True),
+                                           ("skewed", 48, True)])
+def test_decode_merge_kernels(name, sms, wide):
+    """Split partials are merged by a warp per (row, head), or by a CTA per (row, head)
+    when a request has more than 8 chunks or the (row, head) pairs are at most
+    4 x SMs; each choice against the oracle (spec: 1280 pairs of <= 3 chunks; skewed:
+    19 chunks, or 6 chunks over 192 pairs)."""
+    inp = wl.make_decode_inputs(SMALL[name], seed=5, device=DEV)
+    out, lse, plan = run_decode(inp, num_sms=sms, split_waves=2, min_chunk_tokens=128)
+    ex = plan.export()
+    if inp["qo_indptr"] is not None:
+        qlen = (inp["qo_indptr"][1:] - inp["qo_indptr"][:-1]).tolist()
+    else:
+        qlen = [inp["q_len"]] * len(ex["n_chunks"])
+    pairs = sum(L for L, c in zip(qlen, ex["n_chunks"]) if c > 1) * inp["q"].shape[1]
+    assert pairs > 0
+    assert (max(ex["n_chunks"]) > 8 or pairs <= 4 * sms) == wide
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
 @pytest.mark.parametrize("name", ["tiny", "llama3_8b", "skewed"])
 def test_decode_tensor_core_kernel_on_narrow_groups(name):
     """The mma kernel also runs 4- and 8-row groups (rows padded to 16)."""
