@@ -106,6 +106,29 @@ def test_step_host_equals_run_step_after_step(name, kw):
         assert split_seen and io.workspace is not None
 
 
+@pytest.mark.parametrize("in_dtype,out_dtype", [(torch.float16, torch.float32),
+                                               (torch.bfloat16, torch.float16)])
+def test_step_host_input_and_output_types(in_dtype, out_dtype):
+    """Half inputs and fp32 / fp16 outputs: the copies move the plan's element
+    sizes (2-byte q in, 4- or 2-byte O out)."""
+    inp = wl.make_decode_inputs(LLAMA, seed=23, device=DEV, dtype=in_dtype)
+    io = _make_io(inp, out_dtype)
+    plan = decode_plan_for(inp, out_dtype=out_dtype)
+    B, tq = _fill(io, inp)
+    out_h, lse_h = api.paged_decode_step_host(plan, io, inp["k_pages"], inp["v_pages"],
+                                              sinks=inp["sinks"], batch_size=B)
+    plan.check()
+    assert out_h.dtype == out_dtype
+    ref_plan = decode_plan_for(inp, out_dtype=out_dtype)
+    ref_o, ref_l = api.paged_decode_run(ref_plan, inp["q"], inp["k_pages"], inp["v_pages"],
+                                        inp["block_tables"], seq_lens_kv=inp["seq_lens_kv"],
+                                        sinks=inp["sinks"])
+    torch.cuda.synchronize()
+    assert torch.equal(out_h[:tq], ref_o.cpu()) and torch.equal(lse_h[:tq], ref_l.cpu())
+    o_or, l_or = oracle_decode(inp)
+    assert_close(out_h[:tq], lse_h[:tq], o_or, l_or)
+
+
 def test_step_host_rejects_a_batch_larger_than_the_buffers():
     inp = wl.make_decode_inputs(LLAMA, seed=22, device=DEV)
     small = dict(inp, q=inp["q"][:3], block_tables=inp["block_tables"][:3],
