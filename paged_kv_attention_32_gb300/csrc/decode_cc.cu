@@ -67,6 +67,7 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
   constexpr int NCH = DL / 8;     // 16-byte chunks per lane
   constexpr int NSTEP = kUnit / KS;
   constexpr unsigned FULL = 0xffffffffu;
+  pdl_launch_dependents();   // the split merge may be scheduled now; it waits for us
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -374,6 +375,7 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
 // Merge of the split requests' partials: one warp per (token row, q head).
 __global__ void __launch_bounds__(128)
 decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
+  pdl_wait_primary();   // the decode grid's partials are complete and visible
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t idx = (int64_t)blockIdx.x * 4 + warp;
   if (idx >= (int64_t)a.num_merge_rows * a.num_qo_heads) return;
@@ -436,6 +438,7 @@ constexpr int32_t kWideMergeChunks = 8;
 // memory.  A chunk without keys has O = 0 and LSE -inf (weight 0).
 __global__ void __launch_bounds__(128)
 decode_merge_wide_kernel(const __grid_constant__ DecodeArgs a) {
+  pdl_wait_primary();   // the decode grid's partials are complete and visible
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int kGroup = 8;
   __shared__ float4 part_o[4][32];
@@ -532,11 +535,22 @@ int launch_decode(const pka_plan& plan, const DecodeArgs& args, const CUtensorMa
     int32_t max_chunks = 0;
     for (const ReqInfo& r : plan.reqs) max_chunks = r.n_chunks > max_chunks ? r.n_chunks : max_chunks;
     const int64_t pairs = (int64_t)args.num_merge_rows * args.num_qo_heads;
-    if (max_chunks > kWideMergeChunks || pairs <= 4 * (int64_t)plan.desc.num_sms)
-      decode_merge_wide_kernel<<<(unsigned)pairs, 128, 0, stream>>>(args);
-    else
-      decode_merge_kernel<<<(unsigned)((pairs + 3) / 4), 128, 0, stream>>>(args);
-    cudaError_t e = cudaGetLastError();
+    const bool wide = max_chunks > kWideMergeChunks || pairs <= 4 * (int64_t)plan.desc.num_sms;
+    // launched as a programmatic dependent of the decode grid: its CTAs are placed
+    // while the decode's last CTAs run, and wait in-kernel for the partials
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)(wide ? pairs : (pairs + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = wide ? cudaLaunchKernelEx(&cfg, decode_merge_wide_kernel, args)
+                         : cudaLaunchKernelEx(&cfg, decode_merge_kernel, args);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode_merge_kernel launch");
   }
   return PKA_OK;

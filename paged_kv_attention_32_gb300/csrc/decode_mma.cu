@@ -50,6 +50,7 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * NSTAGE * kStageBytes);
 
+  pdl_launch_dependents();   // the split merge may be scheduled now; it waits for us
   const int mt_count = (a.rows_per_cta + 15) >> 4;
   const int item_idx = blockIdx.x / mt_count, mt = blockIdx.x % mt_count;
   const WorkItem it = a.items[item_idx];

@@ -233,6 +233,7 @@ def test_decode_graph_capture_replays_eagerly_equal():
     inp = wl.make_decode_inputs(SMALL["skewed"], seed=9, device=DEV)
     from helpers import decode_plan_for
     plan = decode_plan_for(inp, num_sms=32, split_waves=2)
+    assert plan.info["num_split"] > 0   # the graph holds the decode and its dependent merge
     out = torch.empty_like(inp["q"])
     lse = torch.empty(inp["q"].shape[:2], dtype=torch.float32, device=DEV)
     ws = torch.empty(max(plan.workspace_bytes, 1), dtype=torch.uint8, device=DEV)
