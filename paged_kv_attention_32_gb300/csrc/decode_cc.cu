@@ -372,34 +372,50 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
   }
 }
 
-// Merge of the split requests' partials: one warp per (token row, q head).
+// Merge of the split requests' partials: one warp per (token row, q head).  The
+// launcher sends requests of up to 8 chunks here, so the warp issues every
+// chunk's LSE (one per lane) and O row (8 loads per lane) at once and combines
+// them after one round of memory latency; longer chunk lists take further
+// rounds of 8.  A chunk without keys has O = 0 and LSE -inf (weight 0).
 __global__ void __launch_bounds__(128)
 decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
   pdl_wait_primary();   // the decode grid's partials are complete and visible
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int kGroup = 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t idx = (int64_t)blockIdx.x * 4 + warp;
   if (idx >= (int64_t)a.num_merge_rows * a.num_qo_heads) return;
   const int mr = (int)(idx / a.num_qo_heads), h = (int)(idx % a.num_qo_heads);
   const MergeRow row = a.merge_rows[mr];
   const ReqInfo rq = a.reqs[row.request];
+  const int nc = rq.n_chunks;
   const int64_t stride_c = (int64_t)rq.q_len * a.num_qo_heads;
   const int64_t p0 = rq.part_base + (int64_t)row.row * a.num_qo_heads + h;
   float m = neg_inf();
-  for (int c = 0; c < rq.n_chunks; ++c) m = fmaxf(m, a.ws_lse[p0 + c * stride_c]);
+  for (int c = lane; c < nc; c += 32) m = fmaxf(m, a.ws_lse[p0 + c * stride_c]);
+#pragma unroll
+  for (int delta = 16; delta > 0; delta >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, delta));
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-  if (m != neg_inf()) {
-    for (int c = 0; c < rq.n_chunks; ++c) {
-      const int64_t p = p0 + c * stride_c;
-      const float lc = a.ws_lse[p];
-      if (lc == neg_inf()) continue;
-      const float w = ex2(lc - m);
+  for (int c0 = 0; c0 < nc && m != neg_inf(); c0 += kGroup) {
+    // lane k < kGroup holds the weight of chunk c0 + k; every lane its 4 dims of each O row
+    const int cl = c0 + lane;
+    const float lc = lane < kGroup && cl < nc ? a.ws_lse[p0 + cl * stride_c] : neg_inf();
+    float4 v[kGroup];
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k)
+      v[k] = c0 + k < nc ? *reinterpret_cast<const float4*>(
+                               a.ws_o + (p0 + (int64_t)(c0 + k) * stride_c) * 128 + lane * 4)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float wl = lc == neg_inf() ? 0.f : ex2(lc - m);
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k) {
+      const float w = __shfl_sync(FULL, wl, k);
       wsum += w;
-      const float4 v = *reinterpret_cast<const float4*>(a.ws_o + p * 128 + lane * 4);
-      o.x += w * v.x;
-      o.y += w * v.y;
-      o.z += w * v.z;
-      o.w += w * v.w;
+      o.x += w * v[k].x;
+      o.y += w * v[k].y;
+      o.z += w * v[k].z;
+      o.w += w * v[k].w;
     }
   }
   float denom = wsum;
