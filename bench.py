@@ -31,8 +31,8 @@ sys.path.insert(0, ROOT)
 HEADLINE = "llama3_8b"
 PREFILL_WINDOW = 2047   # sliding-window variant of the ragged prefill (2048 keys per row)
 # DRAM read + write bytes of one headline decode launch (decode_cc_kernel<4,3>,
-# seed 0, one GB300) from an ncu capture of this same command; the full
-# command and numbers are in profiles/decode_cc_kernel_llama3_8b_full_traffic.md.
+# seed 0, one GB300): ncu's dram__bytes_read.sum + dram__bytes_write.sum for
+# that launch, captured on this same command (one metric pass, full size).
 # Other seeds or ranks scale it by their algorithmic K+V bytes.
 # the kernel symbol each decode plan launches
 KERNEL_SYMBOL = {"cuda_core": "decode_cc_kernel", "mma": "decode_mma_kernel"}
@@ -470,9 +470,11 @@ def prefill_result(name, ms, flops, peak_tflops, tiles, clocks):
     return res
 
 
-def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1, dtype=None, head_dim=128):
+def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1, dtype=None, head_dim=128,
+                    cpu=False):
     """Ragged causal prefill; FLOPs = 4 * D per unmasked (query, key) pair per query head
-    (with a window, row i of a request keeps min(i + 1, window_left + 1) keys)."""
+    (with a window, row i of a request keeps min(i + 1, window_left + 1) keys).  With
+    `cpu`, the fp64 oracle is timed beside it on a sample of the same inputs."""
     import torch
     from paged_kv_attention_32_gb300 import api
     from paged_kv_attention_32_gb300 import workloads as wl
@@ -505,7 +507,10 @@ def measure_prefill(seed, steps, warmup, peak_tflops, window_left=-1, dtype=None
         plan.check()
     except Exception as exc:   # reported, not hidden: the line says why there is no number
         return {"workload": name, "status": f"not measured: {exc}", "flops": flops}
-    return prefill_result(name, ms, flops, peak_tflops, plan.num_tiles, clocks)
+    res = prefill_result(name, ms, flops, peak_tflops, plan.num_tiles, clocks)
+    if cpu:
+        res["cpu_baseline"] = prefill_cpu_baseline(inp, w)
+    return res
 
 
 def measure_prefill_fixed(seed, steps, warmup, peak_tflops, variable_window=False, dense=False):
@@ -633,8 +638,117 @@ def cpu_baseline(inp, min_seconds=10.0):
                       f"({done / 1e9:.2f} GB of K+V in {secs:.1f} s)"}
 
 
+def _prefill_oracle_worker(conn, task):
+    """Long-lived prefill oracle worker: one request's query rows of one GQA group,
+    its keys and values for that group's KV head; repeats them on command."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import oracle
+    q_bits, k_bits, v_bits, rows, flops = task
+    lq, lk = q_bits.shape[0], k_bits.shape[0]
+    ind_q, ind_k = [0, lq], [0, lk]
+    while True:
+        msg = conn.recv()
+        if msg is None:
+            return
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.prefill_request(0, q_bits, k_bits, v_bits, ind_q, ind_k, 1, causal=True,
+                                   rows=rows)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= msg:
+                break
+        conn.send((el, reps * flops))
+
+
+def prefill_cpu_baseline(inp, w, min_seconds=8.0, rows_per_task=32):
+    """The fp64 oracle on the host cores, on a bounded sample of the ragged prefill:
+    worker i takes request i % B and the query heads of KV head (i // B) % Hkv, and
+    `rows_per_task` query rows spread evenly over the request; FLOPs = 4 * D per
+    visible (row, key) pair per query head, as the GPU line counts them."""
+    import multiprocessing as mp
+    import numpy as np
+    from paged_kv_attention_32_gb300 import workloads as wl
+    ind = inp["qo_indptr"].cpu().numpy()
+    B, G = len(ind) - 1, w.num_qo_heads // w.num_kv_heads
+    ctx = mp.get_context("spawn")
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+    procs, conns = [], []
+    for i in range(cpu_cores()):
+        b, hk = i % B, (i // B) % w.num_kv_heads
+        s0, s1 = int(ind[b]), int(ind[b + 1])
+        n = s1 - s0
+        rows = np.unique(np.linspace(0, n - 1, min(rows_per_task, n)).astype(np.int64))
+        flops = 4 * w.head_dim * G * int((rows + 1).sum())
+        task = (wl.bf16_bits(inp["q"][s0:s1, hk * G:(hk + 1) * G]),
+                wl.bf16_bits(inp["k"][s0:s1, hk:hk + 1]), wl.bf16_bits(inp["v"][s0:s1, hk:hk + 1]),
+                rows, flops)
+        a, c = ctx.Pipe()
+        pr = ctx.Process(target=_prefill_oracle_worker, args=(c, task), daemon=True)
+        pr.start()
+        procs.append(pr)
+        conns.append(a)
+    try:
+        for c in conns:
+            c.send(min_seconds)
+        res = [c.recv() for c in conns]
+    finally:
+        for c in conns:
+            c.send(None)
+        for pr in procs:
+            pr.join(timeout=10)
+    secs = max(r[0] for r in res)
+    done = sum(r[1] for r in res)
+    return {"value": round(done / secs / 1e12, 6), "unit": "TFLOP/s", "cores": len(procs),
+            "kind": "oracle",
+            "sample": f"fp64 oracle, one spawned process per core, each repeating {rows_per_task} "
+                      f"causal rows of one request x the {G} query heads of one KV head for "
+                      f">= {min_seconds:.0f} s ({done / 1e12:.3f} TFLOP in {secs:.1f} s)"}
+
+
 def emit(line):
     print(json.dumps(line), flush=True)
+
+
+def headline_config(w, inp, world):
+    """The `config` object of the headline line, the same for both arms."""
+    nbytes, keys = kv_bytes(inp)
+    return {"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+            "kv_tokens": keys, "kv_bytes_per_call": nbytes,
+            "l2": "inputs larger than L2 (each call reads >1 GB of K/V; no flush)",
+            "parallelism": f"replicas x{world} (one batch per GPU)"}
+
+
+def clocks_ok(clocks):
+    """False when the clock record shows a throttle reason other than the power cap,
+    or an SM clock well below its maximum with no reason given; None without a record."""
+    if not clocks:
+        return None
+    bad = set(clocks.get("reasons", [])) - {"sw_power_cap"}
+    low = clocks["sm_mhz"] < 0.85 * clocks["sm_max_mhz"] and not clocks.get("reasons")
+    return not bad and not low
+
+
+def compact(r):
+    """A short summary of one sub-line (kept last on the JSON line, so that a reader
+    keeping only the line's tail still sees every workload)."""
+    if "status" in r:
+        return {"status": r["status"][:60]}
+    out = {"ms": r.get("ms_per_call")}
+    if "GB_per_s" in r:
+        out.update(GBps=r["GB_per_s"], frac=r.get("frac_of_measured_hbm"))
+    if "TFLOP_per_s" in r:
+        out.update(TFLOPs=r["TFLOP_per_s"], frac=r.get("frac_of_measured_bf16"))
+        if "frac_of_measured_bf16_sustained" in r:
+            out["frac_sust"] = r["frac_of_measured_bf16_sustained"]
+    if "clocks" in r:
+        out["clk_ok"] = clocks_ok(r["clocks"])
+    if r.get("cpu_baseline"):
+        out["oracle"] = r["cpu_baseline"]["value"]
+    return out
 
 
 def reference_arm(args, rank):
@@ -666,7 +780,8 @@ def reference_arm(args, rank):
           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
           "ms_per_step": round(total * 1e3 / args.steps, 2), "higher_is_better": True,
           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-          "config": {"workload": wl.DECODE_WORKLOADS[HEADLINE].name},
+          "config": headline_config(wl.DECODE_WORKLOADS[HEADLINE], inp,
+                                    int(os.environ.get("WORLD_SIZE", "1"))),
           "cpu_baseline": cpu,
           "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                   "d2h_bytes_per_step": 0}})
@@ -731,12 +846,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads,
-                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                       "page_size": w.page_size, "kv_tokens": head["kv_tokens"],
-                       "kv_bytes_per_call": head["kv_bytes"],
-                       "l2": "inputs larger than L2 (each call reads >1 GB of K/V; no flush)",
-                       "parallelism": f"replicas x{world} (one batch per GPU)"},
+            "config": headline_config(w, inp, world),
             "roofline": {"bound": "hbm", "kernel": KERNEL_SYMBOL[head["kernel"]],
                          "achieved": round(gbs_kernel, 1), "peak": peak_gbs, "unit": "GB/s",
                          "frac": round(gbs_kernel / peak_gbs, 4), "peak_source": peak_kind,
@@ -754,13 +864,14 @@ def main():
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_extra:
         extra = {}
-        for name in ("skewed", "spec"):
+        for name in ("tiny", "skewed", "spec"):
             r, i2, p2 = measure_workload(name, args.seed, max(5, args.steps // 2),
                                          max(3, args.warmup), peak_gbs)
             extra[name] = r
             del i2, p2
             torch.cuda.empty_cache()
-        extra["prefill"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf)
+        extra["prefill"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf,
+                                           cpu=world == 1 and not args.no_cpu)
         extra["prefill_window"] = measure_prefill(args.seed, max(3, args.steps // 4), 3, peak_tf,
                                                   window_left=PREFILL_WINDOW)
         extra["prefill_fixed"] = measure_prefill_fixed(args.seed, max(3, args.steps // 4), 3,
@@ -782,6 +893,12 @@ def main():
                                            peak_gbs)
         line["decode_headline"] = head
         line["other_workloads"] = extra
+        # last key: one short entry per workload, so the line's tail names them all
+        per = {"llama3_8b": compact(dict(head, clocks=clocks))}
+        per.update((k, compact(v)) for k, v in extra.items())
+        if cpu is not None:
+            per["llama3_8b"]["oracle"] = cpu["value"]
+        line["per_config"] = per
     if rank == 0:
         emit(line)
     if dist is not None:

@@ -37,14 +37,20 @@
  *     `stream` is a cudaStream_t (NULL = legacy default stream).
  *   - Element strides are in elements, not bytes.
  *   - q/K/V are bf16 (PKA_DTYPE_BF16) or IEEE half (PKA_DTYPE_F16), one type
- *     for all three (cudnn_batch_decode_with_kv_cache, q: float16 or
- *     bfloat16); the output is bf16, f16 or fp32 (out_dtype of
- *     batch_decode_with_paged_kv_cache and batch_prefill).  head_dim must be 128.
+ *     for all three, chosen by the plan's `dtype` (cudnn_batch_decode_with_kv_cache,
+ *     q: float16 or bfloat16); the output is bf16, f16 or fp32, chosen by the
+ *     plan's `out_dtype` (out_dtype of batch_decode_with_paged_kv_cache and
+ *     batch_prefill).  head_dim is 128 for decode and 128 or 256 for prefill
+ *     (batch_prefill allows those two head sizes).
  *   - The caller owns every device buffer (q, pools, tables, lengths, out,
  *     lse, workspace).  The library owns only the opaque plan objects.
- *   - *_run entry points allocate nothing, never synchronise and never read
- *     device memory on the host, so they may be captured in a CUDA graph.
- *     Plans must be created before capture.
+ *   - paged_decode_run and batch_prefill_run allocate nothing, never
+ *     synchronise and never read device memory on the host, so they may be
+ *     captured in a CUDA graph.  Plans must be created before capture.
+ *   - Prefill, like decode, is split into a host plan (batch_prefill_plan,
+ *     made from host copies of the indptr arrays, before any capture) and a
+ *     run (batch_prefill_run): batch_decode_with_paged_kv_cache's planner note
+ *     asks for exactly this split so that the run stays capturable.
  */
 #ifndef PKA_H
 #define PKA_H
@@ -125,8 +131,8 @@ const char* pka_version(void);
  *                    and <= the length the plan saw (lengths above that are
  *                    clamped to it), and the window start is then found at
  *                    run time (batch_decode_with_paged_kv_cache, planner note:
- *                    "bind a stable runtime seq_lens tensor or let the plan
- *                    retain fixed sequence lengths").
+ *                    a captured run either reads a length tensor that stays
+ *                    in place or uses lengths kept in the plan).
  * num_sms            SM count the planner balances for; 0 = the device's.
  * split_waves        target CTAs = split_waves * num_sms; 0 = the environment
  *                    variable PKA_SPLIT_WAVES if set to a positive integer, else 2.
@@ -176,7 +182,9 @@ typedef struct pka_plan_info {
   int32_t partial_rows;     /* fp32 partial rows in the workspace                   */
   int64_t workspace_bytes;  /* bytes paged_decode_run needs in `workspace`          */
   int32_t kernel;           /* PKA_KERNEL_CUDA_CORE or PKA_KERNEL_MMA               */
-  int32_t rows_per_cta;     /* query rows a CTA holds: (Hq/Hkv) * max_q_len         */
+  int32_t rows_per_cta;     /* query rows per KV head, (Hq/Hkv) * max_q_len: one
+                               CTA holds them all (CUDA-core kernel, <= 8) or one
+                               16-row tile of them (tensor-core kernel, <= 65536) */
   int32_t num_sms;          /* SM count the plan balanced for                       */
   int32_t split_waves;
   int32_t min_chunk_tokens;
@@ -188,7 +196,7 @@ typedef struct pka_plan_info {
  *
  * seq_lens_kv_host  [B] int32 host array, 1 <= kv_len <= C*page_size and
  *                   kv_len >= the request's q_len (cudnn_batch_decode_with_kv_cache,
- *                   q_len_per_req: "Every request needs kv_len >= q_len").
+ *                   q_len_per_req: no request may have fewer keys than query rows).
  * qo_indptr_host    NULL (fixed q_len) or [B+1] int32 host array, cumulative
  *                   query offsets starting at 0, every q_len >= 1 (packed mode,
  *                   batch_decode_with_paged_kv_cache, qo_indptr).
@@ -243,10 +251,11 @@ int paged_decode_plan_export(const pka_plan* plan, int32_t* items, int32_t* n_ch
 /*
  * Run the planned decode.
  *
- * q               bf16, rows [total_q] x heads [Hq] x D; element (t, h, d) at
+ * q               the plan's dtype (bf16 or f16), rows [total_q] x heads [Hq] x D;
+ *                 element (t, h, d) at
  *                 q + t*q_stride_tok + h*q_stride_head + d.  D innermost and
  *                 dense; other strides free (cudnn_batch_decode_with_kv_cache,
- *                 Note: "q may carry arbitrary batch/head strides").
+ *                 Note: q may be a strided view, e.g. part of a fused QKV output).
  *                 Strides must be multiples of 8 elements.
  * k_pages, v_pages  HND pools: element (page, kv_head, slot, d) at
  *                 base + page*kv_stride_page + kv_head*kv_stride_head + slot*D + d
@@ -263,7 +272,8 @@ int paged_decode_plan_export(const pka_plan* plan, int32_t* items, int32_t* n_ch
  * sinks           NULL or fp32 [Hq] device: per-head sink logits joining each
  *                 row's softmax denominator with a zero value row
  *                 (cudnn_batch_decode_with_kv_cache, sinks).
- * out             bf16 [total_q, Hq, D] contiguous.
+ * out             the plan's out_dtype (bf16, f16 or fp32), [total_q, Hq, D]
+ *                 contiguous, 16-byte aligned.
  * lse             NULL or fp32 [total_q, Hq] contiguous: log2 of the sum over
  *                 the row's valid keys of exp(scale * q.k) -- the sink is not
  *                 included (Note "LSE convention").  Required when the plan
@@ -337,7 +347,10 @@ int paged_decode_step_host(pka_plan* plan, int32_t batch_size, const pka_decode_
  * some kernel of an earlier run gave up on a bounded (2 s) wait (the outputs
  * of that run are then not valid); or PKA_ERR_DEVICE_BOUNDS when
  * paged_decode_check_tables found a block-table entry outside [0, num_pages).
- * Synchronises; not for capture.
+ * For a PKA_PLAN_HOST_ONLY plan the word read is the one that
+ * paged_decode_run_noalloc's kernels report into on the current device,
+ * shared by every no-allocation run there: it collects them all since the
+ * last check.  Reading it allocates nothing.  Synchronises; not for capture.
  */
 int paged_decode_plan_check(const pka_plan* plan, void* stream);
 
@@ -378,8 +391,14 @@ int paged_decode_check_tables(const pka_plan* plan, const int32_t* block_tables,
  *   different streams, or from different threads) race and give wrong
  *   results.  Serialise them.
  * - The call copies the plan's host arrays into the array with
- *   cudaMemcpyAsync and clears its status word with cudaMemsetAsync; it
- *   calls no allocating routine.
+ *   cudaMemcpyAsync; it calls no allocating routine.
+ * - Kernels that give up on a bounded wait report it in a status word at the
+ *   start of the array (cleared once at the first call on the device, then
+ *   only by a check): paged_decode_plan_check on a PKA_PLAN_HOST_ONLY plan
+ *   reads and clears it, reporting every no-allocation run since the last
+ *   check.
+ * - A plan with a device copy must be run on the device it was made on; a
+ *   host-only plan runs on the current device.
  */
 int paged_decode_run_noalloc(const pka_plan* plan, const void* q, int64_t q_stride_tok,
                              int64_t q_stride_head, const void* k_pages, const void* v_pages,
@@ -415,7 +434,7 @@ int attn_merge_lse(const float* v_states, const float* s_states, int32_t num_sta
 /* ======================================================================== */
 
 /*
- * batch_size, num_qo_heads, num_kv_heads, head_dim (128) as for decode.
+ * batch_size, num_qo_heads, num_kv_heads as for decode; head_dim 128 or 256.
  * mask         PKA_MASK_CAUSAL (bottom-right aligned) or PKA_MASK_DENSE.
  * window_left  -1 disables; W >= 0 keeps, for query row i of a request with
  *              Lq rows and Lk keys, the keys from Lk - Lq + i - W on (the plain
@@ -487,11 +506,15 @@ int batch_prefill_plan_check(const pka_prefill_plan* plan, void* stream);
 
 /*
  * Run the planned prefill.
- * q      bf16 packed [total_q, Hq, D]: (t, h, d) at q + t*q_stride_tok + h*q_stride_head + d.
- * k, v   bf16 packed [total_kv, Hkv, D]: (t, h, d) at base + t*kv_stride_tok + h*kv_stride_head + d.
+ * q      the plan's dtype (bf16 or f16), packed [total_q, Hq, D]: (t, h, d) at
+ *        q + t*q_stride_tok + h*q_stride_head + d.
+ * k, v   the plan's dtype, packed [total_kv, Hkv, D]: (t, h, d) at
+ *        base + t*kv_stride_tok + h*kv_stride_head + d.
  *        All strides multiples of 8 elements, bases 16-byte aligned.
- * out    bf16 [total_q, Hq, D] contiguous.
+ * out    the plan's out_dtype (bf16, f16 or fp32), [total_q, Hq, D] contiguous,
+ *        16-byte aligned.
  * lse    NULL or fp32 [total_q, Hq] contiguous base-2 LSE (required with return_lse).
+ * workspace, workspace_bytes  unused (the prefill needs none); may be NULL, 0.
  */
 int batch_prefill_run(const pka_prefill_plan* plan, const void* q, int64_t q_stride_tok,
                       int64_t q_stride_head, const void* k, const void* v, int64_t kv_stride_tok,
@@ -521,8 +544,9 @@ int paged_kv_gather(const void* pages, int64_t num_pages, int64_t stride_page,
  * 2e9), ORs the timeout bit (1) into a status word and returns; the context
  * stays usable.  The status word is the decode plan's own when `plan` is not
  * NULL (paged_decode_plan_check then returns PKA_ERR_DEVICE_TIMEOUT, and
- * clears it), else *status_dev (device int32, caller-owned).  Does not
- * synchronise.
+ * clears it) -- for a PKA_PLAN_HOST_ONLY plan the word of
+ * paged_decode_run_noalloc's scratch on the current device -- else
+ * *status_dev (device int32, caller-owned).  Does not synchronise.
  */
 int pka_wait_timeout_probe(const pka_plan* plan, int32_t* status_dev, int64_t limit_ns,
                            void* stream);

@@ -456,8 +456,18 @@ int paged_decode_step_host(pka_plan* p, int32_t batch_size, const pka_decode_hos
 
 int paged_decode_plan_check(const pka_plan* p, void* stream) {
   clear_error();
-  PKA_CHECK_ARG(p != nullptr && p->d_status != nullptr, "plan has no device state");
-  return read_status(p->d_status, static_cast<cudaStream_t>(stream));
+  PKA_CHECK_ARG(p != nullptr, "plan must not be NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p->desc.flags & PKA_PLAN_HOST_ONLY) {
+    // a host-only plan runs only through paged_decode_run_noalloc, whose
+    // kernels report into the status word of its fixed scratch
+    int32_t* word = nullptr;
+    const int rc = noalloc_status_word(s, &word);
+    if (rc != PKA_OK) return rc;
+    return read_status(word, s);
+  }
+  PKA_CHECK_ARG(p->d_status != nullptr, "plan has no device state");
+  return read_status(p->d_status, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -659,7 +669,10 @@ int paged_decode_check_tables(const pka_plan* p, const int32_t* block_tables,
 int pka_wait_timeout_probe(const pka_plan* plan, int32_t* status_dev, int64_t limit_ns,
                            void* stream) {
   clear_error();
-  if (plan != nullptr) {
+  if (plan != nullptr && (plan->desc.flags & PKA_PLAN_HOST_ONLY)) {
+    const int rc = noalloc_status_word(static_cast<cudaStream_t>(stream), &status_dev);
+    if (rc != PKA_OK) return rc;
+  } else if (plan != nullptr) {
     PKA_CHECK_ARG(plan->d_status != nullptr, "plan has no device state");
     status_dev = plan->d_status;
   }

@@ -23,6 +23,7 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+constexpr size_t kStatusBytes = 256;   // the status word, padded to the alignment
 constexpr int kMaxDevices = 256;
 std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices] = {};
@@ -31,14 +32,19 @@ size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Device address of the scratch array on `dev` (the current device), looked
 // up once per device.  In host code the symbol is only a stand-in: kernels
-// get this address, never the symbol itself.
-int scratch_address(int dev, unsigned char** out) {
+// get this address, never the symbol itself.  The set-up also clears the
+// status word once, queued on `stream` ahead of the caller's work; after that
+// only paged_decode_plan_check clears it, so a failed wait in any run since
+// the last check stays visible.
+int scratch_address(int dev, cudaStream_t stream, unsigned char** out) {
   if (dev < 0 || dev >= kMaxDevices) return fail(PKA_ERR_INVALID_ARG, "device %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    e = cudaMemsetAsync(p, 0, kStatusBytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(no-alloc status)");
     g_scratch_addr[dev] = p;
   }
   *out = static_cast<unsigned char*>(g_scratch_addr[dev]);
@@ -46,6 +52,17 @@ int scratch_address(int dev, unsigned char** out) {
 }
 
 }  // namespace
+
+int noalloc_status_word(cudaStream_t stream, int32_t** out) {
+  int dev = -1;
+  PKA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+  unsigned char* base = nullptr;
+  const int rc = scratch_address(dev, stream, &base);
+  if (rc != PKA_OK) return rc;
+  *out = reinterpret_cast<int32_t*>(base);
+  return PKA_OK;
+}
+
 }  // namespace pka
 
 using namespace pka;
@@ -69,6 +86,8 @@ extern "C" int paged_decode_run_noalloc(const pka_plan* p, const void* q, int64_
                     q_stride_head % 8 == 0 && q_stride_tok >= 0 && q_stride_head >= 0,
                 "q must be 16-byte aligned with non-negative strides that are multiples of 8");
   PKA_CHECK_ARG(reinterpret_cast<uintptr_t>(out) % 16 == 0, "out must be 16-byte aligned");
+  PKA_CHECK_ARG(lse == nullptr || reinterpret_cast<uintptr_t>(lse) % 4 == 0,
+                "lse must be 4-byte aligned");
   PKA_CHECK_ARG(kv_stride_page % 8 == 0 && kv_stride_head % 8 == 0,
                 "K/V strides must be multiples of 8 elements");
   PKA_CHECK_ARG(bt_row_stride >= p->C, "bt_row_stride is smaller than the table width");
@@ -77,7 +96,7 @@ extern "C" int paged_decode_run_noalloc(const pka_plan* p, const void* q, int64_
   const size_t n_items = p->items.size() * sizeof(WorkItem);
   const size_t n_reqs = p->reqs.size() * sizeof(ReqInfo);
   const size_t n_merge = p->merge_rows.size() * sizeof(MergeRow);
-  const size_t off_items = 256;
+  const size_t off_items = kStatusBytes;
   const size_t off_reqs = off_items + up256(n_items);
   const size_t off_merge = off_reqs + up256(n_reqs);
   const size_t off_ws = off_merge + up256(n_merge);
@@ -91,13 +110,18 @@ extern "C" int paged_decode_run_noalloc(const pka_plan* p, const void* q, int64_
 
   int dev = -1;
   PKA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
-  unsigned char* base = nullptr;
-  int rc = scratch_address(dev, &base);
-  if (rc != PKA_OK) return rc;
+  // a plan with a device copy was made for one device; a host-only plan runs
+  // on whichever device is current
+  if (p->dev_buf != nullptr)
+    PKA_CHECK_ARG(dev == p->device, "plan was made on device %d, current device is %d",
+                  p->device, dev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // Only the status word must start at zero: every partial row is written by
-  // its chunk before the merge kernel reads it.
-  PKA_CUDA_TRY(cudaMemsetAsync(base, 0, 256, s), "cudaMemsetAsync(no-alloc status)");
+  unsigned char* base = nullptr;
+  int rc = scratch_address(dev, s, &base);
+  if (rc != PKA_OK) return rc;
+  // Nothing else must start at zero: every partial row is written by its
+  // chunk before the merge kernel reads it, and the status word is cleared
+  // only by paged_decode_plan_check (it collects every run since).
   if (n_items)
     PKA_CUDA_TRY(cudaMemcpyAsync(base + off_items, p->items.data(), n_items,
                                  cudaMemcpyHostToDevice, s),

@@ -32,6 +32,10 @@ int launch_check_tables(const WorkItem* items, int32_t num_items, const ReqInfo*
 // timeout bit ends up in *status (device int32).
 int launch_wait_probe(uint64_t limit_ns, int32_t* status, cudaStream_t stream);
 
+// Device address of the status word of paged_decode_run_noalloc's fixed
+// scratch on the current device (set up on first use, on `stream`).
+int noalloc_status_word(cudaStream_t stream, int32_t** out);
+
 int launch_paged_gather(const CUtensorMap& map, const int32_t* block_tables,
                         int64_t bt_row_stride, int32_t page_size, int32_t request,
                         int32_t kv_head, int32_t tok_begin, int32_t tok_end, void* out,

@@ -36,7 +36,10 @@ constexpr int32_t kDefaultMinChunkTokens = 256;
 constexpr int32_t kDefaultMmaMinRows = 8;
 constexpr int32_t kDefaultMmaMinRowsF16 = 4;
 constexpr int32_t kMaxCudaCoreRows = 8;   // rows one warp of the CUDA-core kernel holds
-constexpr int32_t kMaxMmaRows = 64;       // four m16 tiles
+// query rows per KV head the tensor-core kernel takes: one CTA per 16-row
+// tile of every item (4096 tiles); the pages put no bound on the group or on
+// q_len_per_req, this only keeps the launch arithmetic in 32 bits
+constexpr int32_t kMaxMmaRows = 65536;
 
 // A positive integer from the environment variable `name`, else `fallback`.
 int32_t env_int(const char* name, int32_t fallback) {

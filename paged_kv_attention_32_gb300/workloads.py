@@ -16,6 +16,12 @@ Recipe (all seeds explicit):
 * the K/V pool holds ``pool_pages`` pages; every request draws the pages it
   needs, without replacement, from one random permutation of the pool;
   unused ``block_tables`` slots hold -1 and are never read.
+* "climbing" inputs (``climbing_keys``, ``aligned_queries``) replace the
+  N(0, 1) keys and queries with keys whose component along one random unit
+  direction grows linearly with the key's position, and queries close to that
+  direction: every row's scores then rise towards its last keys.  Values and
+  lengths are drawn as above; the extra draws use a CPU generator seeded
+  with ``seed + 2``.
 """
 
 from dataclasses import dataclass, field, replace
@@ -200,3 +206,55 @@ def make_prefill_inputs(w: PrefillWorkload, seed: int = 0, device="cpu"):
 def bf16_bits(t: torch.Tensor):
     """The uint16 bit patterns of a 16-bit (bf16 or f16) tensor, as a numpy array (host copy)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def climbing_keys(positions, num_heads, u, slope, gen, noise=0.25):
+    """Key rows whose component along the unit direction ``u`` grows with the key's
+    position: row p is ``(slope * p) * u + noise * N(0, 1)`` for every head
+    (float32 on the CPU, ``[len(positions), num_heads, D]``).  With queries close to
+    ``u``, each query row's largest scores sit at its last keys, so the running row
+    maximum climbs from one key tile to the next."""
+    pos = torch.as_tensor(positions, dtype=torch.float32)
+    D = u.numel()
+    rows = torch.randn((pos.numel(), num_heads, D), generator=gen, dtype=torch.float32) * noise
+    return rows + (slope * pos)[:, None, None] * u.to(torch.float32)[None, None, :]
+
+
+def aligned_queries(num_rows, num_heads, u, gen, noise=0.05):
+    """Query rows ``a_h * u + noise * N(0, 1)``, one factor ``a_h`` in [1, 1.25] per
+    head (float32 on the CPU, ``[num_rows, num_heads, D]``)."""
+    a = 1.0 + 0.25 * torch.rand((num_heads,), generator=gen, dtype=torch.float32)
+    D = u.numel()
+    rows = torch.randn((num_rows, num_heads, D), generator=gen, dtype=torch.float32) * noise
+    return rows + a[None, :, None] * u.to(torch.float32)[None, None, :]
+
+
+def unit_direction(head_dim, gen):
+    """A random unit vector of ``head_dim`` components (float32 on the CPU)."""
+    u = torch.randn((head_dim,), generator=gen, dtype=torch.float64)
+    return (u / u.norm()).to(torch.float32)
+
+
+def make_climbing_decode_inputs(w: DecodeWorkload, seed: int = 0, device="cpu",
+                                dtype=torch.bfloat16, slope=1.5):
+    """Decode inputs of workload ``w`` (lengths, tables, V, sinks as ``make_decode_inputs``
+    draws them) whose keys climb along one direction with the token index and whose
+    queries point along it (``climbing_keys``, ``aligned_queries``): the scores of every
+    row rise towards its last keys, so the chunks of a split request end with partial
+    LSEs far apart."""
+    inp = make_decode_inputs(w, seed=seed, device=device, dtype=dtype)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 2)
+    u = unit_direction(w.head_dim, g)
+    ps = w.page_size
+    tables = inp["block_tables"].cpu().to(torch.int64)
+    seq = inp["seq_lens_kv"].cpu().to(torch.int64)
+    kp = inp["k_pages"].cpu().to(torch.float32)
+    for b in range(w.batch):
+        t = torch.arange(int(seq[b]), dtype=torch.int64)
+        pages = tables[b, t // ps]
+        kp[pages, :, t % ps, :] = climbing_keys(t, w.num_kv_heads, u, slope, g)
+    inp["k_pages"] = kp.to(dtype).to(device)
+    q = inp["q"]
+    inp["q"] = aligned_queries(q.shape[0], q.shape[1], u, g).to(dtype).to(device)
+    return inp

@@ -57,12 +57,24 @@ def _plan(**kw):
     (dict(qo_indptr=[1, 2, 5]), L.PKA_ERR_INVALID_ARG),
     (dict(qo_indptr=[0, 2, 2]), L.PKA_ERR_INVALID_ARG),                 # empty packed request
     (dict(window_left=-2), L.PKA_ERR_INVALID_ARG),
-    (dict(num_qo_heads=64, num_kv_heads=1, q_len=2), L.PKA_ERR_UNSUPPORTED),  # 128 rows
+    (dict(num_qo_heads=256, num_kv_heads=1, q_len=257, seq=[300, 300]),
+     L.PKA_ERR_UNSUPPORTED),                                            # 65792 rows per KV head
 ])
 def test_plan_rejects(kw, code):
     with pytest.raises(L.PkaError) as ei:
         _plan(**kw)
     assert ei.value.code == code
+
+
+@pytest.mark.parametrize("Hq,Hkv,q_len,tiles", [(128, 1, 1, 8), (64, 1, 2, 8), (16, 2, 16, 8),
+                                                (256, 1, 4, 64)])
+def test_plan_accepts_wide_groups(Hq, Hkv, q_len, tiles):
+    """More than 64 query rows per KV head (MQA with many heads, long q_len_per_req):
+    the tensor-core kernel with one CTA per 16-row tile of each work item."""
+    p = _plan(num_qo_heads=Hq, num_kv_heads=Hkv, q_len=q_len, seq=[100, 50])
+    info = p.info
+    assert info["kernel"] == L.PKA_KERNEL_MMA
+    assert -(-info["rows_per_cta"] // 16) == tiles
 
 
 def test_plan_accepts_packed_and_reports_total_rows():

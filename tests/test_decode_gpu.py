@@ -117,6 +117,29 @@ def test_decode_wide_groups(G, L, packed, split):
     assert_close(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("Hq,Hkv,L,packed,split", [
+    (128, 1, 1, False, False),   # MQA, 128 heads: 8 tiles per item
+    (128, 1, 1, False, True),    #   ... with split chunks and the merge
+    (64, 1, 6, True, True),      # 64 heads x packed q_len 1..6: up to 384 rows, 24 tiles
+    (16, 2, 16, False, False),   # G = 8 x q_len 16: 128 rows, causal
+])
+def test_decode_more_than_64_rows_per_kv_head(Hq, Hkv, L, packed, split):
+    """Groups wider than four 16-row tiles (cudnn_batch_decode_with_kv_cache allows any
+    num_heads_qo >= num_heads_kv and any q_len_per_req): one mma CTA per tile."""
+    w = wl.DecodeWorkload(name="wider", batch=4, num_qo_heads=Hq, num_kv_heads=Hkv,
+                          head_dim=128, page_size=16, kv_len_range=(L, 1300),
+                          q_len_range=(1, L) if packed else (L, L), packed_q=packed,
+                          causal=L > 1, window_left=400 if split else -1, sinks=split)
+    inp = wl.make_decode_inputs(w, seed=22, device=DEV)
+    kw = dict(num_sms=64, split_waves=2, min_chunk_tokens=128) if split else {}
+    out, lse, plan = run_decode(inp, **kw)
+    assert plan.info["kernel"] == 1 and plan.info["rows_per_cta"] > 64
+    if split:
+        assert plan.info["num_split"] > 0
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
 @pytest.mark.parametrize("in_dtype,out_dtype", [
     (torch.float16, None), (torch.float16, torch.float32), (torch.bfloat16, torch.float32),
     (torch.bfloat16, torch.float16)])

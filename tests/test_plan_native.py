@@ -30,6 +30,19 @@ def _cases():
                           sms=rnd.choice([8, 132, 152]), waves=rnd.choice([1, 2, 4]),
                           mct=rnd.choice([128, 256, 512]), frozen=rnd.random() < 0.8,
                           causal=rnd.random() < 0.5, mma_min_rows=rnd.choice([4, 8, 16])))
+    wide = random.Random(29)
+    for _ in range(10):   # more than 64 query rows per KV head (tensor-core kernel, many tiles)
+        B = wide.randint(1, 24)
+        G = wide.choice([16, 32, 64, 128])
+        packed = wide.random() < 0.5
+        ql = [wide.randint(1, 6) if packed else 1 for _ in range(B)]
+        kv = [max(ql[b], wide.randint(1, 20000)) for b in range(B)]
+        cases.append(dict(kv=kv, ql=ql, packed=packed, Hq=G * wide.choice([1, 2]), Hkv=1, ps=16,
+                          W=wide.choice([-1, 4095]), sms=152, waves=2, mct=256,
+                          frozen=True, causal=True, mma_min_rows=8))
+        if wide.random() < 0.5:
+            cases[-1]["Hkv"] = 2
+            cases[-1]["Hq"] = G * 2
     return cases
 
 
@@ -42,9 +55,6 @@ def test_native_plan_matches_spec(c):
         indptr = [0]
         for q in c["ql"]:
             indptr.append(indptr[-1] + q)
-    G = c["Hq"] // c["Hkv"]
-    if G * max(c["ql"]) > 64:
-        pytest.skip("rows per KV head above the supported 64")
     plan = api.paged_decode_plan(
         c["kv"], num_qo_heads=c["Hq"], num_kv_heads=c["Hkv"], page_size=ps,
         max_pages_per_seq=C, num_pages=10 ** 6, qo_indptr=indptr, q_len=1,

@@ -2,8 +2,10 @@
 allocate device memory (code inside an allocator hook, or a process whose
 device memory is a fixed pool it does not control).  It keeps its work list
 and split-KV partials in a fixed array inside the library.  Checked through
-the C ABI against paged_decode_run on two calls in a row.  This file is
-collected last on purpose."""
+the C ABI against paged_decode_run on two calls in a row, against the fp64
+oracle (also with live lengths shorter than planned), and for the report of a
+wait that gave up, read through paged_decode_plan_check on a host-only plan.
+This file is collected last on purpose."""
 
 import ctypes
 
@@ -14,7 +16,7 @@ from paged_kv_attention_32_gb300 import _lib as L
 from paged_kv_attention_32_gb300 import api
 from paged_kv_attention_32_gb300 import workloads as wl
 
-from helpers import LSE_ATOL, O_ATOL, O_RTOL, decode_plan_for
+from helpers import LSE_ATOL, O_ATOL, O_RTOL, assert_close, decode_plan_for, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -71,3 +73,55 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
     rc = _noalloc(plan, inp, out, None)
     assert rc == L.PKA_ERR_WORKSPACE_TOO_SMALL
     assert b"16777216" in L.lib().pka_last_error()
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "spec"])
+def test_noalloc_matches_the_oracle(name):
+    """Frozen lengths (llama3_8b shape: CUDA-core kernel, split) and live lengths shorter
+    than planned (spec shape: tensor-core kernel, causal rows, window, sinks)."""
+    w = {"llama3_8b": wl.shrink(wl.LLAMA3_8B_DECODE, batch=5, kv_len_range=(512, 2100),
+                                pool_pages=1000, table_width=160, return_lse=True),
+         "spec": wl.shrink(wl.SPEC_DECODE, batch=5, kv_len_range=(600, 2600), window_left=700,
+                           table_width=200)}[name]
+    inp = wl.make_decode_inputs(w, seed=21, device="cuda")
+    frozen = name == "llama3_8b"
+    plan = decode_plan_for(inp, num_sms=32, split_waves=2, min_chunk_tokens=128, host_only=True,
+                           freeze_seq_lens=frozen)
+    assert plan.info["num_split"] > 0
+    if not frozen:
+        cut = torch.tensor([0, 7, 100, 333, 1], dtype=torch.int32, device="cuda")
+        inp = dict(inp, seq_lens_kv=inp["seq_lens_kv"] - cut)
+    out = torch.full_like(inp["q"], float("nan"))
+    lse = torch.full(inp["q"].shape[:2], float("nan"), device="cuda")
+    assert _noalloc(plan, inp, out, lse) == L.PKA_OK, L.lib().pka_last_error()
+    torch.cuda.synchronize()
+    plan.check()
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+def test_noalloc_reports_a_wait_that_gave_up():
+    """The kernels' bounded wait, run on the status word of the fixed scratch (the word
+    a host-only plan's check reads), is reported once as PKA_ERR_DEVICE_TIMEOUT and
+    cleared; the next no-allocation decode still matches paged_decode_run."""
+    w = wl.shrink(wl.SKEWED_DECODE, batch=4, fixed_first_kv_len=9000, kv_len_range=(1024, 3000),
+                  table_width=300)
+    inp = wl.make_decode_inputs(w, seed=23, device="cuda")
+    host_plan = decode_plan_for(inp, num_sms=64, split_waves=2, host_only=True)
+    host_plan.check()   # nothing pending
+    api.wait_timeout_probe(limit_ns=20_000_000, plan=host_plan)
+    with pytest.raises(L.PkaError) as exc:
+        host_plan.check()
+    assert exc.value.code == L.PKA_ERR_DEVICE_TIMEOUT
+    host_plan.check()   # the read cleared it
+    ref_plan = decode_plan_for(inp, num_sms=64, split_waves=2)
+    ref_o, ref_l = api.paged_decode_run(ref_plan, inp["q"], inp["k_pages"], inp["v_pages"],
+                                        inp["block_tables"], sinks=inp["sinks"])
+    out = torch.full_like(inp["q"], float("nan"))
+    lse = torch.full(inp["q"].shape[:2], float("nan"), device="cuda")
+    assert _noalloc(host_plan, inp, out, lse) == L.PKA_OK, L.lib().pka_last_error()
+    torch.cuda.synchronize()
+    host_plan.check()
+    diff = (out.float() - ref_o.float()).abs()
+    assert bool((diff <= O_ATOL + O_RTOL * ref_o.float().abs()).all())
+    assert bool(((lse - ref_l).abs() <= LSE_ATOL).all())
