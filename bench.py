@@ -734,16 +734,16 @@ def clocks_ok(clocks):
 
 def compact(r):
     """A short summary of one sub-line (kept last on the JSON line, so that a reader
-    keeping only the line's tail still sees every workload)."""
+    keeping only the line's tail still sees every workload): ms per call, the achieved
+    GB/s or TFLOP/s, the fraction of the measured peak, whether the clocks were clean,
+    and the oracle's rate where one was timed."""
     if "status" in r:
         return {"status": r["status"][:60]}
-    out = {"ms": r.get("ms_per_call")}
+    out = {"ms": float(f"{r.get('ms_per_call'):.4g}")}
     if "GB_per_s" in r:
-        out.update(GBps=r["GB_per_s"], frac=r.get("frac_of_measured_hbm"))
+        out.update(GBps=round(r["GB_per_s"]), frac=round(r.get("frac_of_measured_hbm"), 3))
     if "TFLOP_per_s" in r:
-        out.update(TFLOPs=r["TFLOP_per_s"], frac=r.get("frac_of_measured_bf16"))
-        if "frac_of_measured_bf16_sustained" in r:
-            out["frac_sust"] = r["frac_of_measured_bf16_sustained"]
+        out.update(TFLOPs=round(r["TFLOP_per_s"]), frac=round(r.get("frac_of_measured_bf16"), 3))
     if "clocks" in r:
         out["clk_ok"] = clocks_ok(r["clocks"])
     if r.get("cpu_baseline"):

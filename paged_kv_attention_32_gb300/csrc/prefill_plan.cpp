@@ -6,6 +6,8 @@
 // long causal rows out before the short ones (longest-processing-time order).
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
+#include <string>
 
 #include "host_common.h"
 #include "prefill.h"
@@ -93,12 +95,17 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
       }
       const int32_t kv0 = (int32_t)(lo / kTileK);
       const int32_t n_kv = (int32_t)(ceil_div(hi, kTileK) - kv0);
+      PKA_CHECK_ARG(n_kv >= 1, "request %d: a query tile with no key tile", b);
       for (int32_t h = 0; h < p.Hq; ++h)
         p.tiles.push_back(PrefillTile{b, h, (int32_t)m, n_kv, kv0});
     }
   }
   std::stable_sort(p.tiles.begin(), p.tiles.end(),
                    [](const PrefillTile& a, const PrefillTile& b) { return a.n_kv > b.n_kv; });
+  {
+    const char* k = std::getenv("PKA_PREFILL_KERNEL");
+    p.kernel = (k != nullptr && std::string(k) == "1h") ? 0 : 1;
+  }
   p.total_q = qo[B];
   p.total_kv = kv[B];
   PKA_CHECK_ARG(p.tiles.size() < (size_t)INT32_MAX, "too many prefill tiles");
