@@ -14,14 +14,18 @@
 //
 // One CTA per SM walks the plan's tiles (128 query rows of one request and
 // one query head each, heaviest first) in a snake order over the CTAs.  Roles:
-//   warps 0-3  softmax, one thread per query row (TMEM lane): row max, lazy
-//              rescale of O (when the max grew by more than 2^8), p = exp2,
-//              P (16-bit) over the first 32 columns of the S slot, the final
-//              O / l and LSE; between tiles they copy the next tile's Q from
-//              shared memory into TMEM and write the finished tile's O;
-//   warp 4     TMA: Q tiles (two staging buffers) and K tiles;
-//   warp 5     TMA: V tiles;
-//   warp 6     allocates TMEM and issues every tcgen05.mma (one elected
+//   warps 0-7  softmax: warp w owns the query rows of TMEM lane quarter w % 4
+//              and half w / 4 of each 64-key tile (32 keys) and of O (64
+//              columns); the two warps of a quarter trade their partial row
+//              maxima through shared memory (one named barrier per quarter),
+//              so both take the same lazy-rescale decision (rescale O only
+//              when the max grew by more than 2^8).  p = exp2, P (16-bit)
+//              over the first 32 columns of the S slot, the final O / l and
+//              LSE; between tiles they copy the next tile's Q from shared
+//              memory into TMEM and write the finished tile's O;
+//   warp 8     TMA: Q tiles (two staging buffers) and K tiles;
+//   warp 9     TMA: V tiles;
+//   warp 10    allocates TMEM and issues every tcgen05.mma (one elected
 //              lane, four chained k-steps per asm block).
 // TMEM (512 columns): S slots [0, 256) (4 x 64), O [256, 384), Q buffers
 // [384, 448) and [448, 512) (two tiles' Q, bf16 pairs per column).
@@ -46,7 +50,9 @@ constexpr uint32_t kQBox = 16384;              // 128 rows x 128 bytes (64 colum
 constexpr uint32_t kKBox = 8192;               // 64 rows x 128 bytes
 constexpr uint32_t kQStage = 2 * kQBox;        // one tile's Q (two column blocks)
 constexpr uint32_t kKVStage = 2 * kKBox;       // one K or V tile
-constexpr int kThreads = 224;
+constexpr int kSoftmaxWarps = 8, kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kWarpK = 8, kWarpV = 9, kWarpMma = 10;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint32_t kColO = NS * 64, kColQ = kColO + kD;
 
@@ -55,23 +61,25 @@ constexpr uint32_t kOffEpi = kOffQ + 2 * kQStage;       // O staging (16-bit out
 constexpr uint32_t kOffK = kOffEpi + 128u * kD * 2;     // K stages
 constexpr uint32_t kOffV = kOffK + NK * kKVStage;       // V stages
 constexpr uint32_t kOffBar = kOffV + NV * kKVStage;
-constexpr size_t kSmemBytes = 1024 + kOffBar + 512;
+constexpr uint32_t kOffX = kOffBar + 512;               // row-max / row-sum exchange
+constexpr uint32_t kXBytes = (2 * 2 + 2) * 128 * 4;     // max [parity][half][row], sum [half][row]
+constexpr size_t kSmemBytes = 1024 + kOffX + kXBytes;
 
 // mbarriers.  A parity wait is only correct when the barrier has completed
 // the phase before the awaited one; the argument for each is given where it
 // is waited on.
 enum {
   B_QFULL = 0,              // [2] Q staging buffer b holds tile 2k + b (TMA, tx bytes)
-  B_QEMPTY = 2,             // [2] softmax copied that Q into TMEM (128 arrivals)
-  B_QTM = 4,                // [2] Q of tile 2k + b is in TMEM buffer b (128 arrivals)
+  B_QEMPTY = 2,             // [2] softmax copied that Q into TMEM (256 arrivals)
+  B_QTM = 4,                // [2] Q of tile 2k + b is in TMEM buffer b (256 arrivals)
   B_KFULL = 6,              // [NK]
   B_KEMPTY = B_KFULL + NK,  // [NK] QK of the step that used the stage completed
   B_VFULL = B_KEMPTY + NK,  // [NV]
   B_VEMPTY = B_VFULL + NV,  // [NV] P V of the step completed
   B_SFULL = B_VEMPTY + NV,  // [NS] S of the step is in its slot
-  B_PFULL = B_SFULL + NS,   // [NS] P of the step is in its slot (128 arrivals)
+  B_PFULL = B_SFULL + NS,   // [NS] P of the step is in its slot (256 arrivals)
   B_ODONE = B_PFULL + NS,   // [NS] P V of the step completed
-  B_OFREE = B_ODONE + NS,   // softmax read O of a finished tile (128 arrivals)
+  B_OFREE = B_ODONE + NS,   // softmax read O of a finished tile (256 arrivals)
   B_MMADONE = B_OFREE + 1,
   B_COUNT = B_MMADONE + 1
 };
@@ -88,6 +96,67 @@ __device__ __forceinline__ uint64_t kmajor_b(uint32_t base, int kk) {
 // V tile (64 keys x 128 dims) as the MN-major B operand, k-step kk = keys 16kk..
 __device__ __forceinline__ uint64_t vmn(uint32_t base, int kk) {
   return smem_desc_sw128(base + (uint32_t)kk * 2048u, kKBox, 1024u);
+}
+
+// Named barrier of the two softmax warps of one TMEM lane quarter (ids 1-4):
+// both warps arrive, and each gets the AND of `v` over the 64 threads.  Every
+// bounded wait of these warps is followed by one, so that a wait that gave up
+// makes both warps of the pair leave together (a lone warp would otherwise
+// wait at the next barrier with no partner).
+__device__ __forceinline__ bool pair_all(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, 64, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
+// Row max of 32 scores as four independent chains.
+__device__ __forceinline__ float row_max32(const uint32_t* r) {
+  float mq[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+#pragma unroll
+  for (int i = 0; i < 32; i += 2)
+    mq[(i >> 1) & 3] = fmax3(mq[(i >> 1) & 3], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+  return fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+}
+
+// Scores of keys outside [lo, lo + span) (r: keys key0 .. key0 + 31) to -inf.
+__device__ __forceinline__ void mask_scores32(uint32_t* r, int key0, int lo, unsigned span) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if ((unsigned)(key0 + i - lo) >= span) r[i] = __float_as_uint(neg_inf());
+}
+
+// p = exp2(s * sl2 - m) for 32 scores (keys key0 .. key0 + 31), packed two
+// per 32-bit TMEM column into the 16 columns at p_tm; returns the sum of p.
+// MASKED: keys outside [lo, lo + span) give p = 0 (see exp_tile).
+template <bool MASKED, bool F16>
+__device__ __forceinline__ float exp_half(const uint32_t* r, float sl2, float neg_m, int key0,
+                                          int lo, unsigned span, uint32_t p_tm) {
+  const float2 sc = make_float2(sl2, sl2), nm = make_float2(neg_m, neg_m);
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 x =
+        __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc, nm);
+    float2 p = make_float2(ex2(x.x), ex2(x.y));
+    if constexpr (MASKED) {
+      if ((unsigned)(key0 + 2 * i - lo) >= span) p.x = 0.f;
+      if ((unsigned)(key0 + 2 * i + 1 - lo) >= span) p.y = 0.f;
+    }
+    if (i & 1) acc1 = __fadd2_rn(acc1, p);
+    else acc0 = __fadd2_rn(acc0, p);
+    pk[i] = pack2<F16>(p.x, p.y);
+  }
+  tmem_st16(p_tm, pk);
+  const float2 t = __fadd2_rn(acc0, acc1);
+  return t.x + t.y;
 }
 
 // The plan's tile processed by CTA `cta` (of `ctas`) in its round r, or -1:
@@ -135,8 +204,8 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_QFULL + b), 1);
-      mbar_init(bar(B_QEMPTY + b), 128);
-      mbar_init(bar(B_QTM + b), 128);
+      mbar_init(bar(B_QEMPTY + b), kSoftmaxThreads);
+      mbar_init(bar(B_QTM + b), kSoftmaxThreads);
     }
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
@@ -148,14 +217,14 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     }
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_PFULL + s), 128);
+      mbar_init(bar(B_PFULL + s), kSoftmaxThreads);
       mbar_init(bar(B_ODONE + s), 1);
     }
-    mbar_init(bar(B_OFREE), 128);
+    mbar_init(bar(B_OFREE), kSoftmaxThreads);
     mbar_init(bar(B_MMADONE), 1);
     fence_barrier_init();
   }
-  if (warp == 6) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -164,7 +233,7 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kWarpK) {
     // ---------------- TMA: Q tiles and K tiles ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmq);
@@ -226,7 +295,7 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           mbar_wait(bar(B_KFULL + last_k % NK), (uint32_t)((last_k / NK) & 1), nullptr);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpV) {
     // ---------------- TMA: V tiles ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmv);
@@ -254,7 +323,7 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       if (!ok && last_v >= 0)
         mbar_wait(bar(B_VFULL + last_v % NV), (uint32_t)((last_v / NV) & 1), nullptr);
     }
-  } else if (warp == 6) {
+  } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
     // QK of step gq may be issued once P V of step gq - NS was (its S slot then
     // holds nothing the tensor core still reads: tcgen05 MMAs of one thread run
@@ -277,8 +346,9 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
                warp_wait(k_bar, k_par, a.status);
           if (!ok) break;
         } else {
-          const bool ready = __all_sync(0xffffffffu, (qk.j != 0 || mbar_try_wait(qtm_bar, qtm_par)) &&
-                                                         mbar_try_wait(k_bar, k_par));
+          const bool ready =
+              __all_sync(0xffffffffu, (qk.j != 0 || mbar_test_wait(qtm_bar, qtm_par)) &&
+                                          mbar_test_wait(k_bar, k_par));
           if (!ready) break;
         }
         tc_fence_after();
@@ -314,37 +384,38 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     umma_commit_elect(bar(B_MMADONE));
     warp_wait(bar(B_MMADONE), 0, a.status);   // nothing of ours still runs on the tensor core
   } else {
-    // ---------------- softmax: one thread per query row ----------------
-    const int row = tid;                            // warps 0-3: TMEM lane quarter = warp
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t o_tm = tmem + lane_off + kColO;
+    // ---------------- softmax: 8 warps, two per TMEM lane quarter ----------------
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;            // query row of the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t o_tm = tmem + lane_off + kColO + 64u * (uint32_t)half;   // this warp's O half
     const float sl2 = a.scale_log2;                 // >= 0 (checked by the planner)
+    float* xmax = reinterpret_cast<float*>(smem + kOffX);     // [2][2][128]
+    float* xsum = xmax + 2 * 2 * 128;                         // [2][128]
     bool ok = true;
-    // Q of local tile t: staging buffer t & 1 (row `row`, 128-byte swizzle)
-    // -> TMEM buffer t & 1, bf16 pairs per column, as the A operand of QK.
+    // Q of local tile t: staging buffer t & 1 (128-byte swizzle) -> TMEM Q
+    // buffer t & 1, bf16 pairs per column (the A operand of QK); this warp
+    // copies its rows' column block `half` (dims 64 half .. 64 half + 63).
     auto copy_q = [&](int t) -> bool {
       const int qb = t & 1;
-      if (!warp_wait(bar(B_QFULL + qb), (uint32_t)((t >> 1) & 1), a.status)) return false;
-      const uint8_t* src = smem + kOffQ + (uint32_t)qb * kQStage;
-      const uint32_t q_tm = tmem + lane_off + kColQ + (uint32_t)qb * 64u;
+      if (!warp_wait(bar(B_QFULL + qb), (uint32_t)((t >> 1) & 1), a.status))
+        return pair_all(1 + quarter, false);
+      const uint8_t* src = smem + kOffQ + (uint32_t)qb * kQStage + (uint32_t)half * kQBox;
+      uint32_t r[32];
 #pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        uint32_t r[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src + blk * kQBox + swz128((uint32_t)row, (uint32_t)c));
-          r[4 * c] = v.x;
-          r[4 * c + 1] = v.y;
-          r[4 * c + 2] = v.z;
-          r[4 * c + 3] = v.w;
-        }
-        tmem_st32(q_tm + 32u * (uint32_t)blk, r);
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + swz128((uint32_t)row, (uint32_t)cc));
+        r[4 * cc] = v.x;
+        r[4 * cc + 1] = v.y;
+        r[4 * cc + 2] = v.z;
+        r[4 * cc + 3] = v.w;
       }
+      tmem_st32(tmem + lane_off + kColQ + (uint32_t)qb * 64u + 32u * (uint32_t)half, r);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_QTM + qb));     // QK of tile t may read it
       mbar_arrive(bar(B_QEMPTY + qb));  // the staging buffer may take tile t + 2
-      return true;
+      return pair_all(1 + quarter, true);
     };
     StepCursor c;
     c.start(a);
@@ -368,19 +439,28 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       for (int j = 0; j < n_kv; ++j) {
         const int g = c.g, s = g % NS;
         // SFULL of slot s completes once per step that uses it, in order
-        if (!(ok = warp_wait(bar(B_SFULL + s), (uint32_t)((g / NS) & 1), a.status))) break;
+        const bool s_ok = warp_wait(bar(B_SFULL + s), (uint32_t)((g / NS) & 1), a.status);
         tc_fence_after();
         const uint32_t s_tm = tmem + lane_off + (uint32_t)s * 64u;
-        const int key0 = (kv0 + j) * kTileK;
-        const bool masked = __any_sync(0xffffffffu, key0 < lo || key0 + kTileK > hi);
-        uint32_t ra[32], rb[32];
-        tmem_ld32(s_tm, ra);
-        tmem_ld32(s_tm + 32u, rb);
-        tmem_wait_ld();
-        reg_fence32(ra);
-        reg_fence32(rb);
-        if (masked) mask_scores64(ra, rb, key0, lo, span);
-        const float mraw = row_max64(ra, rb);
+        const int key0 = (kv0 + j) * kTileK + 32 * half;   // this warp's 32 keys
+        const bool masked = __any_sync(0xffffffffu, key0 < lo || key0 + 32 > hi);
+        uint32_t ra[32];
+        float pm = neg_inf();
+        float* xm = xmax + (g & 1) * 256;
+        if (s_ok) {
+          tmem_ld32(s_tm + 32u * (uint32_t)half, ra);
+          tmem_wait_ld();
+          reg_fence32(ra);
+          if (masked) mask_scores32(ra, key0, lo, span);
+          pm = row_max32(ra);
+          // trade the partial maxima with the other half's warp.  The slot of
+          // step g is rewritten at step g + 2, after both warps passed step
+          // g + 1's barrier.
+          xm[half * 128 + row] = pm;
+        }
+        if (!(ok = pair_all(1 + quarter, s_ok))) break;
+        const float mraw = fmaxf(pm, xm[(1 - half) * 128 + row]);
+        // both warps of the pair now hold S in registers: P may overwrite it
         const float mx = mraw == neg_inf() ? neg_inf() : mraw * sl2;
         const bool grow = mx > m_ref + kRescaleThreshold;
         const float m_new = grow ? mx : m_ref;
@@ -390,15 +470,15 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           // slot completed the phase before (P V of g - 1 - NS): S of step g is
           // full, and QK of g was issued after P V of g - NS.
           const int gp = g - 1;
-          if (!(ok = warp_wait(bar(B_ODONE + gp % NS), (uint32_t)((gp / NS) & 1), a.status)))
-            break;
+          ok = warp_wait(bar(B_ODONE + gp % NS), (uint32_t)((gp / NS) & 1), a.status);
+          if (!(ok = pair_all(1 + quarter, ok))) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < kD / 32; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t r[32];
             tmem_ld32_sync(o_tm + (uint32_t)cc * 32u, r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            for (int i2 = 0; i2 < 32; ++i2) r[i2] = __float_as_uint(__uint_as_float(r[i2]) * alpha);
             tmem_st32(o_tm + (uint32_t)cc * 32u, r);
           }
           tmem_wait_st();
@@ -407,11 +487,11 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         const float neg_m = -m_ref;
         const bool zero_again =
             masked && __any_sync(0xffffffffu, !(sl2 > 0.f) || m_ref == neg_inf());
-        const float2 sum = zero_again
-                               ? exp_tile<true, F16>(ra, rb, sl2, neg_m, key0, lo, span, s_tm)
-                               : exp_tile<false, F16>(ra, rb, sl2, neg_m, key0, lo, span, s_tm);
+        const uint32_t p_tm = s_tm + 16u * (uint32_t)half;   // P of keys 32 half .. : 16 columns
+        const float sum = zero_again ? exp_half<true, F16>(ra, sl2, neg_m, key0, lo, span, p_tm)
+                                     : exp_half<false, F16>(ra, sl2, neg_m, key0, lo, span, p_tm);
         tmem_wait_st();
-        l = l * alpha + (sum.x + sum.y);
+        l = l * alpha + sum;
         tc_fence_before();
         mbar_arrive(bar(B_PFULL + s));
         g_last = g;
@@ -420,85 +500,81 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       if (!ok) break;
       // the next tile's Q into TMEM first: its QKs run while this tile's O is written
       if (!c.done() && !(ok = copy_q(c.t))) break;
-      // O is complete once P V of the tile's last step is (the phase before,
-      // P V of g_last - NS, completed: S of g_last is full)
-      if (!(ok = warp_wait(bar(B_ODONE + g_last % NS), (uint32_t)((g_last / NS) & 1), a.status)))
-        break;
+      // the row sum of both halves (the slot is rewritten only after the next
+      // tile's barriers).  O is complete once P V of the tile's last step is
+      // (the phase before, P V of g_last - NS, completed: S of g_last is full).
+      xsum[half * 128 + row] = l;
+      ok = warp_wait(bar(B_ODONE + g_last % NS), (uint32_t)((g_last / NS) & 1), a.status);
+      if (!(ok = pair_all(1 + quarter, ok))) break;
+      const float l_row = l + xsum[(1 - half) * 128 + row];
       tc_fence_after();
-      const float inv = l > 0.f ? a.output_scale / l : 0.f;
-      const int h_out = h;
+      const float inv = l_row > 0.f ? a.output_scale / l_row : 0.f;
+      uint32_t o[2][32];
+      tmem_ld32(o_tm, o[0]);
+      tmem_ld32(o_tm + 32u, o[1]);
+      tmem_wait_ld();
+      reg_fence32(o[0]);
+      reg_fence32(o[1]);
+      tc_fence_before();
+      mbar_arrive(bar(B_OFREE));   // the next tile's first P V may overwrite O
+      const int64_t row_elem = ((int64_t)(q0 + t_idx) * a.num_qo_heads + h) * kD + 64 * half;
       if (a.out_dtype == PKA_DTYPE_F32) {
-        uint32_t o[kD / 32][32];
-#pragma unroll
-        for (int cc = 0; cc < kD / 32; ++cc) tmem_ld32(o_tm + (uint32_t)cc * 32u, o[cc]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < kD / 32; ++cc) reg_fence32(o[cc]);
-        tc_fence_before();
-        mbar_arrive(bar(B_OFREE));   // the next tile's first P V may overwrite O
         if (row_valid) {
-          const int64_t dst = ((int64_t)(q0 + t_idx) * a.num_qo_heads + h_out) * kD;
 #pragma unroll
-          for (int cc = 0; cc < kD / 32; ++cc)
+          for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
             for (int qd = 0; qd < 2; ++qd) {
               float f[16];
 #pragma unroll
               for (int x = 0; x < 16; ++x) f[x] = __uint_as_float(o[cc][16 * qd + x]);
-              store_out<16>(a.out, dst + cc * 32 + qd * 16, f, inv, a.out_dtype);
+              store_out<16>(a.out, row_elem + cc * 32 + qd * 16, f, inv, a.out_dtype);
             }
         }
       } else {
-        // 16-bit O: each warp stages its 32 rows (16-byte chunks XOR-swizzled
-        // by row) and writes whole rows back, two per store instruction
-        constexpr int kRowBytes = kD * 2, kLanesPerRow = kRowBytes / 16;
-        uint8_t* wbuf = smem + kOffEpi + (uint32_t)warp * 32u * kRowBytes;
+        // 16-bit O: the warp stages its 32 half-rows (128 bytes each, 16-byte
+        // chunks XOR-swizzled by row), then writes them back four rows per
+        // store instruction (whole 128-byte segments instead of 32 rows per store)
+        uint8_t* wbuf = smem + kOffEpi + (uint32_t)warp * 32u * 128u;
         const bool f16o = a.out_dtype == PKA_DTYPE_F16;
-#pragma unroll 1
-        for (int cc = 0; cc < kD / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32_sync(o_tm + (uint32_t)cc * 32u, r);
-          if (cc == kD / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(bar(B_OFREE));
-          }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             uint32_t w[4];
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
-              const float lo_v = __uint_as_float(r[8 * k + 2 * x]) * inv;
-              const float hi_v = __uint_as_float(r[8 * k + 2 * x + 1]) * inv;
+              const float lo_v = __uint_as_float(o[cc][8 * k + 2 * x]) * inv;
+              const float hi_v = __uint_as_float(o[cc][8 * k + 2 * x + 1]) * inv;
               w[x] = f16o ? pack2<true>(lo_v, hi_v) : pack2<false>(lo_v, hi_v);
             }
             const int qc = cc * 4 + k;
-            *reinterpret_cast<uint4*>(wbuf + lane * kRowBytes + ((qc ^ (lane & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(wbuf + lane * 128 + ((qc ^ (lane & 7)) << 4)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
           }
-        }
         __syncwarp();
-        const int qc = lane % kLanesPerRow;
-#pragma unroll 4
-        for (int r0 = 0; r0 < 32; r0 += 32 / kLanesPerRow) {
-          const int rr = r0 + lane / kLanesPerRow;
-          const int tr = mt * kTileQ + warp * 32 + rr;
+        const int qc = lane & 7;
+#pragma unroll
+        for (int r0 = 0; r0 < 32; r0 += 4) {
+          const int rr = r0 + (lane >> 3);
+          const int tr = mt * kTileQ + quarter * 32 + rr;
           const uint4 val =
-              *reinterpret_cast<const uint4*>(wbuf + rr * kRowBytes + ((qc ^ (rr & 7)) << 4));
+              *reinterpret_cast<const uint4*>(wbuf + rr * 128 + ((qc ^ (rr & 7)) << 4));
           if (tr < Lq)
             *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
-                                      ((int64_t)(q0 + tr) * a.num_qo_heads + h_out) * kRowBytes +
-                                      qc * 16) = val;
+                                      (((int64_t)(q0 + tr) * a.num_qo_heads + h) * kD +
+                                       64 * half) * 2 + qc * 16) = val;
         }
         __syncwarp();   // the staging rows are read before the next tile writes them
       }
-      if (row_valid && a.lse != nullptr)
-        a.lse[(int64_t)(q0 + t_idx) * a.num_qo_heads + h_out] = l > 0.f ? m_ref + log2f(l) : neg_inf();
+      if (half == 0 && row_valid && a.lse != nullptr)
+        a.lse[(int64_t)(q0 + t_idx) * a.num_qo_heads + h] =
+            l_row > 0.f ? m_ref + log2f(l_row) : neg_inf();
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 6) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
