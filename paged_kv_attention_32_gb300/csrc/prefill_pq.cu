@@ -29,6 +29,9 @@
 //              lane, four chained k-steps per asm block).
 // TMEM (512 columns): S slots [0, 256) (4 x 64), O [256, 384), Q buffers
 // [384, 448) and [448, 512) (two tiles' Q, bf16 pairs per column).
+#include <cstdlib>
+#include <string>
+
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
@@ -44,8 +47,6 @@ using namespace dev;
 namespace {
 
 constexpr int kTileQ = 128, kTileK = 64, kD = 128;
-constexpr int NS = 4;                          // S slots (QK runs up to NS - 1 tiles ahead)
-constexpr int NK = 4, NV = 3;                  // K and V stages
 constexpr uint32_t kQBox = 16384;              // 128 rows x 128 bytes (64 columns)
 constexpr uint32_t kKBox = 8192;               // 64 rows x 128 bytes
 constexpr uint32_t kQStage = 2 * kQBox;        // one tile's Q (two column blocks)
@@ -54,36 +55,24 @@ constexpr int kSoftmaxWarps = 8, kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kWarpK = 8, kWarpV = 9, kWarpMma = 10;
 constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 constexpr float kRescaleThreshold = 8.0f;
-constexpr uint32_t kColO = NS * 64, kColQ = kColO + kD;
+constexpr uint32_t kXBytes = (2 * 2 + 2) * 128 * 4;     // row max [parity][half][row], sum [half][row]
 
-constexpr uint32_t kOffQ = 0;                           // 2 Q staging buffers
-constexpr uint32_t kOffEpi = kOffQ + 2 * kQStage;       // O staging (16-bit outputs)
-constexpr uint32_t kOffK = kOffEpi + 128u * kD * 2;     // K stages
-constexpr uint32_t kOffV = kOffK + NK * kKVStage;       // V stages
-constexpr uint32_t kOffBar = kOffV + NV * kKVStage;
-constexpr uint32_t kOffX = kOffBar + 512;               // row-max / row-sum exchange
-constexpr uint32_t kXBytes = (2 * 2 + 2) * 128 * 4;     // max [parity][half][row], sum [half][row]
-constexpr size_t kSmemBytes = 1024 + kOffX + kXBytes;
-
-// mbarriers.  A parity wait is only correct when the barrier has completed
-// the phase before the awaited one; the argument for each is given where it
-// is waited on.
-enum {
-  B_QFULL = 0,              // [2] Q staging buffer b holds tile 2k + b (TMA, tx bytes)
-  B_QEMPTY = 2,             // [2] softmax copied that Q into TMEM (256 arrivals)
-  B_QTM = 4,                // [2] Q of tile 2k + b is in TMEM buffer b (256 arrivals)
-  B_KFULL = 6,              // [NK]
-  B_KEMPTY = B_KFULL + NK,  // [NK] QK of the step that used the stage completed
-  B_VFULL = B_KEMPTY + NK,  // [NV]
-  B_VEMPTY = B_VFULL + NV,  // [NV] P V of the step completed
-  B_SFULL = B_VEMPTY + NV,  // [NS] S of the step is in its slot
-  B_PFULL = B_SFULL + NS,   // [NS] P of the step is in its slot (256 arrivals)
-  B_ODONE = B_PFULL + NS,   // [NS] P V of the step completed
-  B_OFREE = B_ODONE + NS,   // softmax read O of a finished tile (256 arrivals)
-  B_MMADONE = B_OFREE + 1,
-  B_COUNT = B_MMADONE + 1
+// Shared memory: two Q staging buffers (each also the output staging of the
+// tile before the one whose Q it held), NK K stages, NV V stages, barriers,
+// the row-max / row-sum exchange.  TMEM: NS S slots of 64 columns, O, two Q
+// buffers.
+template <int NS, int NK, int NV>
+struct PqLayout {
+  static constexpr uint32_t kColO = NS * 64, kColQ = kColO + kD;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOffQ + 2 * kQStage;
+  static constexpr uint32_t kOffV = kOffK + NK * kKVStage;
+  static constexpr uint32_t kOffBar = kOffV + NV * kKVStage;
+  static constexpr uint32_t kOffX = kOffBar + 512;
+  static constexpr size_t kSmemBytes = 1024 + kOffX + kXBytes;
+  static_assert(kColQ + 2 * 64 <= 512, "TMEM columns");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
-static_assert(B_COUNT * 8 + 16 <= 512, "barrier area");
 
 template <bool F16> constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, 0, 0, F16);
 template <bool F16> constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kD, 0, 1, F16);
@@ -188,10 +177,31 @@ struct StepCursor {
   }
 };
 
-template <bool F16>
+template <int NS, int NK, int NV, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  using Lay = PqLayout<NS, NK, NV>;
+  constexpr uint32_t kColO = Lay::kColO, kColQ = Lay::kColQ;
+  constexpr uint32_t kOffQ = Lay::kOffQ, kOffK = Lay::kOffK, kOffV = Lay::kOffV;
+  constexpr uint32_t kOffBar = Lay::kOffBar, kOffX = Lay::kOffX;
+  // mbarriers.  A parity wait is only correct when the barrier has completed
+  // the phase before the awaited one; the argument for each is given where it
+  // is waited on.
+  constexpr int B_QFULL = 0;               // [2] Q staging buffer b holds tile 2k + b (TMA)
+  constexpr int B_QEMPTY = 2;              // [2] staging buffer b may take the next Q (256)
+  constexpr int B_QTM = 4;                 // [2] Q of tile 2k + b is in TMEM buffer b (256)
+  constexpr int B_KFULL = 6;               // [NK]
+  constexpr int B_KEMPTY = B_KFULL + NK;   // [NK] QK of the step that used the stage completed
+  constexpr int B_VFULL = B_KEMPTY + NK;   // [NV]
+  constexpr int B_VEMPTY = B_VFULL + NV;   // [NV] P V of the step completed
+  constexpr int B_SFULL = B_VEMPTY + NV;   // [NS] S of the step is in its slot
+  constexpr int B_PFULL = B_SFULL + NS;    // [NS] P of the step is in its slot (256)
+  constexpr int B_ODONE = B_PFULL + NS;    // [NS] P V of the step completed
+  constexpr int B_OFREE = B_ODONE + NS;    // softmax read O of a finished tile (256)
+  constexpr int B_MMADONE = B_OFREE + 1;
+  constexpr int B_COUNT = B_MMADONE + 1;
+  static_assert(B_COUNT * 8 + 16 <= 512, "barrier area");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -414,7 +424,9 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_QTM + qb));     // QK of tile t may read it
-      mbar_arrive(bar(B_QEMPTY + qb));  // the staging buffer may take tile t + 2
+      // the staging buffer may take tile t + 2 now for tile 0; for a later
+      // tile it first stages the output of tile t - 1 (released after that)
+      if (t == 0) mbar_arrive(bar(B_QEMPTY + qb));
       return pair_all(1 + quarter, true);
     };
     StepCursor c;
@@ -436,6 +448,7 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       const unsigned span = (unsigned)(hi - lo);
       float m_ref = neg_inf(), l = 0.f;
       int g_last = c.g;
+      const int t_fin = c.t;
       for (int j = 0; j < n_kv; ++j) {
         const int g = c.g, s = g % NS;
         // SFULL of slot s completes once per step that uses it, in order
@@ -509,6 +522,7 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       const float l_row = l + xsum[(1 - half) * 128 + row];
       tc_fence_after();
       const float inv = l_row > 0.f ? a.output_scale / l_row : 0.f;
+      const int stg = (t_fin + 1) & 1;   // staging buffer of Q(t + 1), copied out above
       uint32_t o[2][32];
       tmem_ld32(o_tm, o[0]);
       tmem_ld32(o_tm + 32u, o[1]);
@@ -534,7 +548,8 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         // 16-bit O: the warp stages its 32 half-rows (128 bytes each, 16-byte
         // chunks XOR-swizzled by row), then writes them back four rows per
         // store instruction (whole 128-byte segments instead of 32 rows per store)
-        uint8_t* wbuf = smem + kOffEpi + (uint32_t)warp * 32u * 128u;
+        // this warp's 4 KB of the staging buffer hold the Q rows it copied itself
+        uint8_t* wbuf = smem + kOffQ + (uint32_t)stg * kQStage + (uint32_t)warp * 32u * 128u;
         const bool f16o = a.out_dtype == PKA_DTYPE_F16;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
@@ -569,6 +584,10 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       if (half == 0 && row_valid && a.lse != nullptr)
         a.lse[(int64_t)(q0 + t_idx) * a.num_qo_heads + h] =
             l_row > 0.f ? m_ref + log2f(l_row) : neg_inf();
+      // the staging buffer may take the Q of the tile after next (a TMA write:
+      // the generic accesses above are ordered before it)
+      fence_proxy_async_smem();
+      mbar_arrive(bar(B_QEMPTY + stg));
     }
   }
 
@@ -578,6 +597,22 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+template <int NS, int NK, int NV>
+int launch_pq(const pka_prefill_plan& plan, const PrefillArgs& args, const CUtensorMap& qmap,
+              const CUtensorMap& kmap, const CUtensorMap& vmap, int sms, cudaStream_t stream) {
+  const bool f16 = plan.desc.dtype == PKA_DTYPE_F16;
+  auto kern = f16 ? prefill_pq_kernel<NS, NK, NV, true> : prefill_pq_kernel<NS, NK, NV, false>;
+  constexpr size_t smem = PqLayout<NS, NK, NV>::kSmemBytes;
+  static std::atomic<uint64_t> smem_set[2];   // per input type: devices whose limit was raised
+  cudaError_t e = set_smem_once(kern, (int)smem, smem_set[f16]);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_pq)");
+  const int grid = args.num_tiles < sms ? args.num_tiles : sms;
+  kern<<<grid, kThreads, smem, stream>>>(args, qmap, kmap, vmap);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "prefill_pq_kernel launch");
+  return PKA_OK;
 }
 
 }  // namespace
@@ -590,15 +625,13 @@ int launch_prefill_pq(const pka_prefill_plan& plan, const PrefillArgs& args,
   PKA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
   PKA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
                "cudaDeviceGetAttribute(SM count)");
-  auto kern = plan.desc.dtype == PKA_DTYPE_F16 ? prefill_pq_kernel<true> : prefill_pq_kernel<false>;
-  static std::atomic<uint64_t> smem_set[2];   // per input type: devices whose limit was raised
-  cudaError_t e = set_smem_once(kern, (int)kSmemBytes, smem_set[plan.desc.dtype == PKA_DTYPE_F16]);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_pq)");
-  const int grid = args.num_tiles < sms ? args.num_tiles : sms;
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(args, qmap, kmap, vmap);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "prefill_pq_kernel launch");
-  return PKA_OK;
+  const char* cfg = std::getenv("PKA_PQ_CFG");
+  const std::string c = cfg ? cfg : "";
+  if (c == "363") return launch_pq<3, 6, 3>(plan, args, qmap, kmap, vmap, sms, stream);
+  if (c == "454") return launch_pq<4, 5, 4>(plan, args, qmap, kmap, vmap, sms, stream);
+  if (c == "372") return launch_pq<3, 7, 2>(plan, args, qmap, kmap, vmap, sms, stream);
+  if (c == "443") return launch_pq<4, 4, 3>(plan, args, qmap, kmap, vmap, sms, stream);
+  return launch_pq<4, 6, 3>(plan, args, qmap, kmap, vmap, sms, stream);
 }
 
 }  // namespace pka
