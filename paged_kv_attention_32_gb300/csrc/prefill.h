@@ -11,14 +11,17 @@
 
 namespace pka {
 
-// One CTA of the prefill kernel: a 128-row query tile of one request for one
-// query head.
-struct PrefillTile {
-  int32_t request;
-  int32_t head;     // first query head of the tile
+// One unit of prefill work: a 128-row query tile of one request for one
+// query head, with the request's offsets (32 bytes, two aligned loads).
+struct alignas(16) PrefillTile {
+  int32_t head;     // query head
   int32_t q_tile;   // 128-row tile index inside the request
   int32_t n_kv;     // KV tiles (64 keys) the tile visits
   int32_t kv0;      // first of them (past 0 only with a window)
+  int32_t q0;       // the request's first packed query row (qo_indptr[b])
+  int32_t lq;       // its query rows
+  int32_t k0;       // its first packed key row (kv_indptr[b])
+  int32_t lk;       // its keys
 };
 
 struct PrefillArgs {

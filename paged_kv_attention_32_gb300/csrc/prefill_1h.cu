@@ -98,10 +98,10 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PrefillTile tile = a.tiles[blockIdx.x];
-  const int b = tile.request, h = tile.head, mt = tile.q_tile, n_kv = tile.n_kv;
+  const int h = tile.head, mt = tile.q_tile, n_kv = tile.n_kv;
   const int kv0 = tile.kv0;
-  const int q0 = a.qo_indptr[b], Lq = a.qo_indptr[b + 1] - q0;
-  const int k0 = a.kv_indptr[b], Lk = a.kv_indptr[b + 1] - k0;
+  const int q0 = tile.q0, Lq = tile.lq;
+  const int k0 = tile.k0, Lk = tile.lk;
   const int hk = h / a.group;
 
   if (tid == 0) {

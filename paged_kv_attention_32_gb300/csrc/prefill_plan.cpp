@@ -97,7 +97,8 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
       const int32_t n_kv = (int32_t)(ceil_div(hi, kTileK) - kv0);
       PKA_CHECK_ARG(n_kv >= 1, "request %d: a query tile with no key tile", b);
       for (int32_t h = 0; h < p.Hq; ++h)
-        p.tiles.push_back(PrefillTile{b, h, (int32_t)m, n_kv, kv0});
+        p.tiles.push_back(PrefillTile{h, (int32_t)m, n_kv, kv0, qo[b], (int32_t)lq, kv[b],
+                                      (int32_t)lk});
     }
   }
   std::stable_sort(p.tiles.begin(), p.tiles.end(),

@@ -158,21 +158,28 @@ __device__ __forceinline__ int tile_of(int r, int cta, int ctas, int num_tiles) 
 
 // Walks the CTA's tiles and the 64-key steps inside them, in the order every
 // role uses (t: local tile count, j: step in the tile, g: step count).  The
-// planner gives every tile at least one key tile.
+// next tile's description is loaded one tile ahead, so that no role waits on
+// a global load at a tile change.  The planner gives every tile at least one
+// key tile.
 struct StepCursor {
-  int t = 0, j = 0, g = 0, n_kv = 0, tile = -1;
+  int t = 0, j = 0, g = 0, tile = -1, next = -1;
+  PrefillTile cur, nxt;
   __device__ __forceinline__ void start(const PrefillArgs& a) {
     tile = tile_of(0, blockIdx.x, gridDim.x, a.num_tiles);
-    n_kv = tile >= 0 ? a.tiles[tile].n_kv : 0;
+    next = tile_of(1, blockIdx.x, gridDim.x, a.num_tiles);
+    if (tile >= 0) cur = a.tiles[tile];
+    if (next >= 0) nxt = a.tiles[next];
   }
   __device__ __forceinline__ bool done() const { return tile < 0; }
   __device__ __forceinline__ void advance(const PrefillArgs& a) {
     ++g;
-    if (++j == n_kv) {
+    if (++j == cur.n_kv) {
       ++t;
       j = 0;
-      tile = tile_of(t, blockIdx.x, gridDim.x, a.num_tiles);
-      n_kv = tile >= 0 ? a.tiles[tile].n_kv : 0;
+      tile = next;
+      cur = nxt;
+      next = tile_of(t + 1, blockIdx.x, gridDim.x, a.num_tiles);
+      if (next >= 0) nxt = a.tiles[next];
     }
   }
 };
@@ -251,17 +258,15 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       // Q of local tile t into staging buffer t & 1.  For t >= 2 the buffer is
       // free once the softmax copied Q of tile t - 2 into TMEM (release number
       // (t >> 1) - 1 of that buffer's QEMPTY; the one after it needs this load).
-      auto load_q = [&](int t, int tile) -> bool {
+      auto load_q = [&](int t, const PrefillTile& tl) -> bool {
         const int qb = t & 1;
         if (t >= 2 && !mbar_wait(bar(B_QEMPTY + qb), (uint32_t)(((t >> 1) - 1) & 1), a.status))
           return false;
-        const PrefillTile tl = a.tiles[tile];
-        const int q0 = a.qo_indptr[tl.request];
         const uint32_t dst = sbase + kOffQ + (uint32_t)qb * kQStage;
         mbar_arrive_expect_tx(bar(B_QFULL + qb), kQStage);
         for (int blk = 0; blk < 2; ++blk)
           tma_load_3d(dst + (uint32_t)blk * kQBox, &tmq, bar(B_QFULL + qb), blk * 64, tl.head,
-                      q0 + tl.q_tile * kTileQ);
+                      tl.q0 + tl.q_tile * kTileQ);
         return true;
       };
       StepCursor c;
@@ -270,7 +275,7 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       int q_loaded = 0;   // Q tiles issued (local tile numbers 0 .. q_loaded - 1)
       int last_k = -1;
       if (!c.done()) {
-        ok = load_q(0, c.tile);
+        ok = load_q(0, c.cur);
         q_loaded = ok;
       }
       while (ok && !c.done()) {
@@ -280,21 +285,21 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           ok = false;
           break;
         }
-        const PrefillTile tl = a.tiles[c.tile];
-        const int hk = tl.head / a.group;
-        const int k0 = a.kv_indptr[tl.request];
+        const PrefillTile& tl = c.cur;
         const uint32_t dst = sbase + kOffK + (uint32_t)st * kKVStage;
         mbar_arrive_expect_tx(bar(B_KFULL + st), kKVStage);
         for (int blk = 0; blk < 2; ++blk)
-          tma_load_3d(dst + (uint32_t)blk * kKBox, &tmk, bar(B_KFULL + st), blk * 64, hk,
-                      k0 + (tl.kv0 + c.j) * kTileK);
+          tma_load_3d(dst + (uint32_t)blk * kKBox, &tmk, bar(B_KFULL + st), blk * 64,
+                      tl.head / a.group, tl.k0 + (tl.kv0 + c.j) * kTileK);
         last_k = g;
-        c.advance(a);
         // once the first K tile of tile t is out, Q of tile t + 1
-        const int nt = tile_of(t + 1, blockIdx.x, gridDim.x, a.num_tiles);
-        if (first && nt >= 0) {
+        if (first && c.next >= 0) {
+          const PrefillTile nt = c.nxt;
+          c.advance(a);
           ok = load_q(t + 1, nt);
           q_loaded += ok;
+        } else {
+          c.advance(a);
         }
       }
       if (!ok) {   // give the copies already issued a bounded chance to land
@@ -319,14 +324,12 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           ok = false;
           break;
         }
-        const PrefillTile tl = a.tiles[c.tile];
-        const int hk = tl.head / a.group;
-        const int k0 = a.kv_indptr[tl.request];
+        const PrefillTile& tl = c.cur;
         const uint32_t dst = sbase + kOffV + (uint32_t)st * kKVStage;
         mbar_arrive_expect_tx(bar(B_VFULL + st), kKVStage);
         for (int blk = 0; blk < 2; ++blk)
-          tma_load_3d(dst + (uint32_t)blk * kKBox, &tmv, bar(B_VFULL + st), blk * 64, hk,
-                      k0 + (tl.kv0 + c.j) * kTileK);
+          tma_load_3d(dst + (uint32_t)blk * kKBox, &tmv, bar(B_VFULL + st), blk * 64,
+                      tl.head / a.group, tl.k0 + (tl.kv0 + c.j) * kTileK);
         last_v = g;
         c.advance(a);
       }
@@ -433,10 +436,9 @@ prefill_pq_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     c.start(a);
     if (!c.done()) ok = copy_q(0);
     while (ok && !c.done()) {
-      const PrefillTile tl = a.tiles[c.tile];
-      const int b = tl.request, h = tl.head, mt = tl.q_tile, n_kv = tl.n_kv, kv0 = tl.kv0;
-      const int q0 = a.qo_indptr[b], Lq = a.qo_indptr[b + 1] - q0;
-      const int Lk = a.kv_indptr[b + 1] - a.kv_indptr[b];
+      const PrefillTile tl = c.cur;
+      const int h = tl.head, mt = tl.q_tile, n_kv = tl.n_kv, kv0 = tl.kv0;
+      const int q0 = tl.q0, Lq = tl.lq, Lk = tl.lk;
       const int t_idx = mt * kTileQ + row;
       const bool row_valid = t_idx < Lq;
       int hi = a.causal ? min(Lk, Lk - Lq + t_idx + 1) : Lk;   // keys [lo, hi) visible
