@@ -64,20 +64,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of phase `parity` (mbarrier.try_wait may suspend the
-// thread for a while before it reports "not yet"; this returns at once).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Waits for phase `parity` of the barrier to complete.  Gives up after
 // limit_ns, OR-ing STATUS_WAIT_TIMEOUT into *status; returns false then.
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, int32_t* status,

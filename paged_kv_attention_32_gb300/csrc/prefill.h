@@ -53,7 +53,6 @@ struct pka_prefill_plan {
   pka_prefill_desc desc;
   int32_t B = 0, Hq = 0, Hkv = 0, G = 0, D = 0;
   int32_t total_q = 0, total_kv = 0;
-  int32_t kernel = 0;   // head_dim 128: 1 = persistent Q-in-TMEM kernel, 0 = one CTA per tile
   float scale = 0.f;
   std::vector<int32_t> qo, kv;
   std::vector<int32_t> win_lo, win_hi;   // variable_window bounds per query row (host)
@@ -76,12 +75,6 @@ namespace pka {
 int build_prefill_plan(pka_prefill_plan& plan, const pka_prefill_desc& desc, const int32_t* qo,
                        const int32_t* kv, const int32_t* win_lo = nullptr,
                        const int32_t* win_hi = nullptr);
-
-// Launches the persistent head_dim 128 prefill kernel (one CTA per SM, Q in
-// tensor memory) over the plan's tiles.
-int launch_prefill_pq(const pka_prefill_plan& plan, const PrefillArgs& args,
-                      const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                      cudaStream_t stream);
 
 // Launches the prefill kernel (one query head and 128 rows per CTA, 64-key
 // tiles; head_dim 128 or 256) over the plan's tiles.

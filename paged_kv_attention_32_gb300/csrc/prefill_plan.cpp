@@ -6,8 +6,6 @@
 // long causal rows out before the short ones (longest-processing-time order).
 #include <algorithm>
 #include <cmath>
-#include <cstdlib>
-#include <string>
 
 #include "host_common.h"
 #include "prefill.h"
@@ -103,10 +101,6 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
   }
   std::stable_sort(p.tiles.begin(), p.tiles.end(),
                    [](const PrefillTile& a, const PrefillTile& b) { return a.n_kv > b.n_kv; });
-  {
-    const char* k = std::getenv("PKA_PREFILL_KERNEL");
-    p.kernel = (k != nullptr && std::string(k) == "1h") ? 0 : 1;
-  }
   p.total_q = qo[B];
   p.total_kv = kv[B];
   PKA_CHECK_ARG(p.tiles.size() < (size_t)INT32_MAX, "too many prefill tiles");
