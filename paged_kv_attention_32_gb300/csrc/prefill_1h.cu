@@ -233,7 +233,11 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       tmem_wait_ld();
       reg_fence32(ra);
       reg_fence32(rb);
-      if (masked) mask_scores64(ra, rb, key0, lo, span);
+      uint32_t w0 = 0xffffffffu, w1 = 0xffffffffu;
+      if (masked) {
+        visible_bits(key0, lo, span, w0, w1);
+        mask_scores64(ra, rb, w0, w1);
+      }
       const float mraw = row_max64(ra, rb);
       // lazy rescale: move the reference max only when it grew by more than 2^8
       const float mx = mraw == neg_inf() ? neg_inf() : mraw * sl2;
@@ -257,14 +261,14 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         tmem_wait_st();
       }
       m_ref = m_new;
-      const float neg_m = -m_ref;
-      // the masked scores are -inf now, so exp2(s * sl2 - m) is already 0 for them
-      // unless sl2 is 0 or the row has no finite reference yet (-inf + inf = NaN)
-      const bool zero_again =
-          masked && __any_sync(0xffffffffu, !(sl2 > 0.f) || m_ref == neg_inf());
+      // A row with no visible key so far keeps m_ref = -inf: its scores here
+      // are all -inf, and exp2(-inf * sl2 + 0) = 0 (-inf - -inf would be NaN).
+      // Masked scores give 0 through their -inf unless the scale is 0.
+      const float neg_m = m_ref == neg_inf() ? 0.f : -m_ref;
+      const bool zero_again = masked && !(sl2 > 0.f);
       const float2 sum = zero_again
-                             ? exp_tile<true, F16>(ra, rb, sl2, neg_m, key0, lo, span, s_tm)
-                             : exp_tile<false, F16>(ra, rb, sl2, neg_m, key0, lo, span, s_tm);
+                             ? exp_tile<true, F16>(ra, rb, sl2, neg_m, w0, w1, s_tm)
+                             : exp_tile<false, F16>(ra, rb, sl2, neg_m, w0, w1, s_tm);
       tmem_wait_st();
       l = l * alpha + (sum.x + sum.y);
       tc_fence_before();
