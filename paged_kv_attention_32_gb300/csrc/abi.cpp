@@ -136,7 +136,9 @@ int upload_prefill_plan(pka_prefill_plan& p, cudaStream_t stream) {
   const size_t off_kv = off_qo + up256(n_ind);
   const size_t off_wlo = off_kv + up256(n_ind);
   const size_t off_whi = off_wlo + up256(n_win);
-  const size_t off_status = off_whi + up256(n_win);
+  const size_t n_map = p.row_map.size() * sizeof(int32_t);
+  const size_t off_map = off_whi + up256(n_win);
+  const size_t off_status = off_map + up256(n_map);
   const size_t total = off_status + 256;
   PKA_CUDA_TRY(cudaGetDevice(&p.device), "cudaGetDevice");
   PKA_CUDA_TRY(cudaMalloc(&p.dev_buf, total), "cudaMalloc(prefill plan)");
@@ -161,6 +163,12 @@ int upload_prefill_plan(pka_prefill_plan& p, cudaStream_t stream) {
     PKA_CUDA_TRY(cudaMemcpyAsync(base + off_whi, p.win_hi.data(), n_win, cudaMemcpyHostToDevice,
                                  stream),
                  "cudaMemcpyAsync(window ends)");
+  }
+  if (n_map) {
+    p.d_row_map = reinterpret_cast<const int32_t*>(base + off_map);
+    PKA_CUDA_TRY(cudaMemcpyAsync(base + off_map, p.row_map.data(), n_map, cudaMemcpyHostToDevice,
+                                 stream),
+                 "cudaMemcpyAsync(row order)");
   }
   PKA_CUDA_TRY(cudaMemsetAsync(base + off_status, 0, 256, stream), "cudaMemsetAsync(status)");
   return PKA_OK;
@@ -612,6 +620,7 @@ int batch_prefill_run(const pka_prefill_plan* p, const void* q, int64_t q_stride
   a.window_left = p->desc.window_left;
   a.window_lo = p->d_win_lo;
   a.window_hi = p->d_win_hi;
+  a.row_map = p->d_row_map;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.output_scale = p->desc.output_scale;
   a.out_dtype = p->desc.out_dtype;

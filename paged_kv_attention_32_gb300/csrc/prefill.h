@@ -42,6 +42,8 @@ struct PrefillArgs {
   int32_t window_left;   // -1: no window
   const int32_t* window_lo;   // variable_window: first key of each query row, else nullptr
   const int32_t* window_hi;   // variable_window: last key (inclusive) of each query row
+  const int32_t* row_map;     // nullptr, or per packed position the request-local query row
+                              // placed there (tiles then hold rows of similar windows)
   float scale_log2;
   float output_scale;
   int32_t out_dtype;       // PKA_DTYPE_BF16 / F16 / F32
@@ -56,6 +58,7 @@ struct pka_prefill_plan {
   float scale = 0.f;
   std::vector<int32_t> qo, kv;
   std::vector<int32_t> win_lo, win_hi;   // variable_window bounds per query row (host)
+  std::vector<int32_t> row_map;          // empty, or the query row order inside the tiles
   std::vector<pka::PrefillTile> tiles;
   void* dev_buf = nullptr;
   const pka::PrefillTile* d_tiles = nullptr;
@@ -63,6 +66,7 @@ struct pka_prefill_plan {
   const int32_t* d_kv = nullptr;
   const int32_t* d_win_lo = nullptr;
   const int32_t* d_win_hi = nullptr;
+  const int32_t* d_row_map = nullptr;
   int32_t* d_status = nullptr;
   int device = -1;
 };

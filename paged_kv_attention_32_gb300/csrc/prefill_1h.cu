@@ -104,8 +104,11 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   const int k0 = tile.k0, Lk = tile.lk;
   const int hk = h / a.group;
 
+  // Q rows in the order of a row map (variable_window tiles of similar
+  // windows) are gathered by the softmax threads, one row each; else one TMA copy
+  const bool gather_q = a.row_map != nullptr;
   if (tid == 0) {
-    mbar_init(bar(B_Q), 1);
+    mbar_init(bar(B_Q), gather_q ? 128 : 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
@@ -133,10 +136,12 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       tma_prefetch_desc(&tmq);
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
-      mbar_arrive_expect_tx(bar(B_Q), NB * kQBox);
-      for (int blk = 0; blk < NB; ++blk)
-        tma_load_3d(sbase + kOffQ + (uint32_t)blk * kQBox, &tmq, bar(B_Q), blk * 64, h,
-                    q0 + mt * kTileQ);
+      if (!gather_q) {
+        mbar_arrive_expect_tx(bar(B_Q), NB * kQBox);
+        for (int blk = 0; blk < NB; ++blk)
+          tma_load_3d(sbase + kOffQ + (uint32_t)blk * kQBox, &tmq, bar(B_Q), blk * 64, h,
+                      q0 + mt * kTileQ);
+      }
       auto load_kv = [&](int j, int which) -> bool {   // which: 0 = K, 1 = V
         const int st = j & 1;
         const int full = which ? B_VFULL : B_KFULL, empty = which ? B_VEMPTY : B_KEMPTY;
@@ -162,7 +167,7 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
         }
       }
       if (!ok) {   // give the copies already issued a bounded chance to land
-        mbar_wait(bar(B_Q), 0, nullptr);
+        if (!gather_q) mbar_wait(bar(B_Q), 0, nullptr);
         if (kd > 0) mbar_wait(bar(B_KFULL + ((kd - 1) & 1)), (uint32_t)(((kd - 1) >> 1) & 1), nullptr);
         if (vd > 0) mbar_wait(bar(B_VFULL + ((vd - 1) & 1)), (uint32_t)(((vd - 1) >> 1) & 1), nullptr);
       }
@@ -205,8 +210,24 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
   } else {
     // ---------------- softmax: one thread per query row ----------------
     const int row = tid;                       // warps 0-3
-    const int t = mt * kTileQ + row;
-    const bool row_valid = t < Lq;
+    const int pos = mt * kTileQ + row;         // the row's position in the request's tiles
+    const bool row_valid = pos < Lq;
+    const int t = gather_q && row_valid ? __ldg(a.row_map + q0 + pos) : pos;   // query row
+    if (gather_q) {
+      // this thread's Q row into the tile's shared-memory layout (128-byte
+      // swizzle, D / 64 column blocks), zeros past the request's rows
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const uint16_t*>(a.q) + (int64_t)(q0 + t) * a.q_stride_tok +
+          (int64_t)h * a.q_stride_head);
+#pragma unroll 4
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(smem + kOffQ + (uint32_t)(c >> 3) * kQBox +
+                                  swz128((uint32_t)row, (uint32_t)(c & 7))) = v;
+      }
+      fence_proxy_async_smem();   // generic writes -> the tensor core's operand reads
+      mbar_arrive(bar(B_Q));
+    }
     int hi = a.causal ? min(Lk, Lk - Lq + t + 1) : Lk;   // keys [lo, hi) visible
     int lo = a.window_left >= 0 ? min(hi, max(0, Lk - Lq + t - a.window_left)) : 0;
     if (a.window_lo != nullptr) {   // variable_window: the row's inclusive bounds
@@ -327,13 +348,15 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
 #pragma unroll 4
         for (int r0 = 0; r0 < 32; r0 += 32 / kLanesPerRow) {
           const int rr = r0 + lane / kLanesPerRow;
-          const int tr = mt * kTileQ + warp * 32 + rr;
+          const int pr = mt * kTileQ + warp * 32 + rr;
           const uint4 val =
               *reinterpret_cast<const uint4*>(wbuf + rr * kRowBytes + ((q ^ (rr & 7)) << 4));
-          if (tr < Lq)
+          if (pr < Lq) {
+            const int tr = gather_q ? __ldg(a.row_map + q0 + pr) : pr;
             *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
                                       ((int64_t)(q0 + tr) * a.num_qo_heads + h) * kRowBytes +
                                       q * 16) = val;
+          }
         }
       }
       if (row_valid && a.lse != nullptr)

@@ -5,7 +5,9 @@
 // (most KV tiles to visit), so that the hardware block scheduler hands the
 // long causal rows out before the short ones (longest-processing-time order).
 #include <algorithm>
+#include <climits>
 #include <cmath>
+#include <numeric>
 
 #include "host_common.h"
 #include "prefill.h"
@@ -13,8 +15,8 @@
 namespace pka {
 
 namespace {
-constexpr int kTileQ = 128;   // query rows per CTA
-constexpr int kTileK = 64;    // keys per K/V tile
+constexpr int kTileQ = 128;     // query rows per CTA
+constexpr int kTileK = 64;      // keys per K/V tile
 }  // namespace
 
 int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const int32_t* qo,
@@ -48,6 +50,9 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
     return fail(PKA_ERR_UNSUPPORTED, "prefill sm_scale must be >= 0 (got %g)", (double)d.sm_scale);
   PKA_CHECK_ARG(qo[0] == 0 && kv[0] == 0, "indptr arrays must start at 0");
   const int32_t B = d.batch_size;
+  for (int32_t b = 0; b < B; ++b)
+    PKA_CHECK_ARG(qo[b + 1] >= qo[b] && kv[b + 1] >= kv[b],
+                  "indptr arrays must be non-decreasing (request %d)", b);
   p.desc = d;
   p.B = B;
   p.Hq = d.num_qo_heads;
@@ -64,6 +69,62 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
     p.win_hi.assign(win_hi, win_hi + qo[B]);
   }
   p.tiles.clear();
+  p.row_map.clear();
+  if (varwin) {
+    // Tiles of rows with similar windows compute fewer invisible scores: each
+    // request's rows are ordered by their last key, cut into bands of a few
+    // tiles, and ordered by their first key inside a band.  The band size that
+    // needs the fewest key tiles is taken (it grows with the spread of the
+    // windows), and the order only where it needs fewer than the rows' own.
+    for (int32_t b = 0; b < B; ++b) {
+      const int64_t lk = (int64_t)kv[b + 1] - kv[b];
+      for (int64_t r = qo[b]; r < qo[b + 1]; ++r)
+        PKA_CHECK_ARG(win_lo[r] >= 0 && win_lo[r] <= win_hi[r] && win_hi[r] < lk,
+                      "request %d row %lld: window bounds [%d, %d] outside 0 <= start <= end < "
+                      "%lld", b, (long long)(r - qo[b]), win_lo[r], win_hi[r], (long long)lk);
+    }
+    std::vector<int32_t> order, best;
+    bool any = false;
+    p.row_map.resize(qo[B]);
+    for (int32_t b = 0; b < B; ++b) {
+      const int64_t lq = (int64_t)qo[b + 1] - qo[b];
+      const int32_t* s0 = win_lo + qo[b];
+      const int32_t* e0 = win_hi + qo[b];
+      auto key_tiles = [&](auto row_at) {
+        int64_t n = 0;
+        for (int64_t m = 0; m * kTileQ < lq; ++m) {
+          int64_t lo = INT64_MAX, hi = 0;
+          for (int64_t r = m * kTileQ; r < std::min<int64_t>(lq, (m + 1) * kTileQ); ++r) {
+            const int32_t i = row_at(r);
+            lo = std::min<int64_t>(lo, s0[i]);
+            hi = std::max<int64_t>(hi, (int64_t)e0[i] + 1);
+          }
+          n += ceil_div(hi, kTileK) - lo / kTileK;
+        }
+        return n;
+      };
+      int64_t best_n = key_tiles([&](int64_t r) { return (int32_t)r; });
+      best.clear();
+      for (int band : {2, 3, 4, 6, 8, 16}) {
+        order.resize(lq);
+        std::iota(order.begin(), order.end(), 0);
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int32_t x, int32_t y) { return e0[x] < e0[y]; });
+        for (int64_t r0 = 0; r0 < lq; r0 += (int64_t)band * kTileQ)
+          std::stable_sort(order.begin() + r0,
+                           order.begin() + std::min<int64_t>(lq, r0 + (int64_t)band * kTileQ),
+                           [&](int32_t x, int32_t y) { return s0[x] < s0[y]; });
+        const int64_t n = key_tiles([&](int64_t r) { return order[r]; });
+        if (n < best_n) {
+          best_n = n;
+          best = order;
+        }
+      }
+      for (int64_t r = 0; r < lq; ++r) p.row_map[qo[b] + r] = best.empty() ? (int32_t)r : best[r];
+      any = any || !best.empty();
+    }
+    if (!any) p.row_map.clear();
+  }
   for (int32_t b = 0; b < B; ++b) {
     const int64_t lq = (int64_t)qo[b + 1] - qo[b], lk = (int64_t)kv[b + 1] - kv[b];
     PKA_CHECK_ARG(lq >= 0 && lk >= 0, "indptr arrays must be non-decreasing (request %d)", b);
@@ -82,11 +143,9 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
       if (varwin) {   // the union of the tile's rows' bounds
         lo = lk;
         hi = 0;
-        for (int64_t r = first_row; r <= last_row; ++r) {
+        for (int64_t pos = first_row; pos <= last_row; ++pos) {
+          const int64_t r = p.row_map.empty() ? pos : p.row_map[qo[b] + pos];
           const int32_t s = win_lo[qo[b] + r], e = win_hi[qo[b] + r];
-          PKA_CHECK_ARG(s >= 0 && s <= e && e < lk,
-                        "request %d row %lld: window bounds [%d, %d] outside 0 <= start <= end < %lld",
-                        b, (long long)r, s, e, (long long)lk);
           lo = std::min<int64_t>(lo, s);
           hi = std::max<int64_t>(hi, (int64_t)e + 1);
         }

@@ -145,6 +145,33 @@ def test_prefill_variable_window(Hq, Hkv, seed):
                 variable_window_token_starts=st, variable_window_token_ends=en)
 
 
+@pytest.mark.parametrize("D,out_dtype", [(128, None), (128, torch.float32), (256, None)])
+def test_prefill_variable_window_reordered_rows(D, out_dtype):
+    """Row i sees [i - U(0, 511), i] (the bench's variable_window shape, smaller): the
+    planner groups rows of similar windows into tiles (rows ordered by last key in
+    bands of four tiles, by first key inside a band), so the kernel gathers Q rows
+    and scatters O / LSE rows through the row order."""
+    B, S, Hq, Hkv = 2, 1024, 4, 2
+    g = np.random.default_rng(100 + D)
+    i = np.arange(S)
+    st = (i - g.integers(0, 512, size=(B, S))).clip(0, None).astype(np.int32)
+    en = np.tile(i, (B, 1)).astype(np.int32)
+    q = _rand((B, S, Hq, D), 101)
+    k, v = _rand((B, S, Hkv, D), 102), _rand((B, S, Hkv, D), 103)
+    plan = api.batch_prefill_plan_fixed(B, S, S, num_qo_heads=Hq, num_kv_heads=Hkv,
+                                        mask_type="variable_window", head_dim=D,
+                                        variable_window_token_starts=st,
+                                        variable_window_token_ends=en, return_lse=True,
+                                        out_dtype=out_dtype)
+    out, lse = api.batch_prefill_run(plan, q, k, v)
+    torch.cuda.synchronize()
+    plan.check()
+    ref_o, ref_l = oracle.batch_prefill(wl.bf16_bits(q.flatten(0, 1)), wl.bf16_bits(k.flatten(0, 1)),
+                                        wl.bf16_bits(v.flatten(0, 1)), np.arange(B + 1) * S,
+                                        np.arange(B + 1) * S, Hkv, window_starts=st, window_ends=en)
+    _check(out.flatten(0, 1), lse.flatten(0, 1), ref_o, ref_l)
+
+
 @pytest.mark.parametrize("dtype,out_dtype", [(torch.float16, None), (torch.float16, torch.float32),
                                              (torch.bfloat16, torch.float32),
                                              (torch.bfloat16, torch.float16)])
