@@ -280,65 +280,86 @@ prefill_gh_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
     }
   } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
-    // Both QKs of step gq may be issued once both P Vs of step gq - 2 were
-    // (their S buffers then hold nothing the tensor core still reads:
-    // tcgen05 MMAs of one thread run in issue order), K of the step is in and
-    // its tile's Q is.  While some P V is still to issue, QK waits only by
-    // polling: the softmax may be waiting for that P V (lazy rescale, end of a
-    // tile) before it lets the next tile's Q in.
-    StepCursor qk, pv;
-    qk.start(a);
-    pv.start(a);
+    // The two heads advance on their own: the warp polls each head's next QK
+    // and next P V and issues whichever can go, so that a head whose P is
+    // late does not hold the other's work back (the tensor core runs one
+    // thread's MMAs in issue order).
+    //   QK of head e, step g: after P V of (e, g - 2) was issued (its S buffer
+    //     then holds nothing the tensor core still reads), K of g is in, and
+    //     the tile's Q is.  K's stage is released once both heads' QKs of g
+    //     were issued (the commit tracks every earlier MMA of this thread).
+    //   P V of head e, step g: P of (e, g) is in, V of g is, and for the first
+    //     step of tile t > 0 the softmax has read O of tile t - 1 (OFREE
+    //     completion t - 1 of the head; completion t needs this P V).  V's
+    //     stage is released once both heads' P Vs of g were issued.
+    // Every wait is a poll; a head that makes no progress for the bound of a
+    // wait gives up as the blocking waits do.
+    StepCursor qk[2], pv[2];
+    for (int e = 0; e < 2; ++e) {
+      qk[e].start(a);
+      pv[e].start(a);
+    }
     bool ok = true;
-    while (ok && !pv.done()) {
-      while (ok && !qk.done() && qk.g <= pv.g + 1) {
-        const int g = qk.g, t = qk.t;
-        const uint32_t q_bar = bar(B_QFULL + (t & 1)), q_par = (uint32_t)((t >> 1) & 1);
-        const uint32_t k_bar = bar(B_KFULL + g % NK), k_par = (uint32_t)((g / NK) & 1);
-        if (qk.g == pv.g) {   // nothing else to issue: block
-          ok = (qk.j != 0 || warp_wait(q_bar, q_par, a.status)) && warp_wait(k_bar, k_par, a.status);
-          if (!ok) break;
-        } else if (!__all_sync(0xffffffffu, (qk.j != 0 || mbar_test(q_bar, q_par)) &&
-                                               mbar_test(k_bar, k_par))) {
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kb = sbase + kOffK + (uint32_t)(g % NK) * kKVStage;
+    uint64_t t_idle = 0;
+    bool idle = false;
+    while (ok && !(pv[0].done() && pv[1].done())) {
+      bool progress = false;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint32_t d = tmem + 256u * (uint32_t)e + (uint32_t)(g & 1) * 64u;
-          const uint32_t qa = sbase + kOffQ + (uint32_t)(t & 1) * kQStage + (uint32_t)e * kQHead;
-#pragma unroll
-          for (int blk = 0; blk < 2; ++blk)   // 4 k-steps of 16 per 64-column block
-            umma_ss_k4(d, kmajor(qa, kQBox, 4 * blk), kmajor(kb, kKBox, 4 * blk), kIdescQK<F16>,
-                       blk > 0 ? 1u : 0u);
-          umma_commit_elect(bar(B_SFULL + 2 * e + (g & 1)));
-        }
-        umma_commit_elect(bar(B_KEMPTY + g % NK));
-        qk.advance(a);
-      }
-      if (!ok) break;
-      // both P Vs of step pv.g
-      const int g = pv.g, s = g & 1;
-      if (!(ok = warp_wait(bar(B_VFULL + g % NV), (uint32_t)((g / NV) & 1), a.status))) break;
-      const uint32_t vb = sbase + kOffV + (uint32_t)(g % NV) * kKVStage;
-#pragma unroll 1
       for (int e = 0; e < 2; ++e) {
-        ok = warp_wait(bar(B_PFULL + 2 * e + s), (uint32_t)((g >> 1) & 1), a.status);
-        // the first P V of tile t overwrites O: the softmax must have read tile
-        // t - 1's O (OFREE completion t - 1; completion t needs this P V)
-        if (ok && pv.j == 0 && pv.t > 0)
-          ok = warp_wait(bar(B_OFREE + e), (uint32_t)((pv.t - 1) & 1), a.status);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t p_tm = tmem + 256u * (uint32_t)e + (uint32_t)s * 64u;   // P: 32 columns
-        umma_ts_k4<2048 / 16>(tmem + 256u * (uint32_t)e + 128u, p_tm, vmn(vb, 0), kIdescPV<F16>,
-                              pv.j > 0 ? 1u : 0u);
-        umma_commit_elect(bar(B_ODONE + 2 * e + s));
+        StepCursor& q = qk[e];
+        if (!q.done() && q.g <= pv[e].g + 1) {
+          const int g = q.g, t = q.t;
+          const bool ready = __all_sync(
+              0xffffffffu, (q.j != 0 || mbar_test(bar(B_QFULL + (t & 1)), (uint32_t)((t >> 1) & 1))) &&
+                               mbar_test(bar(B_KFULL + g % NK), (uint32_t)((g / NK) & 1)));
+          if (ready) {
+            tc_fence_after();
+            const uint32_t kb = sbase + kOffK + (uint32_t)(g % NK) * kKVStage;
+            const uint32_t d = tmem + 256u * (uint32_t)e + (uint32_t)(g & 1) * 64u;
+            const uint32_t qa = sbase + kOffQ + (uint32_t)(t & 1) * kQStage + (uint32_t)e * kQHead;
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk)   // 4 k-steps of 16 per 64-column block
+              umma_ss_k4(d, kmajor(qa, kQBox, 4 * blk), kmajor(kb, kKBox, 4 * blk), kIdescQK<F16>,
+                         blk > 0 ? 1u : 0u);
+            umma_commit_elect(bar(B_SFULL + 2 * e + (g & 1)));
+            if (qk[1 - e].g > g) umma_commit_elect(bar(B_KEMPTY + g % NK));   // both QKs of g out
+            q.advance(a);
+            progress = true;
+          }
+        }
+        StepCursor& p = pv[e];
+        if (!p.done() && p.g < q.g) {
+          const int g = p.g, s = g & 1;
+          const bool ready = __all_sync(
+              0xffffffffu, mbar_test(bar(B_VFULL + g % NV), (uint32_t)((g / NV) & 1)) &&
+                               mbar_test(bar(B_PFULL + 2 * e + s), (uint32_t)((g >> 1) & 1)) &&
+                               (p.j != 0 || p.t == 0 ||
+                                mbar_test(bar(B_OFREE + e), (uint32_t)((p.t - 1) & 1))));
+          if (ready) {
+            tc_fence_after();
+            const uint32_t vb = sbase + kOffV + (uint32_t)(g % NV) * kKVStage;
+            const uint32_t p_tm = tmem + 256u * (uint32_t)e + (uint32_t)s * 64u;   // P: 32 columns
+            umma_ts_k4<2048 / 16>(tmem + 256u * (uint32_t)e + 128u, p_tm, vmn(vb, 0),
+                                  kIdescPV<F16>, p.j > 0 ? 1u : 0u);
+            umma_commit_elect(bar(B_ODONE + 2 * e + s));
+            if (pv[1 - e].g > g) umma_commit_elect(bar(B_VEMPTY + g % NV));   // both P Vs of g out
+            p.advance(a);
+            progress = true;
+          }
+        }
       }
-      if (!ok) break;
-      umma_commit_elect(bar(B_VEMPTY + g % NV));
-      pv.advance(a);
+      if (progress) {
+        idle = false;
+        continue;
+      }
+      __nanosleep(20);   // nothing ready: leave the issue slots to the softmax warps
+      if (!idle) {
+        idle = true;
+        t_idle = global_timer_ns();
+      } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
+        if (lane == 0) atomicOr(a.status, STATUS_WAIT_TIMEOUT);
+        ok = false;
+      }
     }
     umma_commit_elect(bar(B_MMADONE));
     warp_wait(bar(B_MMADONE), 0, a.status);   // nothing of ours still runs on the tensor core
