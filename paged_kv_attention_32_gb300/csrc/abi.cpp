@@ -624,8 +624,6 @@ int batch_prefill_run(const pka_prefill_plan* p, const void* q, int64_t q_stride
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.output_scale = p->desc.output_scale;
   a.out_dtype = p->desc.out_dtype;
-  if (p->head_pairs)
-    return launch_prefill_gh(*p, a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream));
   return launch_prefill_1h(*p, a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream));
 }
 

@@ -55,7 +55,6 @@ struct pka_prefill_plan {
   pka_prefill_desc desc;
   int32_t B = 0, Hq = 0, Hkv = 0, G = 0, D = 0;
   int32_t total_q = 0, total_kv = 0;
-  bool head_pairs = false;   // tiles hold heads (h, h + 1) of one KV head (head-pair kernel)
   float scale = 0.f;
   std::vector<int32_t> qo, kv;
   std::vector<int32_t> win_lo, win_hi;   // variable_window bounds per query row (host)
@@ -80,12 +79,6 @@ namespace pka {
 int build_prefill_plan(pka_prefill_plan& plan, const pka_prefill_desc& desc, const int32_t* qo,
                        const int32_t* kv, const int32_t* win_lo = nullptr,
                        const int32_t* win_hi = nullptr);
-
-// Launches the persistent head-pair prefill kernel (head_dim 128, even GQA
-// group: each tile two query heads of one KV head) over the plan's tiles.
-int launch_prefill_gh(const pka_prefill_plan& plan, const PrefillArgs& args,
-                      const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                      cudaStream_t stream);
 
 // Launches the prefill kernel (one query head and 128 rows per CTA, 64-key
 // tiles; head_dim 128 or 256) over the plan's tiles.

@@ -7,9 +7,7 @@
 #include <algorithm>
 #include <climits>
 #include <cmath>
-#include <cstdlib>
 #include <numeric>
-#include <string>
 
 #include "host_common.h"
 #include "prefill.h"
@@ -72,13 +70,6 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
   }
   p.tiles.clear();
   p.row_map.clear();
-  // head_dim 128 with an even group: one tile for each pair of query heads of
-  // a KV head (they read the same keys and values)
-  {
-    const char* env = std::getenv("PKA_PREFILL_HEAD_PAIRS");
-    p.head_pairs = d.head_dim == 128 && p.G % 2 == 0 && !varwin &&
-                   !(env != nullptr && std::string(env) == "0");
-  }
   if (varwin) {
     // Tiles of rows with similar windows compute fewer invisible scores: each
     // request's rows are ordered by their last key, cut into bands of a few
@@ -162,7 +153,7 @@ int build_prefill_plan(pka_prefill_plan& p, const pka_prefill_desc& d_in, const 
       const int32_t kv0 = (int32_t)(lo / kTileK);
       const int32_t n_kv = (int32_t)(ceil_div(hi, kTileK) - kv0);
       PKA_CHECK_ARG(n_kv >= 1, "request %d: a query tile with no key tile", b);
-      for (int32_t h = 0; h < p.Hq; h += p.head_pairs ? 2 : 1)
+      for (int32_t h = 0; h < p.Hq; ++h)
         p.tiles.push_back(PrefillTile{h, (int32_t)m, n_kv, kv0, qo[b], (int32_t)lq, kv[b],
                                       (int32_t)lk});
     }
