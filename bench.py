@@ -51,8 +51,8 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--workload", default=None,
-                    help="profiling: time only this decode workload (llama3_8b, skewed, spec) "
-                         "or 'prefill'")
+                    help="profiling: time only this decode workload (llama3_8b, skewed, spec), "
+                         "'prefill' or 'prefill_variable_window'")
     ap.add_argument("--batch", type=int, default=None,
                     help="profiling: override the workload's batch size (smaller capture)")
     ap.add_argument("--mma-min-rows", type=int, default=0,
@@ -81,6 +81,8 @@ def profile_case(args):
             wl.RAGGED_PREFILL = wl.shrink(w, batch=args.batch)
         r = measure_prefill(args.seed, args.steps, args.warmup, peak_tf, head_dim=args.head_dim)
         wl.RAGGED_PREFILL = w
+    elif args.workload == "prefill_variable_window":
+        r = measure_prefill_fixed(args.seed, args.steps, args.warmup, peak_tf, variable_window=True)
     else:
         w = wl.DECODE_WORKLOADS[args.workload]
         if args.batch:
@@ -745,7 +747,7 @@ def compact(r):
     if "TFLOP_per_s" in r:
         out.update(TFLOPs=round(r["TFLOP_per_s"]), frac=round(r.get("frac_of_measured_bf16"), 3))
     if "clocks" in r:
-        out["clk_ok"] = clocks_ok(r["clocks"])
+        out["clk"] = clocks_ok(r["clocks"])
     if r.get("cpu_baseline"):
         out["oracle"] = r["cpu_baseline"]["value"]
     return out
