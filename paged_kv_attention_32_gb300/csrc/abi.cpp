@@ -58,11 +58,11 @@ size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 int upload_decode_plan(pka_plan& p, cudaStream_t stream) {
   const size_t n_items = p.items.size() * sizeof(WorkItem);
   const size_t n_reqs = p.reqs.size() * sizeof(ReqInfo);
-  const size_t n_merge = p.merge_rows.size() * sizeof(MergeRow);
+  const size_t n_cnt = (size_t)p.num_merge_counters * sizeof(int32_t);
   const size_t off_reqs = up256(n_items);
-  const size_t off_merge = off_reqs + up256(n_reqs);
-  const size_t off_status = off_merge + up256(n_merge);
-  const size_t total = off_status + 256;
+  const size_t off_status = off_reqs + up256(n_reqs);
+  const size_t off_cnt = off_status + 256;   // merge counters, zero between runs
+  const size_t total = off_cnt + up256(n_cnt);
   if (p.dev_buf == nullptr || total > p.dev_capacity) {
     // a replan that outgrows the buffer reallocates it with headroom
     if (p.dev_buf != nullptr) {
@@ -78,8 +78,8 @@ int upload_decode_plan(pka_plan& p, cudaStream_t stream) {
   uint8_t* base = static_cast<uint8_t*>(p.dev_buf);
   p.d_items = reinterpret_cast<const WorkItem*>(base);
   p.d_reqs = reinterpret_cast<const ReqInfo*>(base + off_reqs);
-  p.d_merge_rows = reinterpret_cast<const MergeRow*>(base + off_merge);
   p.d_status = reinterpret_cast<int32_t*>(base + off_status);
+  p.d_merge_cnt = reinterpret_cast<int32_t*>(base + off_cnt);
   // One asynchronous copy from a pinned image of the buffer.  The image is
   // rewritten only after the copy that last read it has completed (stage_done);
   // stream order keeps the upload behind runs already queued on the same stream.
@@ -102,8 +102,7 @@ int upload_decode_plan(pka_plan& p, cudaStream_t stream) {
     uint8_t* img = static_cast<uint8_t*>(p.host_stage);
     if (n_items) std::memcpy(img, p.items.data(), n_items);
     std::memcpy(img + off_reqs, p.reqs.data(), n_reqs);
-    if (n_merge) std::memcpy(img + off_merge, p.merge_rows.data(), n_merge);
-    std::memset(img + off_status, 0, 256);
+    std::memset(img + off_status, 0, total - off_status);   // status word and counters
     PKA_CUDA_TRY(cudaMemcpyAsync(base, img, total, cudaMemcpyHostToDevice, stream),
                  "cudaMemcpyAsync(plan)");
     if (p.stage_done == nullptr)
@@ -120,11 +119,8 @@ int upload_decode_plan(pka_plan& p, cudaStream_t stream) {
   PKA_CUDA_TRY(cudaMemcpyAsync(base + off_reqs, p.reqs.data(), n_reqs, cudaMemcpyHostToDevice,
                                stream),
                "cudaMemcpyAsync(plan requests)");
-  if (n_merge)
-    PKA_CUDA_TRY(cudaMemcpyAsync(base + off_merge, p.merge_rows.data(), n_merge,
-                                 cudaMemcpyHostToDevice, stream),
-                 "cudaMemcpyAsync(plan merge rows)");
-  PKA_CUDA_TRY(cudaMemsetAsync(base + off_status, 0, 256, stream), "cudaMemsetAsync(status)");
+  PKA_CUDA_TRY(cudaMemsetAsync(base + off_status, 0, total - off_status, stream),
+               "cudaMemsetAsync(status and counters)");
   return PKA_OK;
 }
 
@@ -376,10 +372,10 @@ int paged_decode_run(const pka_plan* p, const void* q, int64_t q_stride_tok,
                        : nullptr;
   a.items = p->d_items;
   a.reqs = p->d_reqs;
-  a.merge_rows = p->d_merge_rows;
+  a.merge_cnt = p->d_merge_cnt;
   a.status = p->d_status;
   a.num_items = (int32_t)p->items.size();
-  a.num_merge_rows = (int32_t)p->merge_rows.size();
+  a.tiles_per_item = p->kernel == PKA_KERNEL_MMA ? (p->rows_per_cta + 15) / 16 : 1;
   a.num_qo_heads = p->Hq;
   a.num_kv_heads = p->Hkv;
   a.group = p->G;

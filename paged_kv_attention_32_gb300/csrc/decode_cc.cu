@@ -24,10 +24,11 @@
 //    probabilities go through a 16 x R shared buffer;
 //  * the four warps' (m, l, acc) are merged through shared memory; the CTA
 //    then writes the final O (bf16, f16 or fp32) and LSE (sink added here), or an fp32
-//    partial (O/l, m + log2 l) for the merge kernel when the request was
-//    split.
+//    partial (O/l, m + log2 l) when the request was split; the chunk CTA of
+//    a (request, KV head) that finishes last merges the partials.
 #include <cuda_bf16.h>
 
+#include "decode_merge.cuh"
 #include "device_common.cuh"
 #include "host_common.h"
 #include "kernels.h"
@@ -67,7 +68,6 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
   constexpr int NCH = DL / 8;     // 16-byte chunks per lane
   constexpr int NSTEP = kUnit / KS;
   constexpr unsigned FULL = 0xffffffffu;
-  pdl_launch_dependents();   // the split merge may be scheduled now; it waits for us
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -370,62 +370,8 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
       if (d == 0) a.ws_lse[prow] = lsum > 0.f ? m + log2f(lsum) : neg_inf();
     }
   }
-}
-
-// Merge of the split requests' partials: one warp per (token row, q head).  The
-// launcher sends requests of up to 8 chunks here, so the warp issues every
-// chunk's LSE (one per lane) and O row (8 loads per lane) at once and combines
-// them after one round of memory latency; longer chunk lists take further
-// rounds of 8.  A chunk without keys has O = 0 and LSE -inf (weight 0).
-__global__ void __launch_bounds__(128)
-decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
-  pdl_wait_primary();   // the decode grid's partials are complete and visible
-  constexpr unsigned FULL = 0xffffffffu;
-  constexpr int kGroup = 8;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t idx = (int64_t)blockIdx.x * 4 + warp;
-  if (idx >= (int64_t)a.num_merge_rows * a.num_qo_heads) return;
-  const int mr = (int)(idx / a.num_qo_heads), h = (int)(idx % a.num_qo_heads);
-  const MergeRow row = a.merge_rows[mr];
-  const ReqInfo rq = a.reqs[row.request];
-  const int nc = rq.n_chunks;
-  const int64_t stride_c = (int64_t)rq.q_len * a.num_qo_heads;
-  const int64_t p0 = rq.part_base + (int64_t)row.row * a.num_qo_heads + h;
-  float m = neg_inf();
-  for (int c = lane; c < nc; c += 32) m = fmaxf(m, a.ws_lse[p0 + c * stride_c]);
-#pragma unroll
-  for (int delta = 16; delta > 0; delta >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, delta));
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  for (int c0 = 0; c0 < nc && m != neg_inf(); c0 += kGroup) {
-    // lane k < kGroup holds the weight of chunk c0 + k; every lane its 4 dims of each O row
-    const int cl = c0 + lane;
-    const float lc = lane < kGroup && cl < nc ? a.ws_lse[p0 + cl * stride_c] : neg_inf();
-    float4 v[kGroup];
-#pragma unroll
-    for (int k = 0; k < kGroup; ++k)
-      v[k] = c0 + k < nc ? *reinterpret_cast<const float4*>(
-                               a.ws_o + (p0 + (int64_t)(c0 + k) * stride_c) * 128 + lane * 4)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float wl = lc == neg_inf() ? 0.f : ex2(lc - m);
-#pragma unroll
-    for (int k = 0; k < kGroup; ++k) {
-      const float w = __shfl_sync(FULL, wl, k);
-      wsum += w;
-      o.x += w * v[k].x;
-      o.y += w * v[k].y;
-      o.z += w * v[k].z;
-      o.w += w * v[k].w;
-    }
-  }
-  float denom = wsum;
-  if (a.sinks != nullptr && m != neg_inf()) denom += ex2(__ldg(a.sinks + h) * kLog2e - m);
-  const float sc = denom > 0.f ? a.bmm2_scale / denom : 0.f;
-  const int64_t t = rq.q_start + row.row;
-  const float ov[4] = {o.x, o.y, o.z, o.w};
-  store_out<4>(a.out, (t * a.num_qo_heads + h) * 128 + lane * 4, ov, sc, a.out_dtype);
-  if (a.lse != nullptr && lane == 0)
-    a.lse[t * a.num_qo_heads + h] = wsum > 0.f ? m + log2f(wsum) : neg_inf();
+  if (rq.part_base >= 0)   // a split request: the group's last chunk merges its rows
+    split_merge_if_last(a, rq, hk, 0, 0, min(rows_b, R));
 }
 
 template <int R, int NSTAGE, bool F16>
@@ -443,85 +389,6 @@ int launch_cc(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMap
   if (e != cudaSuccess) return cuda_fail(e, "decode_cc_kernel launch");
   return PKA_OK;
 }
-
-// Chunk count above which the wide merge runs.
-constexpr int32_t kWideMergeChunks = 8;
-
-// The same merge for requests cut into many chunks: one CTA per (token row, q
-// head).  Each warp takes every fourth chunk and issues the loads of eight of
-// its chunks (LSE and O row) before using any, so a long request's chunks are
-// read in a few rounds of memory latency; the four warps' sums meet in shared
-// memory.  A chunk without keys has O = 0 and LSE -inf (weight 0).
-__global__ void __launch_bounds__(128)
-decode_merge_wide_kernel(const __grid_constant__ DecodeArgs a) {
-  pdl_wait_primary();   // the decode grid's partials are complete and visible
-  constexpr unsigned FULL = 0xffffffffu;
-  constexpr int kGroup = 8;
-  __shared__ float4 part_o[4][32];
-  __shared__ float part_w[4];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t idx = blockIdx.x;
-  if (idx >= (int64_t)a.num_merge_rows * a.num_qo_heads) return;   // the whole CTA
-  const int mr = (int)(idx / a.num_qo_heads), h = (int)(idx % a.num_qo_heads);
-  const MergeRow row = a.merge_rows[mr];
-  const ReqInfo rq = a.reqs[row.request];
-  const int nc = rq.n_chunks;
-  const int64_t stride_c = (int64_t)rq.q_len * a.num_qo_heads;
-  const int64_t p0 = rq.part_base + (int64_t)row.row * a.num_qo_heads + h;
-  float m = neg_inf();
-  for (int c = lane; c < nc; c += 32) m = fmaxf(m, a.ws_lse[p0 + c * stride_c]);
-#pragma unroll
-  for (int delta = 16; delta > 0; delta >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, delta));
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  float ws = 0.f;
-  if (m != neg_inf()) {
-    for (int c0 = warp; c0 < nc; c0 += 4 * kGroup) {
-      float lc[kGroup];
-      float4 v[kGroup];
-#pragma unroll
-      for (int k = 0; k < kGroup; ++k) {
-        const int c = c0 + 4 * k;
-        const int64_t p = p0 + (int64_t)c * stride_c;
-        lc[k] = c < nc ? a.ws_lse[p] : neg_inf();
-        v[k] = c < nc ? *reinterpret_cast<const float4*>(a.ws_o + p * 128 + lane * 4)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int k = 0; k < kGroup; ++k) {
-        const float w = lc[k] == neg_inf() ? 0.f : ex2(lc[k] - m);
-        ws += w;
-        o.x += w * v[k].x;
-        o.y += w * v[k].y;
-        o.z += w * v[k].z;
-        o.w += w * v[k].w;
-      }
-    }
-  }
-  if (warp > 0) {
-    part_o[warp][lane] = o;
-    if (lane == 0) part_w[warp] = ws;
-  }
-  __syncthreads();
-  if (warp != 0) return;
-#pragma unroll
-  for (int w = 1; w < 4; ++w) {
-    const float4 x = part_o[w][lane];
-    o.x += x.x;
-    o.y += x.y;
-    o.z += x.z;
-    o.w += x.w;
-    ws += part_w[w];
-  }
-  float denom = ws;
-  if (a.sinks != nullptr && m != neg_inf()) denom += ex2(__ldg(a.sinks + h) * kLog2e - m);
-  const float sc = denom > 0.f ? a.bmm2_scale / denom : 0.f;
-  const int64_t t = rq.q_start + row.row;
-  const float ov[4] = {o.x, o.y, o.z, o.w};
-  store_out<4>(a.out, (t * a.num_qo_heads + h) * 128 + lane * 4, ov, sc, a.out_dtype);
-  if (a.lse != nullptr && lane == 0)
-    a.lse[t * a.num_qo_heads + h] = ws > 0.f ? m + log2f(ws) : neg_inf();
-}
-
 
 }  // namespace
 
@@ -541,34 +408,6 @@ int launch_decode(const pka_plan& plan, const DecodeArgs& args, const CUtensorMa
                      : launch_cc<8, 3, false>(args, kmap, vmap, stream);
   }
   if (rc != PKA_OK) return rc;
-  if (args.num_merge_rows > 0) {
-    // a warp per (row, head) walks the chunks one after another; a CTA per (row,
-    // head) reads them in parallel, which pays when a request was cut into many
-    // chunks (a long context spread over the GPU) or when there are too few
-    // (row, head) pairs to fill the GPU with warps.  Measured on GB300: 23 chunks
-    // of one request 11.7 -> 5.2 us; 224 pairs of <= 5 chunks 1 % faster; 1500
-    // pairs of 4 chunks 2.6 % slower with the CTA per pair.
-    int32_t max_chunks = 0;
-    for (const ReqInfo& r : plan.reqs) max_chunks = r.n_chunks > max_chunks ? r.n_chunks : max_chunks;
-    const int64_t pairs = (int64_t)args.num_merge_rows * args.num_qo_heads;
-    const bool wide = max_chunks > kWideMergeChunks || pairs <= 4 * (int64_t)plan.desc.num_sms;
-    // launched as a programmatic dependent of the decode grid: its CTAs are placed
-    // while the decode's last CTAs run, and wait in-kernel for the partials
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3((unsigned)(wide ? pairs : (pairs + 3) / 4));
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = wide ? cudaLaunchKernelEx(&cfg, decode_merge_wide_kernel, args)
-                         : cudaLaunchKernelEx(&cfg, decode_merge_kernel, args);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "decode_merge_kernel launch");
-  }
   return PKA_OK;
 }
 

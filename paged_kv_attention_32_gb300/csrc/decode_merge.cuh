@@ -1,0 +1,75 @@
+// The LSE merge of split decode requests, done inside the decode kernels: the
+// chunk CTAs of one (request, KV head, tile) group each write their fp32
+// partial rows (O / l and the base-2 LSE m + log2 l) and count themselves on
+// a counter of the group; the CTA that counts last merges the group's rows.
+// (The partial states of one row are combined as the LSE convention of
+// cudnn_batch_decode_with_kv_cache describes: weights 2^(lse_i - m) with m
+// the largest LSE, the sink added once to the denominator.)  This saves a
+// second kernel launch that would have to wait for the whole decode grid.
+#pragma once
+
+#include "device_common.cuh"
+
+namespace pka {
+namespace dev {
+
+// Called by every thread of a CTA of a split request after the CTA wrote its
+// partial rows r0 .. r0 + nrows - 1 of the work item (row r = i * group + g:
+// token i, head hk * group + g).  Returns at once unless this CTA is the
+// group's last; that CTA resets the group's counter to zero (every chunk has
+// counted) and writes the final O (out_dtype, bmm2_scale) and LSE of the rows.
+__device__ __forceinline__ void split_merge_if_last(const DecodeArgs& a, const ReqInfo& rq, int hk,
+                                                    int tile, int r0, int nrows) {
+  __shared__ int s_last;
+  __threadfence();   // this thread's partial writes, before the CTA counts itself
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t* cnt = a.merge_cnt + rq.cnt_base + hk * a.tiles_per_item + tile;
+    const bool last = atomicAdd(cnt, 1) == rq.n_chunks - 1;
+    if (last) *cnt = 0;   // every chunk has counted: ready for the next run
+    s_last = last;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();   // the other chunks' partials, counted before us, are visible
+  const int rr = threadIdx.x >> 3, d0 = (threadIdx.x & 7) * 16;   // 16 rows x 8 x 16 dims
+  if (rr >= nrows) return;
+  const int G = a.group, r = r0 + rr;
+  const int i = r / G, h = hk * G + r % G;
+  const int nc = rq.n_chunks;
+  const int64_t stride_c = (int64_t)rq.q_len * a.num_qo_heads;
+  const int64_t p0 = rq.part_base + (int64_t)i * a.num_qo_heads + h;
+  float m = neg_inf();
+  for (int c = 0; c < nc; ++c) m = fmaxf(m, __ldcg(a.ws_lse + p0 + c * stride_c));
+  float o[16];
+#pragma unroll
+  for (int x = 0; x < 16; ++x) o[x] = 0.f;
+  float wsum = 0.f;
+  if (m != neg_inf()) {
+    for (int c = 0; c < nc; ++c) {   // a chunk without keys has LSE -inf: weight 0
+      const int64_t p = p0 + c * stride_c;
+      const float lc = __ldcg(a.ws_lse + p);
+      const float w = lc == neg_inf() ? 0.f : ex2(lc - m);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(a.ws_o + p * 128 + d0);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float4 v = __ldcg(src + x);
+        o[4 * x] += w * v.x;
+        o[4 * x + 1] += w * v.y;
+        o[4 * x + 2] += w * v.z;
+        o[4 * x + 3] += w * v.w;
+      }
+    }
+  }
+  float denom = wsum;
+  if (a.sinks != nullptr && m != neg_inf()) denom += ex2(__ldg(a.sinks + h) * kLog2e - m);
+  const float sc = denom > 0.f ? a.bmm2_scale / denom : 0.f;
+  const int64_t t = rq.q_start + i;
+  store_out<16>(a.out, (t * a.num_qo_heads + h) * 128 + d0, o, sc, a.out_dtype);
+  if (a.lse != nullptr && d0 == 0)
+    a.lse[t * a.num_qo_heads + h] = wsum > 0.f ? m + log2f(wsum) : neg_inf();
+}
+
+}  // namespace dev
+}  // namespace pka

@@ -18,11 +18,13 @@
 //    mask, online softmax in base 2 on the fragments, P re-packed to 16-bit
 //    A fragments in registers, O += P V (16 n-tiles, V via ldmatrix.trans);
 //  * the four warps' (m, l, O) are merged through shared memory and the CTA
-//    writes final O/LSE (sink added) or an fp32 partial for the merge kernel.
+//    writes final O/LSE (sink added), or, for a split request, an fp32 partial;
+//    the last chunk CTA of each (request, KV head, tile) merges the partials.
 // Decode is bound by HBM, not by the tensor pipe: mma takes the per-key
 // arithmetic of wide groups off the FP32 pipe.
 #include <cuda_bf16.h>
 
+#include "decode_merge.cuh"
 #include "decode_mma_tile.cuh"
 #include "device_common.cuh"
 #include "host_common.h"
@@ -50,7 +52,6 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * NSTAGE * kStageBytes);
 
-  pdl_launch_dependents();   // the split merge may be scheduled now; it waits for us
   const int mt_count = (a.rows_per_cta + 15) >> 4;
   const int item_idx = blockIdx.x / mt_count, mt = blockIdx.x % mt_count;
   const WorkItem it = a.items[item_idx];
@@ -140,6 +141,8 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   // thread -> (row of the tile, 16 consecutive dims)
   mma_combine_store(a, rq, comb_o, comb_m, comb_l, 0, kWarps, mt, tid >> 3, (tid & 7) * 16, hk,
                     chunk);
+  if (rq.part_base >= 0)   // a split request: the group's last chunk merges its rows
+    split_merge_if_last(a, rq, hk, mt, mt * 16, min(16, rows_b - mt * 16));
 }
 
 template <int NSTAGE, bool F16>

@@ -19,7 +19,7 @@ namespace {
 
 // Fixed scratch: 16 MiB on every GPU that loads the library, held until the
 // process exits.  Layout per call: status word | work items | request info |
-// merge rows | partial outputs | partial LSEs, each 256-byte aligned.
+// merge counters | partial outputs | partial LSEs, each 256-byte aligned.
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -95,11 +95,11 @@ extern "C" int paged_decode_run_noalloc(const pka_plan* p, const void* q, int64_
   // scratch layout for this plan
   const size_t n_items = p->items.size() * sizeof(WorkItem);
   const size_t n_reqs = p->reqs.size() * sizeof(ReqInfo);
-  const size_t n_merge = p->merge_rows.size() * sizeof(MergeRow);
+  const size_t n_cnt = (size_t)p->num_merge_counters * sizeof(int32_t);
   const size_t off_items = kStatusBytes;
   const size_t off_reqs = off_items + up256(n_items);
-  const size_t off_merge = off_reqs + up256(n_reqs);
-  const size_t off_ws = off_merge + up256(n_merge);
+  const size_t off_cnt = off_reqs + up256(n_reqs);
+  const size_t off_ws = off_cnt + up256(n_cnt);
   const size_t off_lse = off_ws + (size_t)p->ws_lse_offset;
   const size_t total = off_ws + (size_t)p->workspace_bytes;
   if (total > kNoAllocScratchBytes)
@@ -119,19 +119,22 @@ extern "C" int paged_decode_run_noalloc(const pka_plan* p, const void* q, int64_
   unsigned char* base = nullptr;
   int rc = scratch_address(dev, s, &base);
   if (rc != PKA_OK) return rc;
-  // Nothing else must start at zero: every partial row is written by its
-  // chunk before the merge kernel reads it, and the status word is cleared
-  // only by paged_decode_plan_check (it collects every run since).
+  // Of the rest only the merge counters must start at zero (below): every
+  // partial row is written by its chunk before the group's last chunk CTA
+  // reads it, and the status word is cleared only by paged_decode_plan_check
+  // (it collects every run since).
   if (n_items)
     PKA_CUDA_TRY(cudaMemcpyAsync(base + off_items, p->items.data(), n_items,
                                  cudaMemcpyHostToDevice, s),
                  "cudaMemcpyAsync(no-alloc items)");
   PKA_CUDA_TRY(cudaMemcpyAsync(base + off_reqs, p->reqs.data(), n_reqs, cudaMemcpyHostToDevice, s),
                "cudaMemcpyAsync(no-alloc requests)");
-  if (n_merge)
-    PKA_CUDA_TRY(cudaMemcpyAsync(base + off_merge, p->merge_rows.data(), n_merge,
-                                 cudaMemcpyHostToDevice, s),
-                 "cudaMemcpyAsync(no-alloc merge rows)");
+  // the last chunk CTA of each split group merges it; the counters that tell it
+  // so start at zero (the kernels leave them at zero, but an earlier call of
+  // another plan may have used this space otherwise)
+  if (n_cnt)
+    PKA_CUDA_TRY(cudaMemsetAsync(base + off_cnt, 0, n_cnt, s),
+                 "cudaMemsetAsync(no-alloc merge counters)");
 
   CUtensorMap kmap, vmap;
   rc = encode_kv_pool_map(&kmap, k_pages, p->desc.num_pages, p->Hkv, p->ps, p->D, kv_stride_page,
@@ -155,10 +158,10 @@ extern "C" int paged_decode_run_noalloc(const pka_plan* p, const void* q, int64_
   a.ws_lse = reinterpret_cast<float*>(base + off_lse);
   a.items = reinterpret_cast<const WorkItem*>(base + off_items);
   a.reqs = reinterpret_cast<const ReqInfo*>(base + off_reqs);
-  a.merge_rows = reinterpret_cast<const MergeRow*>(base + off_merge);
+  a.merge_cnt = reinterpret_cast<int32_t*>(base + off_cnt);
   a.status = reinterpret_cast<int32_t*>(base);
   a.num_items = (int32_t)p->items.size();
-  a.num_merge_rows = (int32_t)p->merge_rows.size();
+  a.tiles_per_item = p->kernel == PKA_KERNEL_MMA ? (p->rows_per_cta + 15) / 16 : 1;
   a.num_qo_heads = p->Hq;
   a.num_kv_heads = p->Hkv;
   a.group = p->G;

@@ -85,16 +85,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
 }
 
 // ---- TMA -------------------------------------------------------------------
-// Programmatic dependent launch: a kernel lets the grid launched after it on the
-// stream (with the programmatic-serialization attribute) be scheduled once all of
-// its CTAs have started; that grid waits for this one's completion and memory.
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait_primary() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -19,7 +19,8 @@ struct ReqInfo {
   int32_t kv_len;     // key count seen by the planner (upper bound when not frozen)
   int32_t part_base;  // first fp32 partial row, -1 when the request is not split
   int32_t n_chunks;   // chunks the request's key range was cut into
-  int32_t pad0, pad1, pad2;
+  int32_t cnt_base;   // split requests: first of its merge counters (one per KV head and tile)
+  int32_t pad1, pad2;
 };
 
 // One decode work item = one CTA: (request, kv head, chunk, pages [lo, hi)).
@@ -29,12 +30,6 @@ struct WorkItem {
   int32_t head_chunk;
   int32_t page_lo;
   int32_t page_hi;
-};
-
-// Token rows of split requests that the merge kernel combines: {request, row}.
-struct MergeRow {
-  int32_t request;
-  int32_t row;
 };
 
 // Everything a decode kernel launch needs besides the two tensor maps.
@@ -52,10 +47,10 @@ struct DecodeArgs {
   float* ws_lse;                 // fp32 partial base-2 LSE [partial_rows]
   const WorkItem* items;
   const ReqInfo* reqs;
-  const MergeRow* merge_rows;
+  int32_t* merge_cnt;            // split requests: chunk CTAs done per (request, KV head, tile)
   int32_t* status;               // device error word (0 = fine)
   int32_t num_items;
-  int32_t num_merge_rows;
+  int32_t tiles_per_item;        // CTAs per work item (16-row tiles of the mma kernel, else 1)
   int32_t num_qo_heads;
   int32_t num_kv_heads;
   int32_t group;                 // Hq / Hkv
@@ -89,14 +84,14 @@ struct pka_plan {
   std::vector<pka::ReqInfo> reqs;
   std::vector<int32_t> page_lo, page_hi, order;
   std::vector<pka::WorkItem> items;
-  std::vector<pka::MergeRow> merge_rows;
-  // one device allocation holding items | reqs | merge rows | status word
+  int32_t num_merge_counters = 0;   // split requests: Hkv x tiles per item each
+  // one device allocation holding items | reqs | status word | merge counters
   void* dev_buf = nullptr;
   size_t dev_capacity = 0;    // bytes of dev_buf (reused by paged_decode_plan_update)
   const pka::WorkItem* d_items = nullptr;
   const pka::ReqInfo* d_reqs = nullptr;
-  const pka::MergeRow* d_merge_rows = nullptr;
   int32_t* d_status = nullptr;
+  int32_t* d_merge_cnt = nullptr;
   int device = -1;
   // pinned host image of dev_buf: a replan writes it and uploads it with one
   // asynchronous copy; stage_done marks when that copy has read it

@@ -234,10 +234,13 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
     }
   }
 
-  // ---- split requests: partial rows, merge rows, workspace ----
+  // ---- split requests: partial rows, merge counters, workspace ----
+  // The last chunk CTA of each (request, KV head, tile) merges that group's
+  // partials; a counter per group tells it that it is the last.
+  const int32_t tiles_per_item =
+      p.kernel == PKA_KERNEL_MMA ? (int32_t)ceil_div(p.rows_per_cta, 16) : 1;
   p.reqs.assign(B, ReqInfo{});
-  p.merge_rows.clear();
-  int64_t prow = 0;
+  int64_t prow = 0, counters = 0;
   int32_t n_split = 0;
   for (int32_t b = 0; b < B; ++b) {
     ReqInfo& r = p.reqs[b];
@@ -245,16 +248,20 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
     r.q_len = qlen[b];
     r.kv_len = seq[b];
     r.n_chunks = nch[b];
+    r.cnt_base = -1;
     if (nch[b] > 1) {
       r.part_base = (int32_t)prow;
       prow += (int64_t)nch[b] * qlen[b] * Hq;
+      r.cnt_base = (int32_t)counters;
+      counters += (int64_t)Hkv * tiles_per_item;
       ++n_split;
-      for (int32_t i = 0; i < qlen[b]; ++i) p.merge_rows.push_back(MergeRow{b, i});
     } else {
       r.part_base = -1;
     }
-    PKA_CHECK_ARG(prow <= (int64_t)INT32_MAX, "too many partial rows");
+    PKA_CHECK_ARG(prow <= (int64_t)INT32_MAX && counters <= (int64_t)INT32_MAX,
+                  "too many partial rows");
   }
+  p.num_merge_counters = (int32_t)counters;
   p.num_split = n_split;
   p.partial_rows = (int32_t)prow;
   const int64_t o_bytes = ceil_div(prow * p.D * 4, 256) * 256;

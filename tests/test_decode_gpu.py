@@ -45,25 +45,23 @@ def test_decode_split_kv_path(name):
     assert_close(out, lse, ref_o, ref_l)
 
 
-@pytest.mark.parametrize("name,sms,wide", [("spec", 148, False), ("skewed", 148, True),
-                                           ("skewed", 48, True)])
-def test_decode_merge_kernels(name, sms, wide):
-    """Split partials are merged by a warp per (row, head), or by a CTA per (row, head)
-    when a request has more than 8 chunks or the (row, head) pairs are at most
-    4 x SMs; each choice against the oracle (spec: 1280 pairs of <= 3 chunks; skewed:
-    19 chunks, or 6 chunks over 192 pairs)."""
+@pytest.mark.parametrize("name,sms", [("spec", 148), ("skewed", 148), ("skewed", 48),
+                                      ("llama3_8b", 64)])
+def test_decode_split_merge_by_the_last_chunk(name, sms):
+    """Split partials are merged inside the decode kernels: the chunk CTA of a (request,
+    KV head, tile) group that counts last combines the group's rows (spec: <= 3 chunks
+    over packed causal rows, three tiles; skewed: 19 or 6 chunks; llama3_8b: the
+    CUDA-core kernel).  Run twice, so that the counters left by the first run (reset to
+    zero by each group's last CTA) serve the second."""
     inp = wl.make_decode_inputs(SMALL[name], seed=5, device=DEV)
-    out, lse, plan = run_decode(inp, num_sms=sms, split_waves=2, min_chunk_tokens=128)
+    from helpers import decode_plan_for
+    plan = decode_plan_for(inp, num_sms=sms, split_waves=2, min_chunk_tokens=128)
     ex = plan.export()
-    if inp["qo_indptr"] is not None:
-        qlen = (inp["qo_indptr"][1:] - inp["qo_indptr"][:-1]).tolist()
-    else:
-        qlen = [inp["q_len"]] * len(ex["n_chunks"])
-    pairs = sum(L for L, c in zip(qlen, ex["n_chunks"]) if c > 1) * inp["q"].shape[1]
-    assert pairs > 0
-    assert (max(ex["n_chunks"]) > 8 or pairs <= 4 * sms) == wide
+    assert max(ex["n_chunks"]) > 1
     ref_o, ref_l = oracle_decode(inp)
-    assert_close(out, lse, ref_o, ref_l)
+    for _ in range(2):
+        out, lse, _ = run_decode(inp, plan=plan)
+        assert_close(out, lse, ref_o, ref_l)
 
 
 @pytest.mark.parametrize("name", ["tiny", "llama3_8b", "skewed"])
