@@ -39,26 +39,44 @@ __device__ __forceinline__ void split_merge_if_last(const DecodeArgs& a, const R
   const int nc = rq.n_chunks;
   const int64_t stride_c = (int64_t)rq.q_len * a.num_qo_heads;
   const int64_t p0 = rq.part_base + (int64_t)i * a.num_qo_heads + h;
+  // loads go out kRound chunks at a time, so that a long chunk list costs a few
+  // rounds of memory latency rather than one per chunk
+  constexpr int kRound = 4;
   float m = neg_inf();
-  for (int c = 0; c < nc; ++c) m = fmaxf(m, __ldcg(a.ws_lse + p0 + c * stride_c));
+  for (int c0 = 0; c0 < nc; c0 += kRound) {
+    float lc[kRound];
+#pragma unroll
+    for (int k = 0; k < kRound; ++k)
+      lc[k] = c0 + k < nc ? __ldcg(a.ws_lse + p0 + (c0 + k) * stride_c) : neg_inf();
+#pragma unroll
+    for (int k = 0; k < kRound; ++k) m = fmaxf(m, lc[k]);
+  }
   float o[16];
 #pragma unroll
   for (int x = 0; x < 16; ++x) o[x] = 0.f;
   float wsum = 0.f;
-  if (m != neg_inf()) {
-    for (int c = 0; c < nc; ++c) {   // a chunk without keys has LSE -inf: weight 0
-      const int64_t p = p0 + c * stride_c;
-      const float lc = __ldcg(a.ws_lse + p);
-      const float w = lc == neg_inf() ? 0.f : ex2(lc - m);
-      wsum += w;
+  for (int c0 = 0; c0 < nc && m != neg_inf(); c0 += kRound) {
+    float lc[kRound];
+    float4 v[kRound][4];
+#pragma unroll
+    for (int k = 0; k < kRound; ++k) {
+      const int64_t p = p0 + (c0 + k) * stride_c;
+      const bool in = c0 + k < nc;
+      lc[k] = in ? __ldcg(a.ws_lse + p) : neg_inf();
       const float4* src = reinterpret_cast<const float4*>(a.ws_o + p * 128 + d0);
 #pragma unroll
+      for (int x = 0; x < 4; ++x) v[k][x] = in ? __ldcg(src + x) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kRound; ++k) {   // a chunk without keys has LSE -inf: weight 0
+      const float w = lc[k] == neg_inf() ? 0.f : ex2(lc[k] - m);
+      wsum += w;
+#pragma unroll
       for (int x = 0; x < 4; ++x) {
-        const float4 v = __ldcg(src + x);
-        o[4 * x] += w * v.x;
-        o[4 * x + 1] += w * v.y;
-        o[4 * x + 2] += w * v.z;
-        o[4 * x + 3] += w * v.w;
+        o[4 * x] += w * v[k][x].x;
+        o[4 * x + 1] += w * v[k][x].y;
+        o[4 * x + 2] += w * v[k][x].z;
+        o[4 * x + 3] += w * v[k][x].w;
       }
     }
   }
