@@ -21,17 +21,21 @@ namespace dev {
 __device__ __forceinline__ void split_merge_if_last(const DecodeArgs& a, const ReqInfo& rq, int hk,
                                                     int tile, int r0, int nrows) {
   __shared__ int s_last;
-  __threadfence();   // this thread's partial writes, before the CTA counts itself
+  // The CTA's partial writes happen before thread 0's count (barrier), and the
+  // count is an acquire-release atomic at GPU scope: it publishes them (fences
+  // are cumulative), and the last count acquires every earlier CTA's writes,
+  // which the barrier below hands on to the CTA's other threads.
   __syncthreads();
   if (threadIdx.x == 0) {
     int32_t* cnt = a.merge_cnt + rq.cnt_base + hk * a.tiles_per_item + tile;
-    const bool last = atomicAdd(cnt, 1) == rq.n_chunks - 1;
+    int32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
+    const bool last = old == rq.n_chunks - 1;
     if (last) *cnt = 0;   // every chunk has counted: ready for the next run
     s_last = last;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();   // the other chunks' partials, counted before us, are visible
   const int rr = threadIdx.x >> 3, d0 = (threadIdx.x & 7) * 16;   // 16 rows x 8 x 16 dims
   if (rr >= nrows) return;
   const int G = a.group, r = r0 + rr;
