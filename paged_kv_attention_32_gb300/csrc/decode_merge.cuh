@@ -43,23 +43,15 @@ __device__ __forceinline__ void split_merge_if_last(const DecodeArgs& a, const R
   const int nc = rq.n_chunks;
   const int64_t stride_c = (int64_t)rq.q_len * a.num_qo_heads;
   const int64_t p0 = rq.part_base + (int64_t)i * a.num_qo_heads + h;
-  // loads go out kRound chunks at a time, so that a long chunk list costs a few
-  // rounds of memory latency rather than one per chunk
+  // One pass with a running maximum; the loads go out kRound chunks at a time,
+  // so that a long chunk list costs a few rounds of memory latency.  A chunk
+  // without keys has LSE -inf: weight 0.
   constexpr int kRound = 4;
-  float m = neg_inf();
-  for (int c0 = 0; c0 < nc; c0 += kRound) {
-    float lc[kRound];
-#pragma unroll
-    for (int k = 0; k < kRound; ++k)
-      lc[k] = c0 + k < nc ? __ldcg(a.ws_lse + p0 + (c0 + k) * stride_c) : neg_inf();
-#pragma unroll
-    for (int k = 0; k < kRound; ++k) m = fmaxf(m, lc[k]);
-  }
+  float m = neg_inf(), wsum = 0.f;
   float o[16];
 #pragma unroll
   for (int x = 0; x < 16; ++x) o[x] = 0.f;
-  float wsum = 0.f;
-  for (int c0 = 0; c0 < nc && m != neg_inf(); c0 += kRound) {
+  for (int c0 = 0; c0 < nc; c0 += kRound) {
     float lc[kRound];
     float4 v[kRound][4];
 #pragma unroll
@@ -71,8 +63,17 @@ __device__ __forceinline__ void split_merge_if_last(const DecodeArgs& a, const R
 #pragma unroll
       for (int x = 0; x < 4; ++x) v[k][x] = in ? __ldcg(src + x) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    float m_new = m;
 #pragma unroll
-    for (int k = 0; k < kRound; ++k) {   // a chunk without keys has LSE -inf: weight 0
+    for (int k = 0; k < kRound; ++k) m_new = fmaxf(m_new, lc[k]);
+    if (m_new == neg_inf()) continue;   // no keys so far
+    const float sc = ex2(m - m_new);    // 0 while m is still -inf
+    m = m_new;
+    wsum *= sc;
+#pragma unroll
+    for (int x = 0; x < 16; ++x) o[x] *= sc;
+#pragma unroll
+    for (int k = 0; k < kRound; ++k) {
       const float w = lc[k] == neg_inf() ? 0.f : ex2(lc[k] - m);
       wsum += w;
 #pragma unroll
