@@ -280,6 +280,11 @@ int paged_decode_plan_export(const pka_plan* plan, int32_t* items, int32_t* n_ch
  *                 has return_lse.
  * workspace       device scratch of at least the plan's workspace_bytes
  *                 (256-byte aligned); holds fp32 split-KV partials.
+ *
+ * A request cut into chunks is merged inside the decode kernel: the chunk CTA
+ * that finishes last combines the partials, counted on counters in the plan's
+ * device buffer (zero between runs).  Runs that use one plan must therefore
+ * not overlap on the GPU (queue them on one stream, or order the streams).
  */
 int paged_decode_run(const pka_plan* plan, const void* q, int64_t q_stride_tok,
                      int64_t q_stride_head, const void* k_pages, const void* v_pages,
