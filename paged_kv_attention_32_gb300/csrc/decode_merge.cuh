@@ -13,11 +13,75 @@
 namespace pka {
 namespace dev {
 
-// Called by every thread of a CTA of a split request after the CTA wrote its
-// partial rows r0 .. r0 + nrows - 1 of the work item (row r = i * group + g:
-// token i, head hk * group + g).  Returns at once unless this CTA is the
-// group's last; that CTA resets the group's counter to zero (every chunk has
-// counted) and writes the final O (out_dtype, bmm2_scale) and LSE of the rows.
+// The merge of rows r0 .. r0 + nrows - 1 by one CTA of 128 threads: TPR
+// threads per row, each owning 128 / TPR dims, with the loads of KR chunks in
+// flight per round (16 float4 per thread whatever TPR is), in one pass with a
+// running maximum.  A chunk without keys has LSE -inf: weight 0.
+template <int TPR>
+__device__ __forceinline__ void merge_rows(const DecodeArgs& a, const ReqInfo& rq, int hk, int r0,
+                                           int nrows) {
+  constexpr int DPT = 128 / TPR, KR = 64 / DPT, NV = DPT / 4;
+  const int rr = threadIdx.x / TPR, d0 = (threadIdx.x % TPR) * DPT;
+  if (rr >= nrows) return;
+  const int G = a.group, r = r0 + rr;
+  const int i = r / G, h = hk * G + r % G;
+  const int nc = rq.n_chunks;
+  const int64_t stride_c = (int64_t)rq.q_len * a.num_qo_heads;
+  const int64_t p0 = rq.part_base + (int64_t)i * a.num_qo_heads + h;
+  float m = neg_inf(), wsum = 0.f;
+  float o[DPT];
+#pragma unroll
+  for (int x = 0; x < DPT; ++x) o[x] = 0.f;
+  for (int c0 = 0; c0 < nc; c0 += KR) {
+    float lc[KR];
+    float4 v[KR][NV];
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+      const int64_t p = p0 + (c0 + k) * stride_c;
+      const bool in = c0 + k < nc;
+      lc[k] = in ? __ldcg(a.ws_lse + p) : neg_inf();
+      const float4* src = reinterpret_cast<const float4*>(a.ws_o + p * 128 + d0);
+#pragma unroll
+      for (int x = 0; x < NV; ++x)
+        v[k][x] = in ? __ldcg(src + x) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float m_new = m;
+#pragma unroll
+    for (int k = 0; k < KR; ++k) m_new = fmaxf(m_new, lc[k]);
+    if (m_new == neg_inf()) continue;   // no keys so far
+    const float sc = ex2(m - m_new);    // 0 while m is still -inf
+    m = m_new;
+    wsum *= sc;
+#pragma unroll
+    for (int x = 0; x < DPT; ++x) o[x] *= sc;
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+      const float w = lc[k] == neg_inf() ? 0.f : ex2(lc[k] - m);
+      wsum += w;
+#pragma unroll
+      for (int x = 0; x < NV; ++x) {
+        o[4 * x] += w * v[k][x].x;
+        o[4 * x + 1] += w * v[k][x].y;
+        o[4 * x + 2] += w * v[k][x].z;
+        o[4 * x + 3] += w * v[k][x].w;
+      }
+    }
+  }
+  float denom = wsum;
+  if (a.sinks != nullptr && m != neg_inf()) denom += ex2(__ldg(a.sinks + h) * kLog2e - m);
+  const float sc = denom > 0.f ? a.bmm2_scale / denom : 0.f;
+  const int64_t t = rq.q_start + i;
+  store_out<DPT>(a.out, (t * a.num_qo_heads + h) * 128 + d0, o, sc, a.out_dtype);
+  if (a.lse != nullptr && d0 == 0)
+    a.lse[t * a.num_qo_heads + h] = wsum > 0.f ? m + log2f(wsum) : neg_inf();
+}
+
+// Called by every thread of a CTA (128 threads) of a split request after the
+// CTA wrote its partial rows r0 .. r0 + nrows - 1 (nrows <= 16) of the work
+// item (row r = i * group + g: token i, head hk * group + g).  Returns at once
+// unless this CTA is the group's last; that CTA resets the group's counter to
+// zero (every chunk has counted) and writes the final O (out_dtype,
+// bmm2_scale) and LSE of the rows.
 __device__ __forceinline__ void split_merge_if_last(const DecodeArgs& a, const ReqInfo& rq, int hk,
                                                     int tile, int r0, int nrows) {
   __shared__ int s_last;
@@ -36,62 +100,11 @@ __device__ __forceinline__ void split_merge_if_last(const DecodeArgs& a, const R
   }
   __syncthreads();
   if (!s_last) return;
-  const int rr = threadIdx.x >> 3, d0 = (threadIdx.x & 7) * 16;   // 16 rows x 8 x 16 dims
-  if (rr >= nrows) return;
-  const int G = a.group, r = r0 + rr;
-  const int i = r / G, h = hk * G + r % G;
-  const int nc = rq.n_chunks;
-  const int64_t stride_c = (int64_t)rq.q_len * a.num_qo_heads;
-  const int64_t p0 = rq.part_base + (int64_t)i * a.num_qo_heads + h;
-  // One pass with a running maximum; the loads go out kRound chunks at a time,
-  // so that a long chunk list costs a few rounds of memory latency.  A chunk
-  // without keys has LSE -inf: weight 0.
-  constexpr int kRound = 4;
-  float m = neg_inf(), wsum = 0.f;
-  float o[16];
-#pragma unroll
-  for (int x = 0; x < 16; ++x) o[x] = 0.f;
-  for (int c0 = 0; c0 < nc; c0 += kRound) {
-    float lc[kRound];
-    float4 v[kRound][4];
-#pragma unroll
-    for (int k = 0; k < kRound; ++k) {
-      const int64_t p = p0 + (c0 + k) * stride_c;
-      const bool in = c0 + k < nc;
-      lc[k] = in ? __ldcg(a.ws_lse + p) : neg_inf();
-      const float4* src = reinterpret_cast<const float4*>(a.ws_o + p * 128 + d0);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) v[k][x] = in ? __ldcg(src + x) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float m_new = m;
-#pragma unroll
-    for (int k = 0; k < kRound; ++k) m_new = fmaxf(m_new, lc[k]);
-    if (m_new == neg_inf()) continue;   // no keys so far
-    const float sc = ex2(m - m_new);    // 0 while m is still -inf
-    m = m_new;
-    wsum *= sc;
-#pragma unroll
-    for (int x = 0; x < 16; ++x) o[x] *= sc;
-#pragma unroll
-    for (int k = 0; k < kRound; ++k) {
-      const float w = lc[k] == neg_inf() ? 0.f : ex2(lc[k] - m);
-      wsum += w;
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        o[4 * x] += w * v[k][x].x;
-        o[4 * x + 1] += w * v[k][x].y;
-        o[4 * x + 2] += w * v[k][x].z;
-        o[4 * x + 3] += w * v[k][x].w;
-      }
-    }
-  }
-  float denom = wsum;
-  if (a.sinks != nullptr && m != neg_inf()) denom += ex2(__ldg(a.sinks + h) * kLog2e - m);
-  const float sc = denom > 0.f ? a.bmm2_scale / denom : 0.f;
-  const int64_t t = rq.q_start + i;
-  store_out<16>(a.out, (t * a.num_qo_heads + h) * 128 + d0, o, sc, a.out_dtype);
-  if (a.lse != nullptr && d0 == 0)
-    a.lse[t * a.num_qo_heads + h] = wsum > 0.f ? m + log2f(wsum) : neg_inf();
+  // a group of at most 8 rows with a long chunk list: 16 threads per row and
+  // 8 chunks per round (fewer rounds of memory latency); else 8 threads per
+  // row and 4 chunks per round
+  if (rq.n_chunks > 8 && nrows <= 8) merge_rows<16>(a, rq, hk, r0, nrows);
+  else merge_rows<8>(a, rq, hk, r0, nrows);
 }
 
 }  // namespace dev

@@ -7,7 +7,9 @@
 //   S = Q K^T          (mma.sync m16n8k16: 2 n-tiles of 8 keys x 8 k-steps,
 //                       Q kept as A fragments in registers)
 //   mask               (causal diagonal kv_len - q_len + i, window_left)
-//   online softmax     (base 2, the scale folded into one multiply)
+//   online softmax     (base 2, the scale folded into one multiply; the
+//                       reference max moves only when a row max passes it
+//                       by more than 2^8, found by one warp vote per unit)
 //   O += P V           (P re-packed to A fragments of the input type, V via
 //                       ldmatrix.trans)
 // A unit is four 2 KB blocks with 128-byte swizzle: K columns 0-63, K 64-127,
@@ -121,17 +123,31 @@ struct MmaTileWarp {
         }
         s[nt][c] = v;
       }
+    // lazy reference: the quad max is taken only when some lane's own max
+    // passes its row's reference by more than 2^8 (one vote otherwise)
     float pmA = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
     float pmB = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-    pmA = fmaxf(pmA, __shfl_xor_sync(FULL, pmA, 1));
-    pmB = fmaxf(pmB, __shfl_xor_sync(FULL, pmB, 1));
-    pmA = fmaxf(pmA, __shfl_xor_sync(FULL, pmA, 2));
-    pmB = fmaxf(pmB, __shfl_xor_sync(FULL, pmB, 2));
-    const float mAn = fmaxf(mA, pmA), mBn = fmaxf(mB, pmB);
-    const float uA = mAn == neg_inf() ? 0.f : mAn, uB = mBn == neg_inf() ? 0.f : mBn;
-    const float alA = ex2(mA - uA), alB = ex2(mB - uB);
-    mA = mAn;
-    mB = mBn;
+    float alA = 1.f, alB = 1.f;
+    if (__any_sync(FULL, pmA > mA + 8.f || pmB > mB + 8.f)) {
+      pmA = fmaxf(pmA, __shfl_xor_sync(FULL, pmA, 1));
+      pmB = fmaxf(pmB, __shfl_xor_sync(FULL, pmB, 1));
+      pmA = fmaxf(pmA, __shfl_xor_sync(FULL, pmA, 2));
+      pmB = fmaxf(pmB, __shfl_xor_sync(FULL, pmB, 2));
+      const bool gA = pmA > mA + 8.f, gB = pmB > mB + 8.f;
+      const float mAn = gA ? pmA : mA, mBn = gB ? pmB : mB;
+      if (gA) alA = ex2(mA - mAn);
+      if (gB) alB = ex2(mB - mBn);
+      mA = mAn;
+      mB = mBn;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        acc[n][0] *= alA;
+        acc[n][1] *= alA;
+        acc[n][2] *= alB;
+        acc[n][3] *= alB;
+      }
+    }
+    const float uA = mA == neg_inf() ? 0.f : mA, uB = mB == neg_inf() ? 0.f : mB;
     float sumA = 0.f, sumB = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -144,15 +160,6 @@ struct MmaTileWarp {
     }
     lA = lA * alA + sumA;
     lB = lB * alB + sumB;
-    if (__any_sync(FULL, alA != 1.f || alB != 1.f)) {
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        acc[n][0] *= alA;
-        acc[n][1] *= alA;
-        acc[n][2] *= alB;
-        acc[n][3] *= alB;
-      }
-    }
     uint32_t pa[4];
     pa[0] = pack2<F16>(s[0][0], s[0][1]);
     pa[1] = pack2<F16>(s[0][2], s[0][3]);
