@@ -191,7 +191,8 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
   for (int k = 0; k < pre; ++k) issue(k);
 
   float* pw = pbuf + warp * kUnit * R;
-  for (int k = 0; k < my_units; ++k) {
+  int k = 0;
+  for (; k < my_units; ++k) {
     const int st = k % NSTAGE;
     // same outcome in every lane: the shuffles below need the whole warp
     if (!__all_sync(FULL, mbar_wait(bar_u32 + st * 8, (uint32_t)((k / NSTAGE) & 1), a.status)))
@@ -301,6 +302,10 @@ decode_cc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ C
     __syncwarp();
     if (k + NSTAGE < my_units) issue(k + NSTAGE);
   }
+  // a wait gave up: let the copies still in flight land (bounded) before the
+  // stages are reused or the CTA exits
+  for (int j = k; j < my_units && j < k + NSTAGE; ++j)
+    (void)mbar_wait(bar_u32 + (j % NSTAGE) * 8, (uint32_t)((j / NSTAGE) & 1), a.status);
 
   // ---- reduce over the key slots of the warp ----
 #pragma unroll

@@ -118,7 +118,8 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   const int pre = my_units < NSTAGE ? my_units : NSTAGE;
   for (int k = 0; k < pre; ++k) issue(k);
 
-  for (int k = 0; k < my_units; ++k) {
+  int k = 0;
+  for (; k < my_units; ++k) {
     const int st = k % NSTAGE;
     if (!__all_sync(FULL, mbar_wait(bar_u32 + st * 8, (uint32_t)((k / NSTAGE) & 1), a.status)))
       break;
@@ -128,6 +129,10 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
     __syncwarp();
     if (k + NSTAGE < my_units) issue(k + NSTAGE);
   }
+  // a wait gave up: let the copies still in flight land (bounded) before the
+  // stages are reused or the CTA exits
+  for (int j = k; j < my_units && j < k + NSTAGE; ++j)
+    (void)mbar_wait(bar_u32 + (j % NSTAGE) * 8, (uint32_t)((j / NSTAGE) & 1), a.status);
   tw.reduce_l();
 
   // ---- merge the four warps through shared memory ----

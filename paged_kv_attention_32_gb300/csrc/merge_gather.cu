@@ -83,7 +83,10 @@ paged_gather_kernel(const __grid_constant__ CUtensorMap map, const int32_t* __re
       mbar_arrive_expect_tx(bar_u32, 2 * kBoxBytes);
       tma_load_kv_unit(dst, &map, bar_u32, (u % upp) * kUnit, kv_head, pid);
     }
-    if (!mbar_wait(bar_u32, phase, status)) return;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar_u32, phase, status))) {
+      (void)mbar_wait(bar_u32, phase, nullptr);   // the copy in flight: one more bounded wait
+      return;
+    }
     phase ^= 1u;
     // lane -> (row j = lane / 2 .. , chunk): 16 rows x 16 chunks = 256 chunk copies
     for (int q = lane; q < kUnit * 16; q += 32) {
