@@ -37,7 +37,7 @@ def test_decode_matches_oracle(name, seed):
 
 @pytest.mark.parametrize("name", ["llama3_8b", "skewed"])
 def test_decode_split_kv_path(name):
-    """Few SMs in the plan force a split of the long requests: partials + merge kernel."""
+    """Few SMs in the plan force a split of the long requests: partials merged in the run."""
     inp = wl.make_decode_inputs(SMALL[name], seed=3, device=DEV)
     out, lse, plan = run_decode(inp, num_sms=32, split_waves=2, min_chunk_tokens=128)
     assert plan.info["num_split"] > 0
@@ -46,13 +46,14 @@ def test_decode_split_kv_path(name):
 
 
 @pytest.mark.parametrize("name,sms", [("spec", 148), ("skewed", 148), ("skewed", 48),
-                                      ("llama3_8b", 64)])
+                                      ("llama3_8b", 64), ("llama3_8b", 1024)])
 def test_decode_split_merge_by_the_last_chunk(name, sms):
     """Split partials are merged inside the decode kernels: the chunk CTA of a (request,
     KV head, tile) group that counts last combines the group's rows (spec: <= 3 chunks
-    over packed causal rows, three tiles; skewed: 19 or 6 chunks; llama3_8b: the
-    CUDA-core kernel).  Run twice, so that the counters left by the first run (reset to
-    zero by each group's last CTA) serve the second."""
+    over packed causal rows, three tiles; skewed: 19 chunks, merged with 16 threads per
+    row, or 6, with 8; llama3_8b: the CUDA-core kernel, with up to 17 chunks at a planned
+    1024 SMs).  Run twice, so that the counters left by the first run (reset to zero by
+    each group's last CTA) serve the second."""
     inp = wl.make_decode_inputs(SMALL[name], seed=5, device=DEV)
     from helpers import decode_plan_for
     plan = decode_plan_for(inp, num_sms=sms, split_waves=2, min_chunk_tokens=128)
@@ -226,6 +227,20 @@ def test_decode_largest_page_sizes(G, ps):
                           head_dim=128, page_size=ps, kv_len_range=(1, 2000), causal=True)
     inp = wl.make_decode_inputs(w, seed=18, device=DEV)
     out, lse, _ = run_decode(inp)
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("G,ps", [(4, 48), (8, 80), (2, 208)])
+def test_decode_page_sizes_not_powers_of_two(G, ps):
+    """Any multiple of 16 is a page size: 3, 5 and 13 TMA units per page, with split
+    requests whose chunks end inside the unit runs of such pages."""
+    w = wl.DecodeWorkload(name="oddpage", batch=3, num_qo_heads=2 * G, num_kv_heads=2,
+                          head_dim=128, page_size=ps, kv_len_range=(1, 2000), causal=True,
+                          sinks=True)
+    inp = wl.make_decode_inputs(w, seed=20 + ps, device=DEV)
+    out, lse, plan = run_decode(inp)
+    assert plan.info["num_split"] > 0
     ref_o, ref_l = oracle_decode(inp)
     assert_close(out, lse, ref_o, ref_l)
 

@@ -34,7 +34,7 @@ def test_merge_matches_oracle(N, S, H, D, out_dtype):
     assert np.all(got[0, 0] == 0)
 
 
-@pytest.mark.parametrize("ps", [16, 32, 64])
+@pytest.mark.parametrize("ps", [16, 32, 48, 64, 80])
 def test_gather_is_bit_exact(ps):
     w = wl.DecodeWorkload(name="g", batch=3, num_qo_heads=4, num_kv_heads=2, head_dim=128,
                           page_size=ps, kv_len_range=(1, 500))
