@@ -434,7 +434,7 @@ def measure_workload(name, seed, steps, warmup, peak_gbs, dist=None, dtype=None)
            "ms_per_call": round(ms, 5), "kv_bytes": nbytes,
            "kv_tokens": keys, "GB_per_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak_gbs, 4),
            "kernel": ["cuda_core", "mma"][info["kernel"]], "ctas": info["num_items"],
-           "split_requests": info["num_split"], "launches_per_call": 1 + (info["num_split"] > 0)}
+           "split_requests": info["num_split"], "launches_per_call": 1}   # the split merge runs inside the decode kernel
     return res, inp, plan
 
 
