@@ -355,8 +355,8 @@ def time_decode(inp, plan, steps, warmup, dist=None):
 
 def time_decode_e2e(inp, plan_kw, steps, warmup):
     """One serving step through the C ABI with host buffers, wall clock per step:
-    ``paged_decode_step_host`` re-plans one plan on the step's host lengths,
-    copies q / block tables (pinned host) to the device, runs the decode and
+    ``paged_decode_step_host`` copies q / block tables (pinned host) to the
+    device, re-plans one plan on the step's host lengths, runs the decode and
     copies O and the LSE back to pinned host memory, then synchronises.  The KV
     pools are the cache: they stay resident on the device."""
     import torch

@@ -17,7 +17,7 @@
  *       packed ragged causal context attention:
  *       "flashinfer.attention.prims_ts.batch_prefill".
  *   paged_decode_step_host
- *       one decode step from host buffers: re-plan, copies in, run, copies
+ *       one decode step from host buffers: copies in, re-plan, run, copies
  *       out, queued in order on one stream.
  *   paged_decode_check_tables
  *       validation of the block-table entries a decode run reads.
@@ -327,18 +327,20 @@ typedef struct pka_decode_host_io {
 } pka_decode_host_io;
 
 /*
- * One decode step from host buffers, as a serving loop runs it: re-plan
- * `plan` on the step's lengths (paged_decode_plan_update), copy q, the block
- * table rows (and the live lengths) host -> device, run the decode over the
+ * One decode step from host buffers, as a serving loop runs it: copy q, the
+ * block table rows (and the live lengths) host -> device, re-plan `plan` on
+ * the step's lengths (paged_decode_plan_update), run the decode over the
  * device-resident K/V pools (arguments as for paged_decode_run, with dense q),
  * and copy O (and the LSE) device -> host, all queued on `stream` in that
- * order.  With `synchronize` nonzero the call returns once O is in host
+ * order (the input copies first, so that the GPU moves them while the host
+ * re-plans).  With `synchronize` nonzero the call returns once O is in host
  * memory; otherwise the caller synchronises `stream` before reading it.
  * workspace_bytes_out (may be NULL) receives the re-planned workspace size.
- * Arguments are checked before anything is queued, and a failed re-plan
- * leaves the plan unchanged.  PKA_ERR_WORKSPACE_TOO_SMALL means the plan was
- * re-planned (its upload queued) but needs more workspace than given, and
- * nothing else was queued.
+ * The io, the pointers and the query rows (qo_indptr_host) are checked
+ * before anything is queued.  A re-plan that fails leaves the plan unchanged,
+ * with only the input copies queued.  PKA_ERR_WORKSPACE_TOO_SMALL means the
+ * plan was re-planned (its upload queued after the input copies) but needs
+ * more workspace than given: the run and the output copies were not queued.
  */
 int paged_decode_step_host(pka_plan* plan, int32_t batch_size, const pka_decode_host_io* io,
                            const void* k_pages, const void* v_pages, int64_t kv_stride_page,

@@ -418,18 +418,24 @@ int paged_decode_step_host(pka_plan* p, int32_t batch_size, const pka_decode_hos
                 "K/V pools must be 16-byte aligned with strides that are multiples of 8");
   PKA_CHECK_ARG(workspace == nullptr || aligned(workspace, 256),
                 "workspace must be 256-byte aligned");
+  PKA_CHECK_ARG(batch_size >= 1, "batch_size must be >= 1 (got %d)", batch_size);
   int rc = check_device(p->device);
   if (rc != PKA_OK) return rc;
 
-  rc = paged_decode_plan_update(p, batch_size, io->seq_lens_kv_host, io->qo_indptr_host,
-                                workspace_bytes_out, stream);
-  if (rc != PKA_OK) return rc;
-  if (p->workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < (size_t)p->workspace_bytes))
-    return fail(PKA_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, the plan needs %lld",
-                workspace_bytes, (long long)p->workspace_bytes);
-
+  // The input copies go first: their sizes follow from the host arrays alone,
+  // so the GPU moves them while the host re-plans.  The query rows are counted
+  // as the planner counts them (packed when qo_indptr is given).
+  int64_t total_q = (int64_t)batch_size * p->desc.q_len;
+  if (io->qo_indptr_host != nullptr) {
+    const int32_t* ind = io->qo_indptr_host;
+    PKA_CHECK_ARG(ind[0] == 0, "qo_indptr[0] must be 0 (got %d)", ind[0]);
+    for (int32_t b = 0; b < batch_size; ++b)
+      PKA_CHECK_ARG(ind[b + 1] > ind[b], "request %d has %lld query rows; packed rows must be >= 1",
+                    b, (long long)ind[b + 1] - ind[b]);
+    total_q = ind[batch_size];
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t rows = (size_t)p->total_q * (size_t)p->Hq;
+  const size_t rows = (size_t)total_q * (size_t)p->Hq;
   const size_t out_elem = p->desc.out_dtype == PKA_DTYPE_F32 ? 4 : 2;
   PKA_CUDA_TRY(cudaMemcpyAsync(io->q_dev, io->q_host, rows * p->D * 2, cudaMemcpyHostToDevice, s),
                "cudaMemcpyAsync (q)");
@@ -441,6 +447,16 @@ int paged_decode_step_host(pka_plan* p, int32_t batch_size, const pka_decode_hos
     PKA_CUDA_TRY(cudaMemcpyAsync(io->seq_lens_kv_dev, io->seq_lens_kv_host,
                                  (size_t)batch_size * sizeof(int32_t), cudaMemcpyHostToDevice, s),
                  "cudaMemcpyAsync (lengths)");
+
+  rc = paged_decode_plan_update(p, batch_size, io->seq_lens_kv_host, io->qo_indptr_host,
+                                workspace_bytes_out, stream);
+  if (rc != PKA_OK) return rc;
+  if (p->total_q != total_q)
+    return fail(PKA_ERR_INVALID_ARG, "the plan counts %d query rows, the step copied %lld",
+                p->total_q, (long long)total_q);
+  if (p->workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < (size_t)p->workspace_bytes))
+    return fail(PKA_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, the plan needs %lld",
+                workspace_bytes, (long long)p->workspace_bytes);
   rc = paged_decode_run(p, io->q_dev, (int64_t)p->Hq * p->D, p->D, k_pages, v_pages,
                         kv_stride_page, kv_stride_head, io->block_tables_dev, io->bt_row_stride,
                         io->seq_lens_kv_dev, sinks, io->out_dev,

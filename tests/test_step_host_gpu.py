@@ -1,5 +1,5 @@
-"""paged_decode_step_host: one decode step from host buffers (re-plan on the
-step's lengths, copies in, run, copies out) returns the bytes paged_decode_run
+"""paged_decode_step_host: one decode step from host buffers (copies in, re-plan
+on the step's lengths, run, copies out) returns the bytes paged_decode_run
 returns on device copies of the same inputs, step after step, and matches the
 oracle."""
 
