@@ -856,9 +856,10 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
                     "h2d_bytes_per_step": bin_, "d2h_bytes_per_step": bout,
-                    "note": "paged_decode_step_host per step: host re-planning of one plan "
-                            "on the step's lengths + pinned H2D of q/tables + run + D2H of "
-                            "O and LSE + synchronise; the KV cache stays resident"},
+                    "note": "paged_decode_step_host per step: pinned H2D of q/tables, host "
+                            "re-planning of one plan on the step's lengths (while the copies "
+                            "run), run, D2H of O and LSE, synchronise; the KV cache stays "
+                            "resident"},
             "gpu_launches": args.steps * head["launches_per_call"],
             "clocks": clocks,
         }
