@@ -31,8 +31,9 @@
  * Conventions shared by every entry point
  *   - Return value: PKA_OK (0) or a negative PKA_ERR_* code.  The message of
  *     the last error on the calling thread is returned by pka_last_error().
- *   - All arguments are checked on the host before anything is launched; an
- *     invalid argument launches nothing.  No kernel traps or asserts.
+ *   - All arguments are checked on the host before any kernel is launched; an
+ *     invalid argument launches no kernel (paged_decode_step_host may have
+ *     queued its input copies by then, see there).  No kernel traps or asserts.
  *   - Device pointers are raw CUDA device addresses of the current device.
  *     `stream` is a cudaStream_t (NULL = legacy default stream).
  *   - Element strides are in elements, not bytes.

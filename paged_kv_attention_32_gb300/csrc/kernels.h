@@ -10,8 +10,8 @@
 
 namespace pka {
 
-// Decode kernel (CUDA-core or mma variant, as the plan chose) followed, when
-// the plan split any request, by the partial-merge kernel.
+// Decode kernel (CUDA-core or mma variant, as the plan chose); the partials of
+// a split request are merged inside it by the last chunk CTA of each group.
 int launch_decode(const pka_plan& plan, const DecodeArgs& args, const CUtensorMap& kmap,
                   const CUtensorMap& vmap, cudaStream_t stream);
 
@@ -20,7 +20,6 @@ int launch_merge_states(const float* v_states, const float* s_states, int32_t n,
                         int32_t h, int32_t d, void* v_out, int32_t out_dtype, float* s_out,
                         cudaStream_t stream);
 
-// Test hook: paged rows -> dense rows through the decode kernels' addressing.
 // Checks the block-table entries a run of the plan reads (see pka.h,
 // paged_decode_check_tables); a bad one sets STATUS_PAGE_BOUNDS in *status.
 int launch_check_tables(const WorkItem* items, int32_t num_items, const ReqInfo* reqs,
@@ -36,6 +35,7 @@ int launch_wait_probe(uint64_t limit_ns, int32_t* status, cudaStream_t stream);
 // scratch on the current device (set up on first use, on `stream`).
 int noalloc_status_word(cudaStream_t stream, int32_t** out);
 
+// Test hook: paged rows -> dense rows through the decode kernels' addressing.
 int launch_paged_gather(const CUtensorMap& map, const int32_t* block_tables,
                         int64_t bt_row_stride, int32_t page_size, int32_t request,
                         int32_t kv_head, int32_t tok_begin, int32_t tok_end, void* out,
