@@ -299,6 +299,16 @@ int paged_decode_run(const pka_plan* plan, const void* q, int64_t q_stride_tok,
  * should be pinned (page-locked) for the copies to be asynchronous; device
  * staging arrays are the caller's and hold at least the sizes below.
  *
+ * In place: a device array may be given as its host array itself (the same
+ * pointer: q_dev == q_host, block_tables_dev == block_tables_host,
+ * seq_lens_kv_dev == seq_lens_kv_host, out_dev == out_host, lse_dev ==
+ * lse_host).  It must then be page-locked host memory that the device can
+ * address (checked with cudaPointerGetAttributes, else PKA_ERR_INVALID_ARG):
+ * the step copies nothing for it, and the kernels read (q, table rows, live
+ * lengths) or write (O, LSE) it where it is, over the host link (NVLink-C2C
+ * on a Grace-Blackwell node).  Such arrays must not be touched by the host
+ * while the step runs.
+ *
  * q_host, q_dev            [total_q, Hq, D] dense, the plan's input type.
  * block_tables_host, _dev  [batch_size, bt_row_stride] int32 (as for
  *                          paged_decode_run); the whole rows are copied.

@@ -199,9 +199,12 @@ class DecodeHostIO:
 
     Host tensors (CPU, pinned for asynchronous copies) hold each step's q, block
     table rows and key lengths and receive O (and the LSE); device tensors of the
-    same shapes are the staging copies the run reads and writes.  The buffers are
-    sized for the largest batch; a step uses their leading rows.  The object keeps
-    every tensor alive and a workspace that grows when a re-plan needs more."""
+    same shapes are the staging copies the run reads and writes.  A device slot may
+    be given its host tensor itself when that is pinned: the run then reads or
+    writes the host memory in place and the step copies nothing for it.  The
+    buffers are sized for the largest batch; a step uses their leading rows.  The
+    object keeps every tensor alive and a workspace that grows when a re-plan
+    needs more."""
 
     def __init__(self, q_host, block_tables_host, seq_lens_kv_host, out_host, q_dev,
                  block_tables_dev, out_dev, lse_host=None, lse_dev=None, seq_lens_kv_dev=None,
@@ -220,6 +223,12 @@ class DecodeHostIO:
             if t is not None and t.dtype != torch.int32:
                 raise ValueError(f"{name} must be int32")
         for name, t in dev.items():
+            h = host.get(name[:-4] + "_host")
+            if t is not None and h is not None and t is h:   # in place: pinned host memory
+                if not h.is_pinned():
+                    raise ValueError(f"{name} may be {name[:-4]}_host itself only when that "
+                                     "tensor is pinned")
+                continue
             if t is not None and (t.device.type != "cuda" or not t.is_contiguous()):
                 raise ValueError(f"{name} must be a contiguous CUDA tensor")
         pairs = (("q", q_host, q_dev), ("block_tables", block_tables_host, block_tables_dev),
@@ -237,9 +246,10 @@ class DecodeHostIO:
 
 def paged_decode_step_host(plan, io, k_pages, v_pages, sinks=None, batch_size=None,
                            synchronize=True, stream=None):
-    """One decode step from host buffers (``paged_decode_step_host``): re-plan on the
-    lengths in ``io``, copy q / tables (/ lengths) in, run, copy O (/ LSE) out.
-    With ``synchronize`` the host outputs are ready on return."""
+    """One decode step from host buffers (``paged_decode_step_host``): copy q / tables
+    (/ lengths) in, re-plan on the lengths in ``io``, run, copy O (/ LSE) out; arrays
+    the io gives in place are read or written where they are.  With ``synchronize``
+    the host outputs are ready on return."""
     t = io.tensors
     _check_inputs(plan, t["q_host"], k_pages, v_pages)
     _check_layout(t["q_dev"], k_pages, v_pages, t["out_dev"], t["lse_dev"], paged=True)
@@ -267,7 +277,7 @@ def paged_decode_step_host(plan, io, k_pages, v_pages, sinks=None, batch_size=No
         if rc != L.PKA_ERR_WORKSPACE_TOO_SMALL or attempt == 1:
             break
         io.workspace = torch.empty(ws_need.value + ws_need.value // 4 + 256, dtype=torch.uint8,
-                                   device=t["q_dev"].device)
+                                   device=k_pages.device)
     L.check(rc, "paged_decode_step_host")
     return (t["out_host"], t["lse_host"]) if plan.desc.return_lse else t["out_host"]
 

@@ -390,6 +390,20 @@ int paged_decode_run(const pka_plan* p, const void* q, int64_t q_stride_tok,
   return launch_decode(*p, a, kmap, vmap, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// The device address of `host` when it is page-locked host memory the current
+// device can address (a kernel may then read or write it in place over the
+// host link), else nullptr.
+void* host_mapped(const void* host) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, host) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return attr.type == cudaMemoryTypeHost ? attr.devicePointer : nullptr;
+}
+}  // namespace
+
 int paged_decode_step_host(pka_plan* p, int32_t batch_size, const pka_decode_host_io* io,
                            const void* k_pages, const void* v_pages, int64_t kv_stride_page,
                            int64_t kv_stride_head, const float* sinks, void* workspace,
@@ -410,8 +424,33 @@ int paged_decode_step_host(pka_plan* p, int32_t batch_size, const pka_decode_hos
   PKA_CHECK_ARG(io->bt_row_stride >= p->C,
                 "bt_row_stride (%lld) is smaller than the table width %d",
                 (long long)io->bt_row_stride, p->C);
-  PKA_CHECK_ARG(aligned(io->q_dev, 16) && aligned(io->out_dev, 16) &&
-                    (io->lse_dev == nullptr || aligned(io->lse_dev, 4)),
+  // A device array given as its host array itself is used in place: the
+  // kernel reads (or writes) the page-locked host memory directly, and the
+  // step copies nothing for it.
+  const void* q_use = io->q_dev;
+  const int32_t* bt_use = io->block_tables_dev;
+  const int32_t* len_use = io->seq_lens_kv_dev;
+  void* out_use = io->out_dev;
+  float* lse_use = io->lse_dev;
+  const bool q_in = io->q_dev == io->q_host;
+  const bool bt_in = io->block_tables_dev == io->block_tables_host;
+  const bool len_in = io->seq_lens_kv_dev != nullptr && io->seq_lens_kv_dev == io->seq_lens_kv_host;
+  const bool out_in = io->out_dev == io->out_host;
+  const bool lse_in = io->lse_dev != nullptr && io->lse_dev == io->lse_host;
+  if (q_in || bt_in || len_in || out_in || lse_in) {
+    int rc0 = check_device(p->device);
+    if (rc0 != PKA_OK) return rc0;
+  }
+  if (q_in) q_use = host_mapped(io->q_host);
+  if (bt_in) bt_use = static_cast<const int32_t*>(host_mapped(io->block_tables_host));
+  if (len_in) len_use = static_cast<const int32_t*>(host_mapped(io->seq_lens_kv_host));
+  if (out_in) out_use = host_mapped(io->out_host);
+  if (lse_in) lse_use = static_cast<float*>(host_mapped(io->lse_host));
+  PKA_CHECK_ARG(q_use && bt_use && out_use && (!lse_in || lse_use) && (!len_in || len_use),
+                "a device array given as its host array must be page-locked host memory that "
+                "the device can address");
+  PKA_CHECK_ARG(aligned(q_use, 16) && aligned(out_use, 16) &&
+                    (lse_use == nullptr || aligned(lse_use, 4)),
                 "q_dev and out_dev must be 16-byte aligned, lse_dev 4-byte aligned");
   PKA_CHECK_ARG(aligned(k_pages, 16) && aligned(v_pages, 16) && kv_stride_page % 8 == 0 &&
                     kv_stride_head % 8 == 0,
@@ -437,13 +476,16 @@ int paged_decode_step_host(pka_plan* p, int32_t batch_size, const pka_decode_hos
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t rows = (size_t)total_q * (size_t)p->Hq;
   const size_t out_elem = p->desc.out_dtype == PKA_DTYPE_F32 ? 4 : 2;
-  PKA_CUDA_TRY(cudaMemcpyAsync(io->q_dev, io->q_host, rows * p->D * 2, cudaMemcpyHostToDevice, s),
-               "cudaMemcpyAsync (q)");
-  PKA_CUDA_TRY(cudaMemcpyAsync(io->block_tables_dev, io->block_tables_host,
-                               (size_t)batch_size * (size_t)io->bt_row_stride * sizeof(int32_t),
-                               cudaMemcpyHostToDevice, s),
-               "cudaMemcpyAsync (block tables)");
-  if (!p->desc.freeze_seq_lens)
+  if (!q_in)
+    PKA_CUDA_TRY(cudaMemcpyAsync(io->q_dev, io->q_host, rows * p->D * 2, cudaMemcpyHostToDevice,
+                                 s),
+                 "cudaMemcpyAsync (q)");
+  if (!bt_in)
+    PKA_CUDA_TRY(cudaMemcpyAsync(io->block_tables_dev, io->block_tables_host,
+                                 (size_t)batch_size * (size_t)io->bt_row_stride * sizeof(int32_t),
+                                 cudaMemcpyHostToDevice, s),
+                 "cudaMemcpyAsync (block tables)");
+  if (!p->desc.freeze_seq_lens && !len_in)
     PKA_CUDA_TRY(cudaMemcpyAsync(io->seq_lens_kv_dev, io->seq_lens_kv_host,
                                  (size_t)batch_size * sizeof(int32_t), cudaMemcpyHostToDevice, s),
                  "cudaMemcpyAsync (lengths)");
@@ -457,16 +499,16 @@ int paged_decode_step_host(pka_plan* p, int32_t batch_size, const pka_decode_hos
   if (p->workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < (size_t)p->workspace_bytes))
     return fail(PKA_ERR_WORKSPACE_TOO_SMALL, "workspace of %zu bytes, the plan needs %lld",
                 workspace_bytes, (long long)p->workspace_bytes);
-  rc = paged_decode_run(p, io->q_dev, (int64_t)p->Hq * p->D, p->D, k_pages, v_pages,
-                        kv_stride_page, kv_stride_head, io->block_tables_dev, io->bt_row_stride,
-                        io->seq_lens_kv_dev, sinks, io->out_dev,
-                        p->desc.return_lse ? io->lse_dev : nullptr, workspace, workspace_bytes,
+  rc = paged_decode_run(p, q_use, (int64_t)p->Hq * p->D, p->D, k_pages, v_pages, kv_stride_page,
+                        kv_stride_head, bt_use, io->bt_row_stride, len_use, sinks, out_use,
+                        p->desc.return_lse ? lse_use : nullptr, workspace, workspace_bytes,
                         stream);
   if (rc != PKA_OK) return rc;
-  PKA_CUDA_TRY(cudaMemcpyAsync(io->out_host, io->out_dev, rows * p->D * out_elem,
-                               cudaMemcpyDeviceToHost, s),
-               "cudaMemcpyAsync (out)");
-  if (p->desc.return_lse)
+  if (!out_in)
+    PKA_CUDA_TRY(cudaMemcpyAsync(io->out_host, io->out_dev, rows * p->D * out_elem,
+                                 cudaMemcpyDeviceToHost, s),
+                 "cudaMemcpyAsync (out)");
+  if (p->desc.return_lse && !lse_in)
     PKA_CUDA_TRY(cudaMemcpyAsync(io->lse_host, io->lse_dev, rows * sizeof(float),
                                  cudaMemcpyDeviceToHost, s),
                  "cudaMemcpyAsync (lse)");

@@ -89,3 +89,15 @@ def test_host_io_wants_host_and_device_tensors_where_stated():
         api.DecodeHostIO(q_host=q, block_tables_host=bt.long(), seq_lens_kv_host=seq,
                          out_host=q.clone(), q_dev=q.clone(), block_tables_dev=bt.clone(),
                          out_dev=q.clone())
+
+
+def test_host_io_in_place_needs_pinned_memory():
+    """A device slot of DecodeHostIO may be its host tensor only when that is pinned
+    (checked before any GPU work; plain CPU tensors are never pinned)."""
+    q = torch.zeros((4, 8, 128), dtype=torch.bfloat16)
+    bt = torch.zeros((4, 4), dtype=torch.int32)
+    seq = torch.ones(4, dtype=torch.int32)
+    out = torch.zeros_like(q)
+    with pytest.raises(ValueError, match="pinned"):
+        api.DecodeHostIO(q_host=q, block_tables_host=bt, seq_lens_kv_host=seq, out_host=out,
+                         q_dev=q, block_tables_dev=bt, out_dev=out)

@@ -1,5 +1,6 @@
 """paged_decode_step_host: one decode step from host buffers (copies in, re-plan
-on the step's lengths, run, copies out) returns the bytes paged_decode_run
+on the step's lengths, run, copies out; or host arrays used in place) returns the
+bytes paged_decode_run
 returns on device copies of the same inputs, step after step, and matches the
 oracle."""
 
@@ -20,23 +21,29 @@ LLAMA = wl.shrink(wl.LLAMA3_8B_DECODE, batch=6, kv_len_range=(512, 2100), pool_p
 SPEC = wl.shrink(wl.SPEC_DECODE, batch=6, kv_len_range=(2048, 6000), table_width=400)
 
 
-def _make_io(inp, out_dtype):
-    """Pinned host buffers and device staging sized for the batch in ``inp``."""
+def _make_io(inp, out_dtype, in_place=False):
+    """Pinned host buffers sized for the batch in ``inp``, with device staging, or
+    (``in_place``) with every device slot given its pinned host tensor itself."""
     q, bt, seq = inp["q"], inp["block_tables"], inp["seq_lens_kv"]
     rows = q.shape[:2]
-    io = api.DecodeHostIO(
+    host = dict(
         q_host=torch.empty(q.shape, dtype=q.dtype).pin_memory(),
         block_tables_host=torch.empty(bt.shape, dtype=torch.int32).pin_memory(),
         seq_lens_kv_host=torch.empty(seq.shape, dtype=torch.int32).pin_memory(),
         out_host=torch.empty(q.shape, dtype=out_dtype).pin_memory(),
         lse_host=torch.empty(rows, dtype=torch.float32).pin_memory(),
         qo_indptr_host=(None if inp["qo_indptr"] is None else
-                        torch.empty(inp["qo_indptr"].shape, dtype=torch.int32).pin_memory()),
-        q_dev=torch.empty_like(q), block_tables_dev=torch.empty_like(bt),
-        seq_lens_kv_dev=torch.empty_like(seq),
-        out_dev=torch.empty(q.shape, dtype=out_dtype, device=DEV),
-        lse_dev=torch.empty(rows, dtype=torch.float32, device=DEV))
-    return io
+                        torch.empty(inp["qo_indptr"].shape, dtype=torch.int32).pin_memory()))
+    if in_place:
+        dev = dict(q_dev=host["q_host"], block_tables_dev=host["block_tables_host"],
+                   seq_lens_kv_dev=host["seq_lens_kv_host"], out_dev=host["out_host"],
+                   lse_dev=host["lse_host"])
+    else:
+        dev = dict(q_dev=torch.empty_like(q), block_tables_dev=torch.empty_like(bt),
+                   seq_lens_kv_dev=torch.empty_like(seq),
+                   out_dev=torch.empty(q.shape, dtype=out_dtype, device=DEV),
+                   lse_dev=torch.empty(rows, dtype=torch.float32, device=DEV))
+    return api.DecodeHostIO(**host, **dev)
 
 
 def _fill(io, inp):
@@ -79,15 +86,18 @@ def _run_reference(inp, **kw):
     return out.cpu(), lse.cpu()
 
 
+@pytest.mark.parametrize("in_place", [False, True])
 @pytest.mark.parametrize("name,kw", [
     ("llama3_8b", {}),
     ("spec", dict(freeze_seq_lens=False, num_sms=32, split_waves=2, min_chunk_tokens=128)),
 ])
-def test_step_host_equals_run_step_after_step(name, kw):
+def test_step_host_equals_run_step_after_step(name, kw, in_place):
+    """Staged (device copies) or in place (the kernels read q, tables and live lengths
+    and write O and the LSE in pinned host memory): the same bytes either way."""
     w = LLAMA if name == "llama3_8b" else SPEC
     inp = wl.make_decode_inputs(w, seed=21, device=DEV)
     out_dtype = inp["q"].dtype
-    io = _make_io(inp, out_dtype)
+    io = _make_io(inp, out_dtype, in_place)
     plan = decode_plan_for(inp, **kw)
     split_seen = False
     for step, batch in enumerate([inp["seq_lens_kv"].numel(), 4, 5]):
@@ -137,3 +147,24 @@ def test_step_host_rejects_a_batch_larger_than_the_buffers():
     plan = decode_plan_for(small)
     with pytest.raises(ValueError):
         api.paged_decode_step_host(plan, io, inp["k_pages"], inp["v_pages"], batch_size=6)
+
+
+def test_step_host_refuses_unpinned_memory_in_place():
+    """Through the C ABI: a host array that is not page-locked, given as its own device
+    array, is refused before anything runs (the kernels could not address it)."""
+    import ctypes
+    from paged_kv_attention_32_gb300 import _lib as L
+    inp = wl.make_decode_inputs(LLAMA, seed=24, device=DEV)
+    io = _make_io(inp, inp["q"].dtype)
+    _fill(io, inp)
+    plan = decode_plan_for(inp)
+    q_plain = io.tensors["q_host"].clone()        # pageable host memory
+    c = L.DecodeHostIO.from_buffer_copy(io.c)
+    c.q_host = c.q_dev = q_plain.data_ptr()
+    ws_need = ctypes.c_size_t()
+    rc = L.lib().paged_decode_step_host(
+        plan.handle, inp["seq_lens_kv"].numel(), ctypes.byref(c), inp["k_pages"].data_ptr(),
+        inp["v_pages"].data_ptr(), inp["k_pages"].stride(0), inp["k_pages"].stride(1), None,
+        None, 0, ctypes.byref(ws_need), 1, torch.cuda.current_stream().cuda_stream)
+    assert rc == L.PKA_ERR_INVALID_ARG
+    assert "page-locked" in L.lib().pka_last_error().decode()
