@@ -37,7 +37,7 @@ PREFILL_WINDOW = 2047   # sliding-window variant of the ragged prefill (2048 key
 # the kernel symbol each decode plan launches
 KERNEL_SYMBOL = {"cuda_core": "decode_cc_kernel", "mma": "decode_mma_kernel"}
 NCU_TRAFFIC = {"kernel": "decode_cc_kernel", "kv_bytes": 1128361984,
-               "dram_bytes": 1130788608 + 3234048}
+               "dram_bytes": 1130799872 + 3269120}
 METRIC = "paged decode effective KV HBM GB/s"
 UNIT = "GB/s"
 
