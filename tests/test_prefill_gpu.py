@@ -220,6 +220,32 @@ def test_prefill_empty_and_single_row_requests(D):
     _run([0, 1, 0, 200, 1], [0, 1, 0, 230, 5], 4, 2, seed=90, D=D)
 
 
+@pytest.mark.parametrize("window", [-1, 4095])
+def test_prefill_one_long_request(window):
+    """One 32768-token causal request: a query tile visits up to 512 key tiles and the
+    K/V token coordinates pass 2^15; with and without a 4096-key window.  Sampled rows
+    (both ends of tiles, the middle, the last rows) and heads against the oracle."""
+    n, Hq, Hkv, D = 32768, 8, 2, 128
+    q, k, v = _rand((n, Hq, D), 40), _rand((n, Hkv, D), 41), _rand((n, Hkv, D), 42)
+    ind = _indptr([n])
+    plan = api.batch_prefill_plan(ind, ind, num_qo_heads=Hq, num_kv_heads=Hkv, causal=True,
+                                  return_lse=True, window_left=window)
+    out, lse = api.batch_prefill_run(plan, q, k, v)
+    torch.cuda.synchronize()
+    plan.check()
+    rows = [0, 1, 127, 128, 4095, 4096, 4097, 16383, 16384, 32639, 32640, 32767]
+    heads = [0, 3, 7]
+    ro, rl = oracle.prefill_request(0, wl.bf16_bits(q), wl.bf16_bits(k), wl.bf16_bits(v),
+                                    ind.numpy(), ind.numpy(), Hkv, heads=heads, rows=rows,
+                                    window_left=window)
+    got_o, got_l = out.float().cpu().numpy(), lse.cpu().numpy()
+    for h in heads:
+        d = np.abs(got_o[rows, h] - ro[rows, h])
+        assert (d <= O_ATOL + O_RTOL * np.abs(ro[rows, h])).all(), d.max()
+        assert (np.abs(got_l[rows, h] - rl[rows, h]) <= LSE_ATOL).all()
+    assert torch.isfinite(out.float()).all()
+
+
 @pytest.mark.parametrize("D", [128, 256])
 def test_prefill_full_size_sampled(D):
     """The ragged prefill workload at full size (as bench.py times it, head_dim 128 and
