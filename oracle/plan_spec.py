@@ -29,7 +29,12 @@ a design choice of this library, stated here:
    as the first wave ends, so each is cut into ``k = S // R`` chunks of
    ``c_b = max(ceil(np_b / k), min(c_min, np_b))`` pages (``n_chunks_b =
    ceil(np_b / c_b)``) when ``k > 1``, so that they run as one short round on
-   all SMs.  Requests are visited longest first
+   all SMs.  With the tensor-core kernel and one 16-row tile per request
+   (``group * max L <= 16``), every request longer than 3/5 of the average
+   load of a resident slot, ``A = Hkv * sum_b np_b / S`` pages (in integers:
+   ``np_b * 5S > 3 Hkv sum np``), is also cut into ``p_b = ceil(5 S np_b /
+   (3 Hkv sum np))`` parts: ``c_b = min(c_b, max(ceil(np_b / p_b), min(c_min,
+   np_b)))``.  Requests are visited longest first
    (``np_b`` descending, ties by ``b`` ascending); for each, chunks in order,
    and for each chunk every KV head: one work item
    ``(b, kv_head, chunk, page_lo, page_hi)``.
@@ -87,10 +92,17 @@ def plan_spec(seq_lens_kv, q_lens, num_qo_heads, num_kv_heads, head_dim, page_si
                 tail.append(b)
         rest = num_kv_heads * sum(tiles[b] for b in tail)
         k = slots // rest if rest else 1
+        c_min = _ceil_div(min_chunk_tokens, page_size)
         if k > 1:
-            c_min = _ceil_div(min_chunk_tokens, page_size)
             for b in tail:
                 cb[b] = max(_ceil_div(npages[b], k), min(c_min, npages[b]))
+        if mma and rows <= 16:   # one tile per request: cut past 3/5 of a slot's load
+            load = num_kv_heads * sum(npages)
+            for b in range(B):
+                num, den = npages[b] * 5 * slots, 3 * load
+                if num > den:
+                    parts = _ceil_div(num, den)
+                    cb[b] = min(cb[b], max(_ceil_div(npages[b], parts), min(c_min, npages[b])))
     n_chunks = [_ceil_div(x, c) for x, c in zip(npages, cb)]
     items = []
     for b in order:

@@ -15,6 +15,12 @@
 //     ends, so they are cut into k = S / R chunks (R = their CTAs) of
 //     max(ceil(np / k), min(c_min, np)) pages when k > 1: one short round on
 //     every SM instead of a long one on a few;
+//   - and, for the mma kernel with one 16-row tile per request, a request
+//     longer than 3/5 of a resident slot's average load (A = Hkv * sum np / S
+//     pages) is cut into ceil(np / (3A/5)) chunks of at least min(c_min, np)
+//     pages: its warps stream at a latency-bound rate, so long CTAs would
+//     finish last (measured on GB300; requests of several tiles, and the
+//     CUDA-core kernel, run best uncut);
 //   - items run longest request first, then chunk, then KV head.
 #include <algorithm>
 #include <climits>
@@ -209,9 +215,22 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
       }
     }
     const int64_t k = rest ? slots / rest : 1;
-    if (k > 1) {
-      const int64_t c_min = ceil_div(d.min_chunk_tokens, ps);
+    const int64_t c_min = ceil_div(d.min_chunk_tokens, ps);
+    if (k > 1)
       for (int32_t b : tail) cb[b] = std::max(ceil_div(npages[b], k), std::min(c_min, npages[b]));
+    // tensor-core kernel, one 16-row tile per request: a request longer than
+    // 3/5 of a resident slot's average load A = Hkv * sum np / S is cut into
+    // ceil(np / (3A/5)) chunks (integer form: np * 5S > 3 * Hkv * sum np)
+    if (p.kernel == PKA_KERNEL_MMA && p.rows_per_cta <= 16) {
+      int64_t load = 0;
+      for (int32_t b = 0; b < B; ++b) load += (int64_t)Hkv * npages[b];
+      for (int32_t b = 0; b < B; ++b) {
+        const int64_t num = npages[b] * 5 * slots, den = 3 * load;
+        if (num > den) {
+          const int64_t parts = ceil_div(num, den);
+          cb[b] = std::min(cb[b], std::max(ceil_div(npages[b], parts), std::min(c_min, npages[b])));
+        }
+      }
     }
   }
 

@@ -43,6 +43,15 @@ def _cases():
         if wide.random() < 0.5:
             cases[-1]["Hkv"] = 2
             cases[-1]["Hq"] = G * 2
+    one_tile = random.Random(31)
+    for G, mmr, mct in [(8, 8, 256), (4, 4, 256), (8, 8, 4096), (16, 8, 256)]:
+        # the tensor-core kernel with one 16-row tile per request, whole requests by
+        # the CTA target: long requests are cut to a share of a resident slot's load
+        B = 64
+        kv = [one_tile.randint(512, 8192) for _ in range(B)]
+        cases.append(dict(kv=kv, ql=[1] * B, packed=False, Hq=G * 8, Hkv=8, ps=16, W=-1,
+                          sms=152, waves=2, mct=mct, frozen=True, causal=False,
+                          mma_min_rows=mmr))
     return cases
 
 

@@ -141,3 +141,23 @@ def test_plan_skewed_long_request_is_split():
     p = plan_spec(kv, [1] * 16, 64, 8, 128, 32, -1, 152, 2, 256)
     assert p["n_chunks"][0] > 1 and p["order"][0] == 0
     assert len(p["items"]) <= 2 * 152
+
+
+def test_plan_single_tile_requests_are_cut_to_a_share_of_the_slot_load():
+    """Tensor-core kernel, one 16-row tile per request, whole requests by the CTA target
+    (64 x 8 CTAs >= 2 x 152): every chunk holds at most 3/5 of a resident slot's average
+    load (A = Hkv * sum np / (3 * 152) pages), rounded up to whole parts, and a request
+    of several tiles (q_len 3) is left whole by this rule."""
+    kv = [512 + 120 * b for b in range(64)]
+    p = plan_spec(kv, [1] * 64, 64, 8, 128, 16, -1, 152, 2, 256)
+    npg = [math.ceil(x / 16) for x in kv]
+    A = 8 * sum(npg) / (3 * 152)
+    long = [b for b, n in enumerate(npg) if n > 0.6 * A]
+    assert long
+    for b in long:
+        parts = math.ceil(npg[b] / (0.6 * A))
+        assert p["n_chunks"][b] == parts and parts >= 2
+    assert max(hi - lo for (_, _, _, lo, hi) in p["items"]) <= math.ceil(0.6 * A)
+    # (the shortest requests are cut by the tail rule, which this rule leaves alone)
+    p3 = plan_spec(kv, [3] * 64, 64, 8, 128, 16, -1, 152, 2, 256)   # 24 rows: 2 tiles
+    assert all(p3["n_chunks"][b] == 1 for b in long)
