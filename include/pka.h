@@ -140,8 +140,10 @@ const char* pka_version(void);
  * min_chunk_tokens   smallest split chunk in tokens; 0 = PKA_MIN_CHUNK_TOKENS,
  *                    else 256.
  * mma_min_rows       the tensor-core kernel is used when
- *                    (Hq/Hkv) * max_q_len >= mma_min_rows; 0 = PKA_MMA_MIN_ROWS,
- *                    else 8 (4 for PKA_DTYPE_F16 inputs).
+ *                    (Hq/Hkv) * max_q_len >= mma_min_rows (or > 8, the rows
+ *                    the CUDA-core kernel holds); 0 = PKA_MMA_MIN_ROWS, else 1
+ *                    (the tensor-core kernel always; a higher value keeps
+ *                    narrower groups on the CUDA-core kernel).
  *                    paged_decode_plan_info reports the values used.
  * flags              PKA_PLAN_HOST_ONLY or 0.
  * out_dtype          PKA_DTYPE_BF16, PKA_DTYPE_F16 or PKA_DTYPE_F32: O of

@@ -53,7 +53,7 @@ def _ceil_div(a, b):
 
 def plan_spec(seq_lens_kv, q_lens, num_qo_heads, num_kv_heads, head_dim, page_size,
               window_left, num_sms, waves, min_chunk_tokens, freeze_seq_lens=True,
-              mma_min_rows=8):
+              mma_min_rows=1):
     """Return the plan as a dict of plain Python lists and ints (see module docstring)."""
     B = len(seq_lens_kv)
     page_lo, page_hi, npages = [], [], []

@@ -36,11 +36,13 @@ namespace pka {
 namespace {
 constexpr int32_t kDefaultWaves = 2;
 constexpr int32_t kDefaultMinChunkTokens = 256;
-// rows per KV head from which the mma.sync kernel runs: measured on GB300, it
-// overtakes the CUDA-core kernel at 8 rows for bf16 and already at 4 for half,
-// whose conversions to fp32 the CUDA-core kernel pays and the tensor cores do not
-constexpr int32_t kDefaultMmaMinRows = 8;
-constexpr int32_t kDefaultMmaMinRowsF16 = 4;
+// rows per KV head from which the mma.sync kernel runs: measured on GB300
+// (B = 64, kv_len U[512, 8192]), with the plan's cut of long single-tile
+// requests it beats the CUDA-core kernel at 1, 2 and 4 rows per KV head, bf16
+// and half alike (1.105 / 1.069 / 1.005 of the copy peak against 1.075 / 1.015
+// / 0.95), so it runs by default; the CUDA-core kernel is kept for a threshold
+// set higher
+constexpr int32_t kDefaultMmaMinRows = 1;
 constexpr int32_t kMaxCudaCoreRows = 8;   // rows one warp of the CUDA-core kernel holds
 // query rows per KV head the tensor-core kernel takes: one CTA per 16-row
 // tile of every item (4096 tiles); the pages put no bound on the group or on
@@ -89,9 +91,7 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
   if (d.split_waves <= 0) d.split_waves = env_int("PKA_SPLIT_WAVES", kDefaultWaves);
   if (d.min_chunk_tokens <= 0)
     d.min_chunk_tokens = env_int("PKA_MIN_CHUNK_TOKENS", kDefaultMinChunkTokens);
-  if (d.mma_min_rows <= 0)
-    d.mma_min_rows = env_int("PKA_MMA_MIN_ROWS", d.dtype == PKA_DTYPE_F16 ? kDefaultMmaMinRowsF16
-                                                                          : kDefaultMmaMinRows);
+  if (d.mma_min_rows <= 0) d.mma_min_rows = env_int("PKA_MMA_MIN_ROWS", kDefaultMmaMinRows);
   if (d.num_sms <= 0) {
     int dev = 0, sms = 0;
     PKA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");

@@ -6,7 +6,7 @@
  * <out dir> as raw little-endian arrays, for tests/test_c_abi_gpu.py to
  * compare with the fp64 oracle.
  *
- * usage: decode_step <out dir> <num_qo_heads>
+ * usage: decode_step <out dir> <num_qo_heads> [mma_min_rows]
  *   3 requests of 37, 100 and 300 keys, 2 KV heads, head_dim 128, 16-token
  *   pages drawn from a pool of 48 in a random order, one query row each, LSE.
  */
@@ -66,8 +66,8 @@ static int save(const char* dir, const char* name, const void* p, size_t n) {
 }
 
 int main(int argc, char** argv) {
-  if (argc != 3) {
-    fprintf(stderr, "usage: %s <out dir> <num_qo_heads>\n", argv[0]);
+  if (argc != 3 && argc != 4) {
+    fprintf(stderr, "usage: %s <out dir> <num_qo_heads> [mma_min_rows]\n", argv[0]);
     return 2;
   }
   const char* dir = argv[1];
@@ -131,6 +131,7 @@ int main(int argc, char** argv) {
   d.return_lse = 1;
   d.freeze_seq_lens = 1;
   d.out_dtype = PKA_DTYPE_BF16;
+  d.mma_min_rows = argc == 4 ? atoi(argv[3]) : 0;   /* 0: the library's default */
 
   pka_plan* plan = NULL;
   size_t ws_bytes = 0;

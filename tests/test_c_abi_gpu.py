@@ -33,12 +33,14 @@ def _build(tmp_path):
     return exe
 
 
-@pytest.mark.parametrize("hq,kernel", [(8, 0), (16, 1)])
-def test_decode_step_from_c(tmp_path, hq, kernel):
-    """Group 4 (CUDA-core kernel) and group 8 (tensor-core kernel); 3 requests on a
-    GB300 are split into chunks, so the in-kernel merge runs too."""
+@pytest.mark.parametrize("hq,mma_min_rows,kernel", [(8, 16, 0), (8, 0, 1), (16, 0, 1)])
+def test_decode_step_from_c(tmp_path, hq, mma_min_rows, kernel):
+    """Groups of 4 and 8 rows on the tensor-core kernel (the default) and 4 rows on the
+    CUDA-core one (mma_min_rows 16); 3 requests on a GB300 are split into chunks, so the
+    in-kernel merge runs too."""
     exe = _build(tmp_path)
-    r = subprocess.run([exe, str(tmp_path), str(hq)], capture_output=True, text=True, timeout=120)
+    r = subprocess.run([exe, str(tmp_path), str(hq), str(mma_min_rows)], capture_output=True,
+                       text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     meta = dict(kv.split("=") for kv in r.stdout.split())
     B, Hkv, D, ps, C, P = (int(meta[x]) for x in ("B", "Hkv", "D", "ps", "C", "P"))

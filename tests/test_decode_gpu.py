@@ -26,28 +26,39 @@ SMALL = {
 }
 
 
-@pytest.mark.parametrize("name", list(SMALL))
+# decode kernel of a test case: the default (the tensor-core kernel), or the CUDA-core one
+# (kept for groups of up to 8 rows per KV head when mma_min_rows is set above them)
+KERNELS = {"default": {}, "cuda_core": dict(mma_min_rows=16)}
+
+
+@pytest.mark.parametrize("name,kernel", [(n, k) for n in SMALL for k in KERNELS
+                                         if not (n == "spec" and k == "cuda_core")])
 @pytest.mark.parametrize("seed", [0, 1])
-def test_decode_matches_oracle(name, seed):
+def test_decode_matches_oracle(name, seed, kernel):
     inp = wl.make_decode_inputs(SMALL[name], seed=seed, device=DEV)
-    out, lse, plan = run_decode(inp)
+    out, lse, plan = run_decode(inp, **KERNELS[kernel])
+    assert plan.info["kernel"] == (0 if kernel == "cuda_core" else 1)
     ref_o, ref_l = oracle_decode(inp)
     assert_close(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("name", ["llama3_8b", "skewed"])
-def test_decode_split_kv_path(name):
+def test_decode_split_kv_path(name, kernel):
     """Few SMs in the plan force a split of the long requests: partials merged in the run."""
     inp = wl.make_decode_inputs(SMALL[name], seed=3, device=DEV)
-    out, lse, plan = run_decode(inp, num_sms=32, split_waves=2, min_chunk_tokens=128)
+    out, lse, plan = run_decode(inp, num_sms=32, split_waves=2, min_chunk_tokens=128,
+                                **KERNELS[kernel])
     assert plan.info["num_split"] > 0
     ref_o, ref_l = oracle_decode(inp)
     assert_close(out, lse, ref_o, ref_l)
 
 
-@pytest.mark.parametrize("name,sms", [("spec", 148), ("skewed", 148), ("skewed", 48),
-                                      ("llama3_8b", 64), ("llama3_8b", 1024)])
-def test_decode_split_merge_by_the_last_chunk(name, sms):
+@pytest.mark.parametrize("name,sms,kernel", [
+    ("spec", 148, "default"), ("skewed", 148, "default"), ("skewed", 48, "default"),
+    ("llama3_8b", 64, "default"), ("llama3_8b", 64, "cuda_core"),
+    ("llama3_8b", 1024, "cuda_core")])
+def test_decode_split_merge_by_the_last_chunk(name, sms, kernel):
     """Split partials are merged inside the decode kernels: the chunk CTA of a (request,
     KV head, tile) group that counts last combines the group's rows (spec: <= 3 chunks
     over packed causal rows, three tiles; skewed: 19 chunks, merged with 16 threads per
@@ -56,7 +67,8 @@ def test_decode_split_merge_by_the_last_chunk(name, sms):
     each group's last CTA) serve the second."""
     inp = wl.make_decode_inputs(SMALL[name], seed=5, device=DEV)
     from helpers import decode_plan_for
-    plan = decode_plan_for(inp, num_sms=sms, split_waves=2, min_chunk_tokens=128)
+    plan = decode_plan_for(inp, num_sms=sms, split_waves=2, min_chunk_tokens=128,
+                           **KERNELS[kernel])
     ex = plan.export()
     assert max(ex["n_chunks"]) > 1
     ref_o, ref_l = oracle_decode(inp)
@@ -65,31 +77,36 @@ def test_decode_split_merge_by_the_last_chunk(name, sms):
         assert_close(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("name", ["tiny", "llama3_8b", "skewed"])
-def test_decode_tensor_core_kernel_on_narrow_groups(name):
-    """The mma kernel also runs 4- and 8-row groups (rows padded to 16)."""
+def test_decode_both_kernels_on_narrow_groups(name, kernel):
+    """4- and 8-row groups on either kernel (the tensor-core one pads the rows to 16)."""
     inp = wl.make_decode_inputs(SMALL[name], seed=4, device=DEV)
-    out, lse, plan = run_decode(inp, mma_min_rows=1)
-    assert plan.info["kernel"] == 1
+    out, lse, plan = run_decode(inp, **KERNELS[kernel])
+    assert plan.info["kernel"] == (0 if kernel == "cuda_core" else 1)
     ref_o, ref_l = oracle_decode(inp)
     assert_close(out, lse, ref_o, ref_l)
 
 
-@pytest.mark.parametrize("G,L,causal,W,sinks", [
-    (4, 2, True, -1, False),     # 8 rows, CUDA-core kernel, causal multi-token
-    (2, 3, False, 40, True),     # dense mask with a window, sinks
-    (1, 1, False, 0, True),      # window 0: only the diagonal key
-    (8, 8, True, 100, True),     # 64 rows, four m16 tiles
-    (4, 8, True, 33, True),      # 32 rows, two m16 tiles
-    (8, 3, False, -1, False),    # 24 rows, dense mask
-    (4, 3, True, 17, False),     # 12 rows: mma kernel
+@pytest.mark.parametrize("G,L,causal,W,sinks,kernel", [
+    (4, 2, True, -1, False, "cuda_core"),   # 8 rows, causal multi-token
+    (4, 2, True, -1, False, "default"),
+    (2, 3, False, 40, True, "cuda_core"),   # dense mask with a window, sinks
+    (2, 3, False, 40, True, "default"),
+    (1, 1, False, 0, True, "cuda_core"),    # window 0: only the diagonal key
+    (1, 1, False, 0, True, "default"),
+    (8, 8, True, 100, True, "default"),     # 64 rows, four m16 tiles
+    (4, 8, True, 33, True, "default"),      # 32 rows, two m16 tiles
+    (8, 3, False, -1, False, "default"),    # 24 rows, dense mask
+    (4, 3, True, 17, False, "cuda_core"),   # 12 rows: the tensor-core kernel whatever is asked
 ])
-def test_decode_masks_and_groups(G, L, causal, W, sinks):
+def test_decode_masks_and_groups(G, L, causal, W, sinks, kernel):
     w = wl.DecodeWorkload(name="masks", batch=5, num_qo_heads=2 * G, num_kv_heads=2,
                           head_dim=128, page_size=16, kv_len_range=(L, 700), q_len_range=(L, L),
                           causal=causal, window_left=W, sinks=sinks)
     inp = wl.make_decode_inputs(w, seed=5, device=DEV)
-    out, lse, plan = run_decode(inp)
+    out, lse, plan = run_decode(inp, **KERNELS[kernel])
+    assert plan.info["kernel"] == (0 if kernel == "cuda_core" and G * L <= 8 else 1)
     ref_o, ref_l = oracle_decode(inp)
     assert_close(out, lse, ref_o, ref_l)
 
@@ -142,11 +159,13 @@ def test_decode_more_than_64_rows_per_kv_head(Hq, Hkv, L, packed, split):
 @pytest.mark.parametrize("in_dtype,out_dtype", [
     (torch.float16, None), (torch.float16, torch.float32), (torch.bfloat16, torch.float32),
     (torch.bfloat16, torch.float16)])
-@pytest.mark.parametrize("name,mma", [("llama3_8b", 0), ("spec", 0), ("skewed", 16)])
+@pytest.mark.parametrize("name,mma", [("llama3_8b", 16), ("llama3_8b", 0), ("spec", 0),
+                                      ("skewed", 16)])
 def test_decode_input_and_output_dtypes(in_dtype, out_dtype, name, mma):
     """fp16 q/K/V (cudnn_batch_decode_with_kv_cache takes float16 or bfloat16) and
     out_dtype bf16 / f16 / fp32 (batch_decode_with_paged_kv_cache, out_dtype), on the
-    CUDA-core kernel (4 and 8 rows), the mma kernel and the split + merge path."""
+    CUDA-core kernel (4 and 8 rows: mma_min_rows 16), the tensor-core kernel (the
+    default) and the split + merge path."""
     inp = wl.make_decode_inputs(SMALL[name], seed=14, device=DEV, dtype=in_dtype)
     kw = dict(out_dtype=out_dtype, num_sms=32, split_waves=2, min_chunk_tokens=128)
     if mma:
@@ -220,26 +239,29 @@ def test_decode_plan_update_reuses_and_grows():
         assert_close(out, lse, ref_o, ref_l)
 
 
-@pytest.mark.parametrize("G,ps", [(4, 256), (8, 256), (16, 128)])
-def test_decode_largest_page_sizes(G, ps):
+@pytest.mark.parametrize("G,ps,kernel", [(4, 256, "cuda_core"), (4, 256, "default"),
+                                         (8, 256, "default"), (16, 128, "default")])
+def test_decode_largest_page_sizes(G, ps, kernel):
     """page_size up to 256 (16 TMA units per page), GQA group 4, 8 and 16 rows."""
     w = wl.DecodeWorkload(name="bigpage", batch=3, num_qo_heads=2 * G, num_kv_heads=2,
                           head_dim=128, page_size=ps, kv_len_range=(1, 2000), causal=True)
     inp = wl.make_decode_inputs(w, seed=18, device=DEV)
-    out, lse, _ = run_decode(inp)
+    out, lse, _ = run_decode(inp, **KERNELS[kernel])
     ref_o, ref_l = oracle_decode(inp)
     assert_close(out, lse, ref_o, ref_l)
 
 
-@pytest.mark.parametrize("G,ps", [(4, 48), (8, 80), (2, 208)])
-def test_decode_page_sizes_not_powers_of_two(G, ps):
+@pytest.mark.parametrize("G,ps,kernel", [(4, 48, "cuda_core"), (4, 48, "default"),
+                                         (8, 80, "default"), (2, 208, "cuda_core"),
+                                         (2, 208, "default")])
+def test_decode_page_sizes_not_powers_of_two(G, ps, kernel):
     """Any multiple of 16 is a page size: 3, 5 and 13 TMA units per page, with split
     requests whose chunks end inside the unit runs of such pages."""
     w = wl.DecodeWorkload(name="oddpage", batch=3, num_qo_heads=2 * G, num_kv_heads=2,
                           head_dim=128, page_size=ps, kv_len_range=(1, 2000), causal=True,
                           sinks=True)
     inp = wl.make_decode_inputs(w, seed=20 + ps, device=DEV)
-    out, lse, plan = run_decode(inp)
+    out, lse, plan = run_decode(inp, **KERNELS[kernel])
     assert plan.info["num_split"] > 0
     ref_o, ref_l = oracle_decode(inp)
     assert_close(out, lse, ref_o, ref_l)
@@ -295,11 +317,12 @@ def test_decode_graph_capture_replays_eagerly_equal():
 # requests (longest, shortest, a middle one) against the oracle.
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["llama3_8b", "skewed", "spec"])
-def test_decode_full_size_sampled(name):
+@pytest.mark.parametrize("name,kernel", [("llama3_8b", "default"), ("llama3_8b", "cuda_core"),
+                                         ("skewed", "default"), ("spec", "default")])
+def test_decode_full_size_sampled(name, kernel):
     w = wl.DECODE_WORKLOADS[name]
     inp = wl.make_decode_inputs(w, seed=0, device=DEV)
-    out, lse, plan = run_decode(inp, return_lse=True)
+    out, lse, plan = run_decode(inp, return_lse=True, **KERNELS[kernel])
     seq = inp["seq_lens_kv"].cpu().numpy()
     order = np.argsort(-seq, kind="stable")
     reqs = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2])})

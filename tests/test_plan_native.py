@@ -93,15 +93,15 @@ def test_kernel_choice_follows_rows_per_kv_head():
                                   max_pages_per_seq=8, num_pages=100, q_len=L, num_sms=8,
                                   mma_min_rows=mma_min_rows, host_only=True, dtype=dtype)
         return p.info["kernel"], p.info["rows_per_cta"]
-    assert kernel(4, 1) == (0, 4)
-    assert kernel(8, 1) == (1, 8)       # default threshold: 8 rows per KV head
+    assert kernel(1, 1) == (1, 1)       # default threshold 1 row: the tensor-core kernel
+    assert kernel(4, 1) == (1, 4)
+    assert kernel(2, 1, dtype=torch.float16) == (1, 2)
     assert kernel(8, 1, mma_min_rows=16) == (0, 8)
     assert kernel(8, 2) == (1, 16)
     assert kernel(4, 3, mma_min_rows=16) == (1, 12)   # 9..15 rows exceed one CUDA-core warp
     assert kernel(4, 1, mma_min_rows=4) == (1, 4)
-    assert kernel(4, 1, dtype=torch.float16) == (1, 4)   # half: default threshold 4 rows
-    assert kernel(2, 1, dtype=torch.float16) == (0, 2)
-    assert kernel(4, 1, mma_min_rows=8, dtype=torch.float16) == (0, 4)
+    assert kernel(4, 1, mma_min_rows=8) == (0, 4)
+    assert kernel(2, 1, mma_min_rows=4, dtype=torch.float16) == (0, 2)
 
 
 def test_plan_update_equals_a_fresh_plan():
@@ -132,17 +132,17 @@ def test_planner_tunables_from_the_environment(monkeypatch):
               num_pages=1000, q_len=1, num_sms=8, host_only=True)
     monkeypatch.setenv("PKA_SPLIT_WAVES", "5")
     monkeypatch.setenv("PKA_MIN_CHUNK_TOKENS", "512")
-    monkeypatch.setenv("PKA_MMA_MIN_ROWS", "4")
+    monkeypatch.setenv("PKA_MMA_MIN_ROWS", "8")
     info = api.paged_decode_plan(seq, **kw).info
     assert (info["split_waves"], info["min_chunk_tokens"]) == (5, 512)
-    assert info["kernel"] == 1                      # group of 4 rows >= 4: tensor-core kernel
+    assert info["kernel"] == 0                      # group of 4 rows < 8: CUDA-core kernel
     info = api.paged_decode_plan(seq, split_waves=3, **kw).info
     assert info["split_waves"] == 3
     monkeypatch.setenv("PKA_SPLIT_WAVES", "abc")
     monkeypatch.setenv("PKA_MIN_CHUNK_TOKENS", "0")
     monkeypatch.delenv("PKA_MMA_MIN_ROWS")
     info = api.paged_decode_plan(seq, **kw).info
-    assert (info["split_waves"], info["min_chunk_tokens"], info["kernel"]) == (2, 256, 0)
+    assert (info["split_waves"], info["min_chunk_tokens"], info["kernel"]) == (2, 256, 1)
 
 
 def test_an_empty_batch_is_rejected_by_name():

@@ -187,10 +187,13 @@ def _chunk_lse_spread(inp, plan):
     return spread
 
 
-@pytest.mark.parametrize("name", list(DECODE_CASES))
-def test_decode_split_partials_far_apart(name):
+@pytest.mark.parametrize("name,mma_min_rows", [(n, 0) for n in DECODE_CASES] +
+                         [("llama3_8b", 16)])   # the last: the CUDA-core kernel
+def test_decode_split_partials_far_apart(name, mma_min_rows):
     inp = wl.make_climbing_decode_inputs(DECODE_CASES[name], seed=130, device="cuda", slope=1.0)
-    plan = decode_plan_for(inp, num_sms=64, split_waves=2, min_chunk_tokens=128)
+    plan = decode_plan_for(inp, num_sms=64, split_waves=2, min_chunk_tokens=128,
+                           mma_min_rows=mma_min_rows)
+    assert plan.info["kernel"] == (0 if mma_min_rows == 16 else 1)
     assert plan.info["num_split"] > 0
     spread = _chunk_lse_spread(inp, plan)
     assert spread > 20.0, spread
