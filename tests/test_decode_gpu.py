@@ -62,9 +62,9 @@ def test_decode_split_merge_by_the_last_chunk(name, sms, kernel):
     """Split partials are merged inside the decode kernels: the chunk CTA of a (request,
     KV head, tile) group that counts last combines the group's rows (spec: <= 3 chunks
     over packed causal rows, three tiles; skewed: 19 chunks, merged with 16 threads per
-    row, or 6, with 8; llama3_8b: the CUDA-core kernel, with up to 17 chunks at a planned
-    1024 SMs).  Run twice, so that the counters left by the first run (reset to zero by
-    each group's last CTA) serve the second."""
+    row, or 6, with 8; llama3_8b: both kernels, and the CUDA-core one with up to 17 chunks
+    at a planned 1024 SMs).  Run twice, so that the counters left by the first run (reset to
+    zero by each group's last CTA) serve the second."""
     inp = wl.make_decode_inputs(SMALL[name], seed=5, device=DEV)
     from helpers import decode_plan_for
     plan = decode_plan_for(inp, num_sms=sms, split_waves=2, min_chunk_tokens=128,

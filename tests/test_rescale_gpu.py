@@ -138,7 +138,7 @@ def test_prefill_lazy_rescale_variable_window():
 # --------------------------------------------------------------------------
 
 DECODE_CASES = {
-    # CUDA-core kernel (4 rows per KV head)
+    # 4 rows per KV head (the tensor-core kernel by default; the CUDA-core one below)
     "llama3_8b": wl.shrink(wl.LLAMA3_8B_DECODE, batch=4, kv_len_range=(1500, 2100),
                            pool_pages=700, table_width=160, return_lse=True),
     # tensor-core kernel (8 rows), one long request

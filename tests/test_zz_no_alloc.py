@@ -75,10 +75,12 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
     assert b"16777216" in L.lib().pka_last_error()
 
 
-@pytest.mark.parametrize("name", ["llama3_8b", "spec"])
-def test_noalloc_matches_the_oracle(name):
-    """Frozen lengths (llama3_8b shape: CUDA-core kernel, split) and live lengths shorter
-    than planned (spec shape: tensor-core kernel, causal rows, window, sinks)."""
+@pytest.mark.parametrize("name,mma_min_rows", [("llama3_8b", 0), ("llama3_8b", 16),
+                                               ("spec", 0)])
+def test_noalloc_matches_the_oracle(name, mma_min_rows):
+    """Frozen lengths (llama3_8b shape, split; the tensor-core kernel, the default, and the
+    CUDA-core one) and live lengths shorter than planned (spec shape: causal rows, window,
+    sinks)."""
     w = {"llama3_8b": wl.shrink(wl.LLAMA3_8B_DECODE, batch=5, kv_len_range=(512, 2100),
                                 pool_pages=1000, table_width=160, return_lse=True),
          "spec": wl.shrink(wl.SPEC_DECODE, batch=5, kv_len_range=(600, 2600), window_left=700,
@@ -86,7 +88,9 @@ def test_noalloc_matches_the_oracle(name):
     inp = wl.make_decode_inputs(w, seed=21, device="cuda")
     frozen = name == "llama3_8b"
     plan = decode_plan_for(inp, num_sms=32 if frozen else 128, split_waves=2,
-                           min_chunk_tokens=128, host_only=True, freeze_seq_lens=frozen)
+                           min_chunk_tokens=128, host_only=True, freeze_seq_lens=frozen,
+                           mma_min_rows=mma_min_rows)
+    assert plan.info["kernel"] == (0 if mma_min_rows == 16 else 1)
     assert plan.info["num_split"] > 0
     if not frozen:
         cut = torch.tensor([0, 7, 100, 333, 1], dtype=torch.int32, device="cuda")
