@@ -1,4 +1,6 @@
-// Paged decode attention, CUDA-core variant (FFMA2 + warp shuffles).
+// Paged decode attention, CUDA-core variant (FFMA2 + warp shuffles), for
+// groups of up to 8 query rows per KV head when the plan's mma_min_rows is set
+// above them (the tensor-core variant, decode_mma.cu, is the default).
 //
 // Computes, for every query row of one (request, KV head, key chunk) work
 // item, softmax(scale * q K^T) V over the keys the row may see

@@ -1,7 +1,7 @@
-// Paged decode attention, tensor-core variant for wide query groups
-// ((Hq/Hkv) * max_q_len >= 8 rows per KV head by default, 4 with half inputs:
-// e.g. 8 query heads per KV head, or speculative packed-Q verification with
-// cudnn_batch_decode_with_kv_cache's q_len_per_req rows).
+// Paged decode attention, tensor-core variant: the plan's default for every
+// query group, from one row per KV head (MHA) through GQA groups to
+// speculative packed-Q verification with cudnn_batch_decode_with_kv_cache's
+// q_len_per_req rows; narrow groups are padded to one 16-row tile.
 //
 // Same work items, masks, softmax and outputs as the CUDA-core kernel; the
 // two contractions run on mma.sync m16n8k16 (bf16 or f16 in, fp32 accumulate):
