@@ -332,6 +332,25 @@ def test_decode_full_size_sampled(name, kernel):
     assert torch.isfinite(out.float()).all()
 
 
+def test_decode_long_single_tile_requests_cut_by_slot_load():
+    """64 requests of U[512, 8192] keys with 8 query heads per KV head (one 16-row tile per
+    request): the CTA target leaves them whole, and the plan cuts those longer than 3/5 of a
+    resident slot's average load into chunks merged in the kernel.  Sampled requests (the
+    longest, the shortest, the middle) against the oracle."""
+    w = wl.DecodeWorkload(name="cut", batch=64, num_qo_heads=64, num_kv_heads=8, head_dim=128,
+                          page_size=16, kv_len_range=(512, 8192), pool_pages=40000,
+                          table_width=512, return_lse=True)
+    inp = wl.make_decode_inputs(w, seed=33, device=DEV)
+    out, lse, plan = run_decode(inp, num_sms=152)
+    assert plan.info["kernel"] == 1 and plan.info["num_split"] > 0
+    assert plan.info["num_items"] > 64 * 8
+    seq = inp["seq_lens_kv"].cpu().numpy()
+    order = np.argsort(-seq, kind="stable")
+    reqs = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2])})
+    ref_o, ref_l = oracle_decode(inp, requests=reqs)
+    assert_close(out, lse, ref_o, ref_l, rows=row_mask(inp, reqs))
+
+
 def test_decode_many_short_requests():
     """2048 requests of 1-64 keys (4096 CTAs, ragged single pages), sampled requests."""
     w = wl.shrink(wl.TINY_DECODE, batch=2048, kv_len_range=(1, 64), pool_pages=2048 * 4 + 64,
