@@ -392,9 +392,8 @@ def time_decode_e2e(inp, plan_kw, steps, warmup, in_place=True):
         kw["qo_indptr"] = t["qo_indptr_host"]
     plan = api.paged_decode_plan(t["seq_lens_kv_host"], stream=stream, **kw)   # re-planned per step
 
-    def step():
-        api.paged_decode_step_host(plan, io, inp["k_pages"], inp["v_pages"], sinks=inp["sinks"],
-                                   stream=stream)
+    step = api.DecodeStep(plan, io, inp["k_pages"], inp["v_pages"], sinks=inp["sinks"],
+                          stream=stream)
 
     for _ in range(warmup):
         step()

@@ -282,6 +282,65 @@ def paged_decode_step_host(plan, io, k_pages, v_pages, sinks=None, batch_size=No
     return (t["out_host"], t["lse_host"]) if plan.desc.return_lse else t["out_host"]
 
 
+class DecodeStep:
+    """``paged_decode_step_host`` prepared for a serving loop that repeats it on one
+    plan, io, pair of pools and stream: the binding's checks of the tensors run once
+    here, and each call is a single C-ABI call with its arguments already marshalled
+    (the library still checks them all on every call).  A call runs one step on the
+    current contents of the io's host arrays (lengths, offsets, q, tables) and returns
+    what ``paged_decode_step_host`` returns.  The io's packed offsets may change
+    between calls; their row count is checked against the io's q rows each time."""
+
+    def __init__(self, plan, io, k_pages, v_pages, sinks=None, batch_size=None,
+                 synchronize=True, stream=None):
+        t = io.tensors
+        _check_inputs(plan, t["q_host"], k_pages, v_pages)
+        _check_layout(t["q_dev"], k_pages, v_pages, t["out_dev"], t["lse_dev"], paged=True)
+        if t["out_dev"].dtype != _TORCH[plan.desc.out_dtype]:
+            raise ValueError(f"out must be {_TORCH[plan.desc.out_dtype]} (the plan's out_dtype)")
+        B = t["seq_lens_kv_host"].numel() if batch_size is None else int(batch_size)
+        if B < 1 or B > t["block_tables_host"].shape[0] or B > t["seq_lens_kv_host"].numel():
+            raise ValueError("batch_size must be >= 1 and within the io's table rows and lengths")
+        ind = t["qo_indptr_host"]
+        if ind is not None and ind.numel() < B + 1:
+            raise ValueError("qo_indptr_host holds fewer than batch_size + 1 offsets")
+        self.plan, self.io, self.batch_size = plan, io, B
+        self._keep = (k_pages, v_pages, sinks)
+        self._rows = t["q_host"].shape[0]
+        self._ind = None if ind is None else ctypes.cast(ind.data_ptr(), L._pi32)
+        if self._ind is None and B * plan.desc.q_len > self._rows:
+            raise ValueError(f"the batch has {B * plan.desc.q_len} query rows, the io holds "
+                             f"{self._rows}")
+        self._fn = L.lib().paged_decode_step_host
+        self._need = ctypes.c_size_t()
+        self._head = (plan.handle, B, ctypes.byref(io.c), _ptr(k_pages), _ptr(v_pages),
+                      k_pages.stride(0), k_pages.stride(1), _ptr(sinks))
+        self._tail = (ctypes.byref(self._need), int(bool(synchronize)), _stream(stream))
+        self._result = (t["out_host"], t["lse_host"]) if plan.desc.return_lse else t["out_host"]
+        self._bind_workspace()
+
+    def _bind_workspace(self):
+        ws = self.io.workspace
+        self._args = self._head + (_ptr(ws), 0 if ws is None else ws.numel()) + self._tail
+
+    def __call__(self):
+        if self._ind is not None and self._ind[self.batch_size] > self._rows:
+            raise ValueError(f"the batch has {self._ind[self.batch_size]} query rows, the io "
+                             f"holds {self._rows}")
+        rc = self._fn(*self._args)
+        if rc == L.PKA_ERR_WORKSPACE_TOO_SMALL:   # re-planned, not run: grow and step again
+            need = self._need.value
+            self.io.workspace = torch.empty(need + need // 4 + 256, dtype=torch.uint8,
+                                            device=self._keep[0].device)
+            self._bind_workspace()
+            rc = self._fn(*self._args)
+        if rc in (L.PKA_OK, L.PKA_ERR_WORKSPACE_TOO_SMALL):   # the plan was re-planned
+            self.plan.desc.batch_size = self.batch_size
+            self.plan.workspace_bytes = self._need.value
+        L.check(rc, "paged_decode_step_host")
+        return self._result
+
+
 def attn_merge_lse(v_states, s_states, out_dtype=torch.bfloat16, v_out=None, s_out=None,
                    stream=None):
     """Merge ``[N, S, H, D]`` fp32 states by their ``[N, S, H]`` base-2 LSEs."""

@@ -116,6 +116,42 @@ def test_step_host_equals_run_step_after_step(name, kw, in_place):
         assert split_seen and io.workspace is not None
 
 
+@pytest.mark.parametrize("in_place", [False, True])
+@pytest.mark.parametrize("name,kw", [
+    ("llama3_8b", {}),
+    ("spec", dict(freeze_seq_lens=False, num_sms=32, split_waves=2, min_chunk_tokens=128)),
+])
+def test_prepared_step_equals_run_step_after_step(name, kw, in_place):
+    """DecodeStep (the step call marshalled once, then repeated on new host contents):
+    each call re-plans on the step's lengths and returns the bytes paged_decode_run
+    returns on device copies of the same inputs; a packed batch whose rows outgrow the
+    io is refused before the call."""
+    w = LLAMA if name == "llama3_8b" else SPEC
+    inp = wl.make_decode_inputs(w, seed=25, device=DEV)
+    io = _make_io(inp, inp["q"].dtype, in_place)
+    plan = decode_plan_for(inp, **kw)
+    B = inp["seq_lens_kv"].numel()
+    step = api.DecodeStep(plan, io, inp["k_pages"], inp["v_pages"], sinks=inp["sinks"])
+    for k in range(3):
+        cur = inp if k == 0 else _next_step(inp, seed=200 + k, batch=B)
+        _, tq = _fill(io, cur)
+        out_h, lse_h = step()
+        plan.check()
+        ref_o, ref_l = _run_reference(cur, **kw)
+        assert torch.equal(out_h[:tq], ref_o), f"step {k}: O differs from paged_decode_run"
+        assert torch.equal(lse_h[:tq], ref_l), f"step {k}: LSE differs from paged_decode_run"
+    o_or, l_or = oracle_decode(cur)
+    assert_close(out_h[:tq], lse_h[:tq], o_or, l_or)
+    if kw:
+        assert io.workspace is not None and plan.info["num_split"] > 0
+        ind = io.tensors["qo_indptr_host"]
+        saved = int(ind[B])
+        ind[B] = io.tensors["q_host"].shape[0] + 1
+        with pytest.raises(ValueError):
+            step()
+        ind[B] = saved
+
+
 @pytest.mark.parametrize("in_dtype,out_dtype", [(torch.float16, torch.float32),
                                                (torch.bfloat16, torch.float16)])
 def test_step_host_input_and_output_types(in_dtype, out_dtype):
