@@ -264,8 +264,13 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
       const float mx = mraw == neg_inf() ? neg_inf() : mraw * sl2;
       const bool grow = mx > m_ref + kRescaleThreshold;
       const float m_new = grow ? mx : m_ref;
-      const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+      // A row that had no visible key yet holds O = 0 and l = 0 (its P was 0):
+      // it takes its first reference without a rescale, so that rows whose
+      // windows start at different key tiles do not stall the warp on the
+      // previous tile's P V one after another.
+      const bool rescale = grow && m_ref != neg_inf();
+      const float alpha = rescale ? ex2(m_ref - m_new) : 1.f;
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
         // O holds tiles before j: wait for P V of tile j - 1 before rescaling
         if (!(ok = warp_wait(bar(B_ODONE + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1),
                              a.status)))
