@@ -356,8 +356,8 @@ prefill_1h_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__
           const int pr = mt * kTileQ + warp * 32 + rr;
           const uint4 val =
               *reinterpret_cast<const uint4*>(wbuf + rr * kRowBytes + ((q ^ (rr & 7)) << 4));
+          const int tr = __shfl_sync(0xffffffffu, t, rr);   // row rr's query row (lane rr's t)
           if (pr < Lq) {
-            const int tr = gather_q ? __ldg(a.row_map + q0 + pr) : pr;
             *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) +
                                       ((int64_t)(q0 + tr) * a.num_qo_heads + h) * kRowBytes +
                                       q * 16) = val;
