@@ -197,27 +197,33 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
   // ---- longest request first; chunk length per request ----
   p.order.resize(B);
   std::iota(p.order.begin(), p.order.end(), 0);
-  std::stable_sort(p.order.begin(), p.order.end(),
-                   [&](int32_t a, int32_t b) { return npages[a] > npages[b]; });
+  // longest first, ties in request order (a stable order without the stable
+  // sort's buffer)
+  std::sort(p.order.begin(), p.order.end(), [&](int32_t a, int32_t b) {
+    return npages[a] > npages[b] || (npages[a] == npages[b] && a < b);
+  });
   std::vector<int64_t> cb(B, chunk);
   if (tiles_sum * Hkv >= target) {
     const int64_t slots = (int64_t)(p.kernel == PKA_KERNEL_MMA ? 3 : 2) * d.num_sms;
+    // the tail: order[first_tail ..], past the longest-first prefix that fits
     int64_t acc = 0, rest = 0;
-    bool in_tail = false;
-    std::vector<int32_t> tail;
-    for (int32_t b : p.order) {
-      if (!in_tail && acc + Hkv * tiles[b] <= slots) {
+    int32_t first_tail = B;
+    for (int32_t i = 0; i < B; ++i) {
+      const int32_t b = p.order[i];
+      if (first_tail == B && acc + Hkv * tiles[b] <= slots) {
         acc += Hkv * tiles[b];
       } else {
-        in_tail = true;
-        tail.push_back(b);
+        if (first_tail == B) first_tail = i;
         rest += Hkv * tiles[b];
       }
     }
     const int64_t k = rest ? slots / rest : 1;
     const int64_t c_min = ceil_div(d.min_chunk_tokens, ps);
     if (k > 1)
-      for (int32_t b : tail) cb[b] = std::max(ceil_div(npages[b], k), std::min(c_min, npages[b]));
+      for (int32_t i = first_tail; i < B; ++i) {
+        const int32_t b = p.order[i];
+        cb[b] = std::max(ceil_div(npages[b], k), std::min(c_min, npages[b]));
+      }
     // tensor-core kernel, one 16-row tile per request: a request longer than
     // 3/5 of a resident slot's average load A = Hkv * sum np / S is cut into
     // ceil(np / (3A/5)) chunks (integer form: np * 5S > 3 * Hkv * sum np)
@@ -243,13 +249,15 @@ int build_decode_plan(pka_plan& p, const pka_decode_desc& d_in, const int32_t* s
   for (int32_t b = 0; b < B; ++b)
     PKA_CHECK_ARG(nch[b] < 65536, "request %d needs %d chunks (limit 65535)", b, nch[b]);
   PKA_CHECK_ARG(Hkv < 65536, "num_kv_heads must be < 65536");
-  p.items.clear();
-  p.items.reserve((size_t)n_items);
+  p.items.resize((size_t)n_items);
+  WorkItem* item = p.items.data();
   for (int32_t b : p.order) {
-    for (int32_t ci = 0; ci < nch[b]; ++ci) {
-      const int32_t lo = p.page_lo[b] + (int32_t)(ci * cb[b]);
-      const int32_t hi = (int32_t)std::min<int64_t>(p.page_lo[b] + (ci + 1) * cb[b], p.page_hi[b]);
-      for (int32_t hk = 0; hk < Hkv; ++hk) p.items.push_back(WorkItem{b, (ci << 16) | hk, lo, hi});
+    const int64_t c = cb[b];
+    const int32_t lo0 = p.page_lo[b], hi0 = p.page_hi[b], n = nch[b];
+    for (int32_t ci = 0; ci < n; ++ci) {
+      const int32_t lo = lo0 + (int32_t)(ci * c);
+      const int32_t hi = (int32_t)std::min<int64_t>(lo0 + (ci + 1) * c, hi0);
+      for (int32_t hk = 0; hk < Hkv; ++hk) *item++ = WorkItem{b, (ci << 16) | hk, lo, hi};
     }
   }
 
