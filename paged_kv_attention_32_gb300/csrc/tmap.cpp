@@ -52,11 +52,10 @@ int encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t
   return PKA_OK;
 }
 
-int encode_kv_pool_map(CUtensorMap* map, const void* pool, int64_t num_pages, int32_t num_heads,
-                       int32_t page_size, int32_t head_dim, int64_t stride_page,
-                       int64_t stride_head) {
-  PKA_CHECK_ARG(stride_head > 0 && stride_page > 0, "K/V strides must be positive");
-  PKA_CHECK_ARG(head_dim == 128, "the K/V pool map takes head_dim 128 (got %d)", head_dim);
+namespace {
+int encode_pool_map_uncached(CUtensorMap* map, const void* pool, int64_t num_pages,
+                             int32_t num_heads, int32_t page_size, int32_t head_dim,
+                             int64_t stride_page, int64_t stride_head) {
   // The 128 columns are split as (d_lo 0..63, d_hi 0..1) and d_hi is placed
   // after the slot dimension: (d_lo, slot, d_hi, head, page).  A box of
   // {64, 16, 2, 1, 1} then lands in shared memory as the two 64-column halves
@@ -66,6 +65,51 @@ int encode_kv_pool_map(CUtensorMap* map, const void* pool, int64_t num_pages, in
                                (uint64_t)stride_page * 2};
   const uint32_t box[5] = {64, 16, 2, 1, 1};
   return encode_bf16_map(map, pool, 5, dims, strides, box);
+}
+
+// A pool map is a pure function of the pool's address, shape and strides, so
+// the maps of the last few pools a thread ran on are kept (a serving loop runs
+// the same K and V pools every step) and reused without the driver call.
+struct PoolMapKey {
+  const void* pool;
+  int64_t num_pages, stride_page, stride_head;
+  int32_t num_heads, page_size;
+  bool operator==(const PoolMapKey& o) const {
+    return pool == o.pool && num_pages == o.num_pages && stride_page == o.stride_page &&
+           stride_head == o.stride_head && num_heads == o.num_heads && page_size == o.page_size;
+  }
+};
+constexpr int kPoolMapCache = 4;
+struct PoolMapCache {
+  PoolMapKey key[kPoolMapCache] = {};
+  CUtensorMap map[kPoolMapCache];
+  bool used[kPoolMapCache] = {};
+  int next = 0;
+};
+thread_local PoolMapCache t_pool_maps;
+}  // namespace
+
+int encode_kv_pool_map(CUtensorMap* map, const void* pool, int64_t num_pages, int32_t num_heads,
+                       int32_t page_size, int32_t head_dim, int64_t stride_page,
+                       int64_t stride_head) {
+  PKA_CHECK_ARG(stride_head > 0 && stride_page > 0, "K/V strides must be positive");
+  PKA_CHECK_ARG(head_dim == 128, "the K/V pool map takes head_dim 128 (got %d)", head_dim);
+  const PoolMapKey key{pool, num_pages, stride_page, stride_head, num_heads, page_size};
+  PoolMapCache& c = t_pool_maps;
+  for (int i = 0; i < kPoolMapCache; ++i)
+    if (c.used[i] && c.key[i] == key) {
+      *map = c.map[i];
+      return PKA_OK;
+    }
+  const int rc = encode_pool_map_uncached(map, pool, num_pages, num_heads, page_size, head_dim,
+                                          stride_page, stride_head);
+  if (rc == PKA_OK) {
+    c.key[c.next] = key;
+    c.map[c.next] = *map;
+    c.used[c.next] = true;
+    c.next = (c.next + 1) % kPoolMapCache;
+  }
+  return rc;
 }
 
 }  // namespace pka
