@@ -288,8 +288,10 @@ class DecodeStep:
     here, and each call is a single C-ABI call with its arguments already marshalled
     (the library still checks them all on every call).  A call runs one step on the
     current contents of the io's host arrays (lengths, offsets, q, tables) and returns
-    what ``paged_decode_step_host`` returns.  The io's packed offsets may change
-    between calls; their row count is checked against the io's q rows each time."""
+    what ``paged_decode_step_host`` returns.  The batch size is fixed here (a batch of
+    another size needs another DecodeStep); the lengths and the io's packed offsets may
+    change between calls, and the offsets' row count is checked against the io's q rows
+    each time."""
 
     def __init__(self, plan, io, k_pages, v_pages, sinks=None, batch_size=None,
                  synchronize=True, stream=None):
