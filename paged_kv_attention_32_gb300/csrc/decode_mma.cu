@@ -1,7 +1,7 @@
 // Paged decode attention, tensor-core variant: the plan's default for every
 // query group, from one row per KV head (MHA) through GQA groups to
 // speculative packed-Q verification with cudnn_batch_decode_with_kv_cache's
-// q_len_per_req rows; narrow groups are padded to one 16-row tile.
+// q_len_per_req rows.
 //
 // Same work items, masks, softmax and outputs as the CUDA-core kernel; the
 // two contractions run on mma.sync m16n8k16 (bf16 or f16 in, fp32 accumulate):
@@ -17,11 +17,17 @@
 //  * per unit: S = Q K^T (2 n-tiles x 8 k-steps, Q in A-fragment registers),
 //    mask, online softmax in base 2 on the fragments, P re-packed to 16-bit
 //    A fragments in registers, O += P V (16 n-tiles, V via ldmatrix.trans);
+//    a group of at most 8 rows (NARROW) takes the transposed step instead,
+//    S^T = K Q^T and O^T += V^T P^T, with the 16 keys of a unit on the
+//    16-row side of the instruction and the rows on its 8-column side: half
+//    the mma of a padded 16-row tile;
 //  * the four warps' (m, l, O) are merged through shared memory and the CTA
 //    writes final O/LSE (sink added), or, for a split request, an fp32 partial;
 //    the last chunk CTA of each (request, KV head, tile) merges the partials.
 // Decode is bound by HBM, not by the tensor pipe: mma takes the per-key
 // arithmetic of wide groups off the FP32 pipe.
+#include <type_traits>
+
 #include <cuda_bf16.h>
 
 #include "decode_merge.cuh"
@@ -41,7 +47,7 @@ constexpr int kUnit = kMmaUnitTok;
 constexpr int kStageBytes = kMmaUnitBytes;
 constexpr int kBoxBytes = kMmaBoxBytes;
 
-template <int NSTAGE, bool F16>
+template <int NSTAGE, bool F16, bool NARROW>
 __global__ void __launch_bounds__(kWarps * 32, 3)
 decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
@@ -86,7 +92,7 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   }
   __syncthreads();
 
-  MmaTileWarp<F16> tw;
+  std::conditional_t<NARROW, MmaTileWarpT<F16>, MmaTileWarp<F16>> tw;
   tw.init(a, rq, kv_len, hk, mt, lane);
   const float sl2 = a.scale_log2;
 
@@ -150,13 +156,13 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
     split_merge_if_last(a, rq, hk, mt, mt * 16, min(16, rows_b - mt * 16));
 }
 
-template <int NSTAGE, bool F16>
+template <int NSTAGE, bool F16, bool NARROW>
 int launch_mma(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMap& vmap,
                cudaStream_t stream) {
   const size_t smem = 1024 + (size_t)kWarps * NSTAGE * kStageBytes + kWarps * NSTAGE * 8;
   static_assert(kWarps * 16 * (kMmaCombStride + 2) * 4 <= kWarps * NSTAGE * kStageBytes,
                 "merge buffer does not fit in the stage area");
-  auto kern = decode_mma_kernel<NSTAGE, F16>;
+  auto kern = decode_mma_kernel<NSTAGE, F16, NARROW>;
   static std::atomic<uint64_t> smem_set{0};   // devices whose limit this launcher raised
   cudaError_t e = set_smem_once(kern, (int)smem, smem_set);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_mma)");
@@ -174,8 +180,11 @@ int launch_mma(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMa
 int launch_decode_mma(const pka_plan& plan, const DecodeArgs& args, const CUtensorMap& kmap,
                       const CUtensorMap& vmap, cudaStream_t stream) {
   (void)plan;
-  return args.in_f16 ? launch_mma<2, true>(args, kmap, vmap, stream)
-                     : launch_mma<2, false>(args, kmap, vmap, stream);
+  if (args.rows_per_cta <= 8)   // the transposed tile: keys on the 16-row side
+    return args.in_f16 ? launch_mma<2, true, true>(args, kmap, vmap, stream)
+                       : launch_mma<2, false, true>(args, kmap, vmap, stream);
+  return args.in_f16 ? launch_mma<2, true, false>(args, kmap, vmap, stream)
+                     : launch_mma<2, false, false>(args, kmap, vmap, stream);
 }
 
 }  // namespace pka

@@ -1,4 +1,5 @@
-// One warp's share of the tensor-core decode: a 16-row query tile against a
+// One warp's share of the tensor-core decode: a 16-row query tile (or, with
+// MmaTileWarpT, up to 8 rows on the instruction's narrow side) against a
 // stream of 16-token K/V units staged in shared memory by TMA.
 //
 // Rows of a tile are r = i*group + g (token i of the request, head g of the
@@ -203,6 +204,148 @@ struct MmaTileWarp {
       comb_l[slot * 16 + g4] = lA;
       comb_m[slot * 16 + g4 + 8] = mB;
       comb_l[slot * 16 + g4 + 8] = lB;
+    }
+  }
+};
+
+// The same warp step for a tile of at most 8 query rows, with the two
+// contractions transposed so that the keys fill the 16-row side of
+// m16n8k16 and the query rows its 8-column side:
+//   S^T = K Q^T     (K as the A operand from the unit, Q^T as B fragments in
+//                    registers: 8 mma per unit instead of 16)
+//   O^T += V^T P^T  (V^T via ldmatrix.trans as A, P^T as B: 8 mma, one per 16
+//                    dims, instead of 16)
+// Lane (g4, t4) holds the scores of keys g4 and g4 + 8 for rows 2 t4 and
+// 2 t4 + 1; P^T goes from that C layout to the B layout with one movmatrix
+// transpose per 8 keys.  Row maxima and sums run across the 8 lanes of a t4.
+template <bool F16>
+struct MmaTileWarpT {
+  uint32_t qb[8][2];    // Q^T B fragments, k-step ks
+  float acc[8][4];      // O^T: dims m*16 + g4 (+ 8) x rows 2 t4, 2 t4 + 1
+  float mA, mB, lA, lB; // running max / sum of rows 2 t4 (A) and 2 t4 + 1 (B)
+  int loA, hiA, loB, hiB;
+
+  __device__ __forceinline__ void init(const DecodeArgs& a, const ReqInfo& rq, int kv_len, int hk,
+                                       int tile, int lane) {
+    (void)tile;   // one tile: at most 8 rows
+    const int G = a.group, L = rq.q_len, rows_b = G * L;
+    const int g4 = lane >> 2, t4 = lane & 3;
+    const int rA = 2 * t4, rB = rA + 1;
+    loA = 0; hiA = 0x7fffffff; loB = 0; hiB = 0x7fffffff;
+    if (rA < rows_b) mma_row_key_range(kv_len, L, rA / G, a.causal, a.window_left, loA, hiA);
+    if (rB < rows_b) mma_row_key_range(kv_len, L, rB / G, a.causal, a.window_left, loB, hiB);
+    // B fragment of k-step ks: Q[row g4][dims ks*16 + 2 t4 (+1)] and [.. + 8 (+9)]
+    const uint16_t* qp = static_cast<const uint16_t*>(a.q);
+    const uint16_t* src = nullptr;
+    if (g4 < rows_b)
+      src = qp + (int64_t)(rq.q_start + g4 / G) * a.q_stride_tok +
+            (int64_t)(hk * G + g4 % G) * a.q_stride_head;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int c0 = ks * 16 + t4 * 2;
+      qb[ks][0] = src ? __ldg(reinterpret_cast<const uint32_t*>(src + c0)) : 0u;
+      qb[ks][1] = src ? __ldg(reinterpret_cast<const uint32_t*>(src + c0 + 8)) : 0u;
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+    mA = mB = neg_inf();
+    lA = lB = 0.f;
+  }
+
+  __device__ __forceinline__ void step(uint32_t k_u32, int tok0, bool full_unit, float sl2,
+                                       int lane) {
+    constexpr unsigned FULL = 0xffffffffu;
+    const uint32_t v_u32 = k_u32 + 2 * kMmaBoxBytes;
+    const int g4 = lane >> 2, lm_mat = lane >> 3, lm_row = lane & 7;
+    // S^T = K Q^T: even and odd k-steps in two chains
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t ka[4];
+      // matrices: keys 0-7 / 8-15 (lm_mat & 1) x dims ks*16 + 0-7 / 8-15 (lm_mat >> 1)
+      ldmatrix_x4(k_u32 + mma_unit_chunk_offset((lm_mat & 1) * 8 + lm_row, 2 * ks + (lm_mat >> 1)),
+                  ka[0], ka[1], ka[2], ka[3]);
+      mma_16816<F16>((ks & 1) ? s2 : s, ka, qb[ks][0], qb[ks][1]);
+    }
+    // c: keys g4 (c < 2) or g4 + 8, rows A (even c) or B
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float v = (s[c] + s2[c]) * sl2;
+      if (!full_unit) {
+        const int tok = tok0 + g4 + (c >= 2 ? 8 : 0);
+        const int lo = (c & 1) ? loB : loA, hi = (c & 1) ? hiB : hiA;
+        if (tok < lo || tok >= hi) v = neg_inf();
+      }
+      s[c] = v;
+    }
+    float pmA = fmaxf(s[0], s[2]), pmB = fmaxf(s[1], s[3]);
+    float alA = 1.f, alB = 1.f;
+    if (__any_sync(FULL, pmA > mA + 8.f || pmB > mB + 8.f)) {
+#pragma unroll
+      for (int x = 4; x < 32; x <<= 1) {
+        pmA = fmaxf(pmA, __shfl_xor_sync(FULL, pmA, x));
+        pmB = fmaxf(pmB, __shfl_xor_sync(FULL, pmB, x));
+      }
+      const bool gA = pmA > mA + 8.f, gB = pmB > mB + 8.f;
+      const float mAn = gA ? pmA : mA, mBn = gB ? pmB : mB;
+      if (gA) alA = ex2(mA - mAn);
+      if (gB) alB = ex2(mB - mBn);
+      mA = mAn;
+      mB = mBn;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        acc[m][0] *= alA;
+        acc[m][1] *= alB;
+        acc[m][2] *= alA;
+        acc[m][3] *= alB;
+      }
+    }
+    const float uA = mA == neg_inf() ? 0.f : mA, uB = mB == neg_inf() ? 0.f : mB;
+    const float p0 = ex2(s[0] - uA), p1 = ex2(s[1] - uB), p2 = ex2(s[2] - uA), p3 = ex2(s[3] - uB);
+    lA = lA * alA + (p0 + p2);
+    lB = lB * alB + (p1 + p3);
+    // P^T in C layout (keys x rows) -> B layout (rows g4 x keys 2 t4 ..)
+    const uint32_t b0 = movmatrix_trans(pack2<F16>(p0, p1));
+    const uint32_t b1 = movmatrix_trans(pack2<F16>(p2, p3));
+    // O^T += V^T P^T: one m-tile of 16 dims per mma
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      uint32_t va[4];
+      // matrices: dims m*16 + 0-7 / 8-15 (lm_mat & 1) x keys 0-7 / 8-15 (lm_mat >> 1)
+      ldmatrix_x4_trans(v_u32 + mma_unit_chunk_offset((lm_mat >> 1) * 8 + lm_row, 2 * m + (lm_mat & 1)),
+                        va[0], va[1], va[2], va[3]);
+      mma_16816<F16>(acc[m], va, b0, b1);
+    }
+  }
+
+  // Sums l over the 8 lanes that share a row.
+  __device__ __forceinline__ void reduce_l() {
+    constexpr unsigned FULL = 0xffffffffu;
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+      lA += __shfl_xor_sync(FULL, lA, x);
+      lB += __shfl_xor_sync(FULL, lB, x);
+    }
+  }
+
+  // Writes (O, m, l) of rows 0-7 to merge slot `slot` (layout of store_comb).
+  __device__ __forceinline__ void store_comb(float* comb_o, float* comb_m, float* comb_l, int slot,
+                                             int lane) const {
+    const int g4 = lane >> 2, t4 = lane & 3;
+    float* oA = comb_o + (slot * 16 + 2 * t4) * kMmaCombStride + g4;
+    float* oB = oA + kMmaCombStride;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      oA[m * 16] = acc[m][0];
+      oB[m * 16] = acc[m][1];
+      oA[m * 16 + 8] = acc[m][2];
+      oB[m * 16 + 8] = acc[m][3];
+    }
+    if (g4 == 0) {
+      comb_m[slot * 16 + 2 * t4] = mA;
+      comb_l[slot * 16 + 2 * t4] = lA;
+      comb_m[slot * 16 + 2 * t4 + 1] = mB;
+      comb_l[slot * 16 + 2 * t4 + 1] = lB;
     }
   }
 };
