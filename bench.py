@@ -30,14 +30,15 @@ sys.path.insert(0, ROOT)
 
 HEADLINE = "llama3_8b"
 PREFILL_WINDOW = 2047   # sliding-window variant of the ragged prefill (2048 keys per row)
-# DRAM read + write bytes of one headline decode launch (decode_mma_kernel<2>,
-# seed 0, one GB300): ncu's dram__bytes_read.sum + dram__bytes_write.sum for
-# that launch, captured on this same command (one metric pass, full size).
-# Other seeds or ranks scale it by their algorithmic K+V bytes.
+# DRAM read + write bytes of one headline decode launch (decode_mma_kernel<2>
+# with the transposed step of groups of at most 8 rows, seed 0, one GB300):
+# ncu's dram__bytes_read.sum + dram__bytes_write.sum for that launch, captured
+# on this same command (one metric pass, full size).  Other seeds or ranks
+# scale it by their algorithmic K+V bytes.
 # the kernel symbol each decode plan launches
 KERNEL_SYMBOL = {"cuda_core": "decode_cc_kernel", "mma": "decode_mma_kernel"}
 NCU_TRAFFIC = {"kernel": "decode_mma_kernel", "kv_bytes": 1128361984,
-               "dram_bytes": 1130842880 + 4337152}
+               "dram_bytes": 1130968064 + 4109824}
 METRIC = "paged decode effective KV HBM GB/s"
 UNIT = "GB/s"
 
