@@ -17,7 +17,8 @@
 //  * per unit: S = Q K^T (2 n-tiles x 8 k-steps, Q in A-fragment registers),
 //    mask, online softmax in base 2 on the fragments, P re-packed to 16-bit
 //    A fragments in registers, O += P V (16 n-tiles, V via ldmatrix.trans);
-//    a group of at most 8 rows (NARROW) takes the transposed step instead,
+//    a tile of at most 8 live rows (a group of at most 8 rows, or the last
+//    tile of one of 8 (mod 16)) takes the transposed step instead,
 //    S^T = K Q^T and O^T += V^T P^T, with the 16 keys of a unit on the
 //    16-row side of the instruction and the rows on its 8-column side: half
 //    the mma of a padded 16-row tile;
@@ -26,8 +27,6 @@
 //    the last chunk CTA of each (request, KV head, tile) merges the partials.
 // Decode is bound by HBM, not by the tensor pipe: mma takes the per-key
 // arithmetic of wide groups off the FP32 pipe.
-#include <type_traits>
-
 #include <cuda_bf16.h>
 
 #include "decode_merge.cuh"
@@ -47,6 +46,9 @@ constexpr int kUnit = kMmaUnitTok;
 constexpr int kStageBytes = kMmaUnitBytes;
 constexpr int kBoxBytes = kMmaBoxBytes;
 
+// NARROW: every group has at most 8 rows, and only the transposed step is
+// compiled; otherwise a CTA takes it when its tile has at most 8 live rows
+// (the last tile of a group of 8 (mod 16) rows), else the 16-row step.
 template <int NSTAGE, bool F16, bool NARROW>
 __global__ void __launch_bounds__(kWarps * 32, 3)
 decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
@@ -92,8 +94,6 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
   }
   __syncthreads();
 
-  std::conditional_t<NARROW, MmaTileWarpT<F16>, MmaTileWarp<F16>> tw;
-  tw.init(a, rq, kv_len, hk, mt, lane);
   const float sl2 = a.scale_log2;
 
   // ---- per-warp TMA pipeline over units warp, warp+4, ... ----
@@ -107,7 +107,7 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
     if (k < my_units) return __ldg(trow + (unit0 + warp + k * kWarps) / upp);
     return 0;
   };
-  int tcur = table_batch(0), tnext = table_batch(1), tbatch = 0;
+  int tcur = 0, tnext = 0, tbatch = 0;
   auto issue = [&](int k) {
     if ((k >> 5) > tbatch) {
       tcur = tnext;
@@ -121,32 +121,48 @@ decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ 
     const uint32_t dst = stage_u32 + st * kStageBytes, bar = bar_u32 + st * 8;
     tma_load_kv_pair_elect(dst, dst + 2 * kBoxBytes, &tmk, &tmv, bar, kStageBytes, slot, hk, pid);
   };
-  const int pre = my_units < NSTAGE ? my_units : NSTAGE;
-  for (int k = 0; k < pre; ++k) issue(k);
-
-  int k = 0;
-  for (; k < my_units; ++k) {
-    const int st = k % NSTAGE;
-    if (!__all_sync(FULL, mbar_wait(bar_u32 + st * 8, (uint32_t)((k / NSTAGE) & 1), a.status)))
-      break;
-    const int tok0 = (unit0 + warp + k * kWarps) * kUnit;
-    const bool full_unit = tok0 >= all_lo && tok0 + kUnit <= all_hi;
-    tw.step(stage_u32 + st * kStageBytes, tok0, full_unit, sl2, lane);
-    __syncwarp();
-    if (k + NSTAGE < my_units) issue(k + NSTAGE);
-  }
-  // a wait gave up: let the copies still in flight land (bounded) before the
-  // stages are reused or the CTA exits
-  for (int j = k; j < my_units && j < k + NSTAGE; ++j)
-    (void)mbar_wait(bar_u32 + (j % NSTAGE) * 8, (uint32_t)((j / NSTAGE) & 1), a.status);
-  tw.reduce_l();
-
-  // ---- merge the four warps through shared memory ----
-  __syncthreads();   // every warp is done with its stages
   float* comb_o = reinterpret_cast<float*>(stages);              // [warps][16][kMmaCombStride]
   float* comb_m = comb_o + kWarps * 16 * kMmaCombStride;         // [warps][16]
   float* comb_l = comb_m + kWarps * 16;                          // [warps][16]
-  tw.store_comb(comb_o, comb_m, comb_l, warp, lane);
+
+  // the warp's units through tile step `tw`, then its (m, l, O) into the
+  // merge buffers (which reuse the stages)
+  auto run = [&](auto& tw) {
+    tw.init(a, rq, kv_len, hk, mt, lane);
+    tcur = table_batch(0);
+    tnext = table_batch(1);
+    const int pre = my_units < NSTAGE ? my_units : NSTAGE;
+    for (int k = 0; k < pre; ++k) issue(k);
+
+    int k = 0;
+    for (; k < my_units; ++k) {
+      const int st = k % NSTAGE;
+      if (!__all_sync(FULL, mbar_wait(bar_u32 + st * 8, (uint32_t)((k / NSTAGE) & 1), a.status)))
+        break;
+      const int tok0 = (unit0 + warp + k * kWarps) * kUnit;
+      const bool full_unit = tok0 >= all_lo && tok0 + kUnit <= all_hi;
+      tw.step(stage_u32 + st * kStageBytes, tok0, full_unit, sl2, lane);
+      __syncwarp();
+      if (k + NSTAGE < my_units) issue(k + NSTAGE);
+    }
+    // a wait gave up: let the copies still in flight land (bounded) before the
+    // stages are reused or the CTA exits
+    for (int j = k; j < my_units && j < k + NSTAGE; ++j)
+      (void)mbar_wait(bar_u32 + (j % NSTAGE) * 8, (uint32_t)((j / NSTAGE) & 1), a.status);
+    tw.reduce_l();
+    __syncthreads();   // every warp is done with its stages
+    tw.store_comb(comb_o, comb_m, comb_l, warp, lane);
+  };
+  // a tile of at most 8 live rows takes the transposed step
+  if (NARROW || rows_b - mt * 16 <= 8) {
+    MmaTileWarpT<F16> tw;
+    run(tw);
+  } else {
+    if constexpr (!NARROW) {
+      MmaTileWarp<F16> tw;
+      run(tw);
+    }
+  }
   __syncthreads();
 
   // thread -> (row of the tile, 16 consecutive dims)
@@ -180,7 +196,7 @@ int launch_mma(const DecodeArgs& args, const CUtensorMap& kmap, const CUtensorMa
 int launch_decode_mma(const pka_plan& plan, const DecodeArgs& args, const CUtensorMap& kmap,
                       const CUtensorMap& vmap, cudaStream_t stream) {
   (void)plan;
-  if (args.rows_per_cta <= 8)   // the transposed tile: keys on the 16-row side
+  if (args.rows_per_cta <= 8)   // the transposed step only: keys on the 16-row side
     return args.in_f16 ? launch_mma<2, true, true>(args, kmap, vmap, stream)
                        : launch_mma<2, false, true>(args, kmap, vmap, stream);
   return args.in_f16 ? launch_mma<2, true, false>(args, kmap, vmap, stream)

@@ -227,19 +227,19 @@ struct MmaTileWarpT {
 
   __device__ __forceinline__ void init(const DecodeArgs& a, const ReqInfo& rq, int kv_len, int hk,
                                        int tile, int lane) {
-    (void)tile;   // one tile: at most 8 rows
     const int G = a.group, L = rq.q_len, rows_b = G * L;
     const int g4 = lane >> 2, t4 = lane & 3;
-    const int rA = 2 * t4, rB = rA + 1;
+    const int r0 = tile * 16;   // the tile's first row (its live rows are at most 8)
+    const int rA = r0 + 2 * t4, rB = rA + 1;
     loA = 0; hiA = 0x7fffffff; loB = 0; hiB = 0x7fffffff;
     if (rA < rows_b) mma_row_key_range(kv_len, L, rA / G, a.causal, a.window_left, loA, hiA);
     if (rB < rows_b) mma_row_key_range(kv_len, L, rB / G, a.causal, a.window_left, loB, hiB);
     // B fragment of k-step ks: Q[row g4][dims ks*16 + 2 t4 (+1)] and [.. + 8 (+9)]
     const uint16_t* qp = static_cast<const uint16_t*>(a.q);
     const uint16_t* src = nullptr;
-    if (g4 < rows_b)
-      src = qp + (int64_t)(rq.q_start + g4 / G) * a.q_stride_tok +
-            (int64_t)(hk * G + g4 % G) * a.q_stride_head;
+    if (r0 + g4 < rows_b)
+      src = qp + (int64_t)(rq.q_start + (r0 + g4) / G) * a.q_stride_tok +
+            (int64_t)(hk * G + (r0 + g4) % G) * a.q_stride_head;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const int c0 = ks * 16 + t4 * 2;
@@ -328,7 +328,8 @@ struct MmaTileWarpT {
     }
   }
 
-  // Writes (O, m, l) of rows 0-7 to merge slot `slot` (layout of store_comb).
+  // Writes (O, m, l) of the tile's rows 0-7 to merge slot `slot` (layout of
+  // store_comb).
   __device__ __forceinline__ void store_comb(float* comb_o, float* comb_m, float* comb_l, int slot,
                                              int lane) const {
     const int g4 = lane >> 2, t4 = lane & 3;
