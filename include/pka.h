@@ -443,7 +443,14 @@ int paged_decode_run_noalloc(const pka_plan* plan, const void* q, int64_t q_stri
  *            sum_i 2^(s_i - m) v_i / sum_i 2^(s_i - m), m = max_i s_i.
  * s_out      NULL or fp32 [num_rows, num_heads]: m + log2 sum_i 2^(s_i - m).
  * Rows whose states are all -inf get v = 0 and s = -inf.
- * head_dim must be a multiple of 4 (<= 1024); num_states >= 1.
+ * head_dim must be a multiple of 4 (<= 1024); num_states >= 1; v_states and
+ * v_out 16-byte aligned.  With head_dim 128 the states stream through shared
+ * memory by bulk copies under bounded waits; a wait that gives up (the copies
+ * read only the caller's arrays, so this means a failing device) leaves v_out
+ * and s_out unwritten and sets the timeout bit of the device status word of
+ * the library's fixed scratch, which paged_decode_plan_check on a
+ * PKA_PLAN_HOST_ONLY plan reads.  The first call on a device sets that word
+ * up (one cudaMemsetAsync on `stream`).
  */
 int attn_merge_lse(const float* v_states, const float* s_states, int32_t num_states,
                    int32_t num_rows, int32_t num_heads, int32_t head_dim, void* v_out,

@@ -4,8 +4,10 @@
 // attn_merge_lse: the states are normalised partial outputs over disjoint key
 // subsets with their base-2 LSEs (cudnn_batch_decode_with_kv_cache, Note "LSE
 // convention": the base-2 LSE is what the cascade-merge kernels consume).
-// One warp per (row, head): m = max_i s_i, w_i = 2^(s_i - m),
-// v = sum_i w_i v_i / sum_i w_i, s = m + log2 sum_i w_i.
+// v = sum_i w_i v_i / sum_i w_i and s = m + log2 sum_i w_i with
+// w_i = 2^(s_i - m), m = max_i s_i: head_dim 128 streams the states through
+// shared memory (merge_states_stream_kernel), other head sizes take one warp
+// per (row, head) (merge_states_kernel).
 //
 // paged_kv_gather: copies paged rows into a dense buffer through the decode
 // kernels' own tensor map, unit coordinates and swizzled shared-memory reads,
@@ -53,6 +55,108 @@ merge_states_kernel(const float* __restrict__ v, const float* __restrict__ s, in
     store_out<4>(v_out, idx * d + c, ov, inv, out_dtype);
   }
   if (s_out != nullptr && lane == 0) s_out[idx] = wsum > 0.f ? m + log2f(wsum) : neg_inf();
+}
+
+// The same merge for head_dim 128 as a stream: one CTA takes kMergePairs
+// consecutive (row, head) pairs, and each state's rows of them (32 KB,
+// contiguous in [N, S, H, D]) arrive by one bulk copy into a ring of
+// kMergeStages buffers.  Warp w accumulates pairs 8w .. 8w + 7, lane l their
+// dims 4l .. 4l + 3, with a running maximum per pair: a state whose LSE passes
+// it rescales the sums so far by 2^(m_old - m_new), and every state is weighted
+// 2^(s_i - m).  A wait that gives up sets STATUS_WAIT_TIMEOUT in *status.
+constexpr int kMergePairs = 64, kMergeStages = 3, kMergeD = 128;
+constexpr uint32_t kMergeStageBytes = kMergePairs * kMergeD * 4;
+
+__global__ void __launch_bounds__(256, 2)
+merge_states_stream_kernel(const float* __restrict__ v, const float* __restrict__ s, int n,
+                           int64_t per_state, void* __restrict__ v_out, int out_dtype,
+                           float* __restrict__ s_out, int32_t* status) {
+  constexpr unsigned FULL = 0xffffffffu;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~uintptr_t(127));
+  const float* stages = reinterpret_cast<const float*>(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kMergeStages * kMergeStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t idx0 = (int64_t)blockIdx.x * kMergePairs;
+  const int np = per_state - idx0 < kMergePairs ? (int)(per_state - idx0) : kMergePairs;
+  const uint32_t bytes = (uint32_t)np * kMergeD * 4;
+  const uint32_t stage0 = smem_u32(smem), bar0 = smem_u32(bars);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMergeStages; ++i) mbar_init(bar0 + 8 * i, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int i) {   // state i's rows into stage i % kMergeStages
+    const uint32_t st = (uint32_t)(i % kMergeStages);
+    mbar_arrive_expect_tx(bar0 + 8 * st, bytes);
+    bulk_load(stage0 + st * kMergeStageBytes, v + ((int64_t)i * per_state + idx0) * kMergeD,
+              bytes, bar0 + 8 * st);
+  };
+  int issued = 0;
+  if (threadIdx.x == 0)
+    for (; issued < n && issued < kMergeStages; ++issued) issue(issued);
+
+  const int p0 = warp * 8;   // this warp's first pair
+  float acc[8][4], m[8], l[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    m[j] = neg_inf();
+    l[j] = 0.f;
+  }
+  auto lse_of = [&](int i) -> float {   // lane j < 8: state i's LSE of pair p0 + j
+    return lane < 8 && p0 + lane < np ? __ldg(s + (int64_t)i * per_state + idx0 + p0 + lane)
+                                      : neg_inf();
+  };
+  float lse_next = lse_of(0);
+  int i = 0;
+  for (; i < n; ++i) {
+    const float lse_cur = lse_next;
+    if (i + 1 < n) lse_next = lse_of(i + 1);
+    const uint32_t st = (uint32_t)(i % kMergeStages);
+    const bool ok = mbar_wait(bar0 + 8 * st, (uint32_t)((i / kMergeStages) & 1), status);
+    if (__syncthreads_or(!ok)) break;
+    const float* x = stages + st * (kMergeStageBytes / 4) + p0 * kMergeD + lane * 4;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float sj = __shfl_sync(FULL, lse_cur, j);
+      if (sj == neg_inf()) continue;   // an empty state (or a pair past the end)
+      if (sj > m[j]) {
+        const float sc = ex2(m[j] - sj);   // 0 while m is still -inf
+        acc[j][0] *= sc;
+        acc[j][1] *= sc;
+        acc[j][2] *= sc;
+        acc[j][3] *= sc;
+        l[j] *= sc;
+        m[j] = sj;
+      }
+      const float w = ex2(sj - m[j]);
+      l[j] += w;
+      const float4 xv = *reinterpret_cast<const float4*>(x + j * kMergeD);
+      acc[j][0] += w * xv.x;
+      acc[j][1] += w * xv.y;
+      acc[j][2] += w * xv.z;
+      acc[j][3] += w * xv.w;
+    }
+    __syncthreads();   // every warp is done with this stage
+    if (threadIdx.x == 0 && issued < n) issue(issued++);
+  }
+  if (i < n) {   // a wait gave up: the copies still in flight land (bounded) before exit
+    if (threadIdx.x == 0)
+      for (int j = i; j < issued; ++j)
+        (void)mbar_wait(bar0 + 8 * (uint32_t)(j % kMergeStages),
+                        (uint32_t)((j / kMergeStages) & 1), nullptr);
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (p0 + j >= np) break;
+    const int64_t idx = idx0 + p0 + j;
+    const float inv = l[j] > 0.f ? 1.f / l[j] : 0.f;
+    store_out<4>(v_out, idx * kMergeD + lane * 4, acc[j], inv, out_dtype);
+    if (s_out != nullptr && lane == 0) s_out[idx] = l[j] > 0.f ? m[j] + log2f(l[j]) : neg_inf();
+  }
 }
 
 constexpr int kUnit = 16;
@@ -164,6 +268,21 @@ int launch_merge_states(const float* v_states, const float* s_states, int32_t n,
                         cudaStream_t stream) {
   const int64_t rows = (int64_t)s * h;
   if (rows == 0) return PKA_OK;
+  if (d == kMergeD) {
+    constexpr int smem = kMergeStages * kMergeStageBytes + kMergeStages * 8 + 128;
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = set_smem_once(merge_states_stream_kernel, smem, smem_set);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_states_stream)");
+    int32_t* status = nullptr;
+    const int rc = noalloc_status_word(stream, &status);
+    if (rc != PKA_OK) return rc;
+    const int64_t blocks = (rows + kMergePairs - 1) / kMergePairs;
+    merge_states_stream_kernel<<<(unsigned)blocks, 256, smem, stream>>>(
+        v_states, s_states, n, rows, v_out, out_dtype, s_out, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "merge_states_stream_kernel launch");
+    return PKA_OK;
+  }
   const int64_t blocks = (rows + 7) / 8;
   merge_states_kernel<<<(unsigned)blocks, 256, 0, stream>>>(v_states, s_states, n, s, h, d, v_out,
                                                            out_dtype, s_out);
