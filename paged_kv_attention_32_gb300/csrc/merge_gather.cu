@@ -60,14 +60,17 @@ merge_states_kernel(const float* __restrict__ v, const float* __restrict__ s, in
 // The same merge for head_dim 128 as a stream: one CTA takes kMergePairs
 // consecutive (row, head) pairs, and each state's rows of them (32 KB,
 // contiguous in [N, S, H, D]) arrive by one bulk copy into a ring of
-// kMergeStages buffers.  Warp w accumulates pairs 8w .. 8w + 7, lane l their
+// kMergeStages buffers (two, so that three CTAs fit an SM: measured on GB300
+// against three buffers and two CTAs, and against 16 KB pieces four or six
+// deep).  Warp w accumulates pairs kMergePPW * w onwards, lane l their
 // dims 4l .. 4l + 3, with a running maximum per pair: a state whose LSE passes
 // it rescales the sums so far by 2^(m_old - m_new), and every state is weighted
 // 2^(s_i - m).  A wait that gives up sets STATUS_WAIT_TIMEOUT in *status.
-constexpr int kMergePairs = 64, kMergeStages = 3, kMergeD = 128;
+constexpr int kMergePairs = 64, kMergeStages = 2, kMergeD = 128, kMergeMinBlocks = 3;
+constexpr int kMergePPW = kMergePairs / 8;   // pairs per warp
 constexpr uint32_t kMergeStageBytes = kMergePairs * kMergeD * 4;
 
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, kMergeMinBlocks)
 merge_states_stream_kernel(const float* __restrict__ v, const float* __restrict__ s, int n,
                            int64_t per_state, void* __restrict__ v_out, int out_dtype,
                            float* __restrict__ s_out, int32_t* status) {
@@ -97,16 +100,16 @@ merge_states_stream_kernel(const float* __restrict__ v, const float* __restrict_
   if (threadIdx.x == 0)
     for (; issued < n && issued < kMergeStages; ++issued) issue(issued);
 
-  const int p0 = warp * 8;   // this warp's first pair
-  float acc[8][4], m[8], l[8];
+  const int p0 = warp * kMergePPW;   // this warp's first pair
+  float acc[kMergePPW][4], m[kMergePPW], l[kMergePPW];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < kMergePPW; ++j) {
     acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
     m[j] = neg_inf();
     l[j] = 0.f;
   }
-  auto lse_of = [&](int i) -> float {   // lane j < 8: state i's LSE of pair p0 + j
-    return lane < 8 && p0 + lane < np ? __ldg(s + (int64_t)i * per_state + idx0 + p0 + lane)
+  auto lse_of = [&](int i) -> float {   // lane j < kMergePPW: state i's LSE of pair p0 + j
+    return lane < kMergePPW && p0 + lane < np ? __ldg(s + (int64_t)i * per_state + idx0 + p0 + lane)
                                       : neg_inf();
   };
   float lse_next = lse_of(0);
@@ -119,7 +122,7 @@ merge_states_stream_kernel(const float* __restrict__ v, const float* __restrict_
     if (__syncthreads_or(!ok)) break;
     const float* x = stages + st * (kMergeStageBytes / 4) + p0 * kMergeD + lane * 4;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kMergePPW; ++j) {
       const float sj = __shfl_sync(FULL, lse_cur, j);
       if (sj == neg_inf()) continue;   // an empty state (or a pair past the end)
       if (sj > m[j]) {
@@ -150,7 +153,7 @@ merge_states_stream_kernel(const float* __restrict__ v, const float* __restrict_
     return;
   }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < kMergePPW; ++j) {
     if (p0 + j >= np) break;
     const int64_t idx = idx0 + p0 + j;
     const float inv = l[j] > 0.f ? 1.f / l[j] : 0.f;

@@ -12,7 +12,7 @@ from paged_kv_attention_32_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
-# head_dim 128 streams 64 (row, head) pairs per CTA through a ring of 3 state
+# head_dim 128 streams 64 (row, head) pairs per CTA through a ring of 2 state
 # buffers: cases below, at and past the ring depth, and row counts that leave a
 # partial last block; other head sizes take the warp-per-pair kernel
 @pytest.mark.parametrize("N,S,H,D", [(1, 3, 2, 128), (5, 17, 8, 128), (3, 4, 3, 64), (7, 2, 1, 256),
