@@ -53,9 +53,10 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--workload", default=None,
                     help="profiling: time only this decode workload (llama3_8b, skewed, spec), "
-                         "'prefill' or 'prefill_variable_window'")
+                         "'prefill', 'prefill_variable_window' or 'merge'")
     ap.add_argument("--batch", type=int, default=None,
-                    help="profiling: override the workload's batch size (smaller capture)")
+                    help="profiling: override the workload's batch size (smaller capture; "
+                         "for 'merge', the rows per state)")
     ap.add_argument("--mma-min-rows", type=int, default=0,
                     help="decode plan: rows per KV head from which the mma kernel is used")
     ap.add_argument("--split-waves", type=int, default=0,
@@ -84,6 +85,8 @@ def profile_case(args):
         wl.RAGGED_PREFILL = w
     elif args.workload == "prefill_variable_window":
         r = measure_prefill_fixed(args.seed, args.steps, args.warmup, peak_tf, variable_window=True)
+    elif args.workload == "merge":
+        r = measure_merge(args.seed, args.steps, args.warmup, peak_gbs, rows=args.batch or 8192)
     else:
         w = wl.DECODE_WORKLOADS[args.workload]
         if args.batch:
@@ -563,13 +566,13 @@ def measure_prefill_fixed(seed, steps, warmup, peak_tflops, variable_window=Fals
     return prefill_result(name, ms, flops, peak_tflops, plan.num_tiles, clocks)
 
 
-def measure_merge(seed, steps, warmup, peak_gbs):
-    """Standalone attn_merge_lse: N=8 partial states of S=8192 rows, H=32 heads, D=128
-    (fp32 V [N, S, H, D] and base-2 LSE [N, S, H]) merged into bf16 O and an fp32 LSE.
+def measure_merge(seed, steps, warmup, peak_gbs, rows=8192):
+    """Standalone attn_merge_lse: N=8 partial states of S=8192 rows (`rows`), H=32 heads,
+    D=128 (fp32 V [N, S, H, D] and base-2 LSE [N, S, H]) merged into bf16 O and an fp32 LSE.
     Algorithmic bytes = every partial read once + the outputs written once."""
     import torch
     from paged_kv_attention_32_gb300 import api
-    N, S, H, D = 8, 8192, 32, 128
+    N, S, H, D = 8, rows, 32, 128
     g = torch.Generator(device="cuda").manual_seed(seed + 9)
     vs = torch.randn((N, S, H, D), generator=g, device="cuda", dtype=torch.float32)
     ss = torch.randn((N, S, H), generator=g, device="cuda", dtype=torch.float32)
@@ -590,7 +593,7 @@ def measure_merge(seed, steps, warmup, peak_gbs):
     return {"workload": f"attn_merge_lse N={N} S={S} H={H} D={D} fp32 states -> bf16",
             "ms_per_call": round(ms, 5), "bytes": nbytes, "GB_per_s": round(gbs, 1),
             "frac_of_measured_hbm": round(gbs / peak_gbs, 4),
-            "l2": "inputs (1.07 GB) larger than L2"}
+            "l2": "inputs (%.2f GB) larger than L2" % (vs.numel() * 4 / 1e9)}
 
 
 def _oracle_worker(conn, task):
