@@ -133,6 +133,32 @@ def test_decode_wide_groups(G, L, packed, split):
     assert_close(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("G,L,packed,split", [
+    (3, 7, False, False),   # 21 rows: a 16-row tile and a 5-row tail (tokens 5-6 of the request)
+    (7, 3, False, True),    # 21 rows, split chunks
+    (6, 4, False, False),   # 24 rows: a tail of exactly 8
+    (5, 5, False, False),   # 25 rows: a 9-row tail on the 16-row step
+    (1, 9, False, True),    # 9 rows in one tile
+    (3, 2, False, False),   # 6 rows: the transposed step alone
+    (5, 7, True, True),     # packed 1..7 tokens: 5..35 rows, tails of every size
+])
+def test_decode_tile_tails(G, L, packed, split):
+    """Tiles whose live rows cross token boundaries at every tail size: a tile of at most
+    8 live rows takes the transposed step (the rows' key ranges and their q rows offset by
+    the tile), a wider one the 16-row step."""
+    w = wl.DecodeWorkload(name="tails", batch=6, num_qo_heads=2 * G, num_kv_heads=2,
+                          head_dim=128, page_size=16, kv_len_range=(L, 1200),
+                          q_len_range=(1, L) if packed else (L, L), packed_q=packed, causal=True,
+                          window_left=200 if split else 37, sinks=True)
+    inp = wl.make_decode_inputs(w, seed=31, device=DEV)
+    kw = dict(num_sms=40, split_waves=2, min_chunk_tokens=128) if split else {}
+    out, lse, plan = run_decode(inp, **kw)
+    if split:
+        assert plan.info["num_split"] > 0
+    ref_o, ref_l = oracle_decode(inp)
+    assert_close(out, lse, ref_o, ref_l)
+
+
 @pytest.mark.parametrize("Hq,Hkv,L,packed,split", [
     (128, 1, 1, False, False),   # MQA, 128 heads: 8 tiles per item
     (128, 1, 1, False, True),    #   ... with split chunks and the merge
