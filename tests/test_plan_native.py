@@ -52,6 +52,12 @@ def _cases():
         cases.append(dict(kv=kv, ql=[1] * B, packed=False, Hq=G * 8, Hkv=8, ps=16, W=-1,
                           sms=152, waves=2, mct=mct, frozen=True, causal=False,
                           mma_min_rows=mmr))
+    # equal lengths: the longest-first order keeps tied requests in request order
+    for kv, sms, waves in [([4096] * 40, 152, 2), ([1000, 4096] * 30, 152, 2),
+                           ([5000] * 12, 64, 2), ([300, 300, 9000, 9000, 300] * 4, 16, 4)]:
+        B = len(kv)
+        cases.append(dict(kv=kv, ql=[1] * B, packed=False, Hq=32, Hkv=8, ps=16, W=-1, sms=sms,
+                          waves=waves, mct=256, frozen=True, causal=False, mma_min_rows=1))
     return cases
 
 
