@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 # partial last block; other head sizes take the warp-per-pair kernel
 @pytest.mark.parametrize("N,S,H,D", [(1, 3, 2, 128), (5, 17, 8, 128), (3, 4, 3, 64), (7, 2, 1, 256),
                                      (4, 37, 5, 128), (2, 100, 3, 128), (9, 64, 2, 128),
-                                     (3, 64, 1, 128)])
+                                     (3, 64, 1, 128), (40, 9, 3, 128)])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32, torch.float16])
 def test_merge_matches_oracle(N, S, H, D, out_dtype):
     g = torch.Generator().manual_seed(N * 100 + D)
